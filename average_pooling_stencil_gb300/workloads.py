@@ -1,0 +1,108 @@
+"""The synthetic workloads: input shapes, value distributions, op parameters and
+seeds.  Nothing here computes any part of the ops (output shapes come from the
+library's shape queries on one side and from the oracle on the other).
+
+Each workload mirrors one task traced on the Kimi-K2.6 pages:
+  * ``fused_tiny`` / ``fused``  -- Kimi-K2.6__l2_p50: ConvTranspose3d(3->16, k3, s2,
+    p1) with conv bias, x0.5, AvgPool3d(2), + bias[16,1,1,1], x1.0.
+  * ``avgpool``                 -- Kimi-K2.6__l1_p46: AvgPool3d(k3, s2, p1),
+    count_include_pad, on [16,32,128,128,256].
+  * ``convt1d``                 -- Kimi-K2.6__l1_p74: ConvTranspose1d(32->64, K5,
+    s1, p0, d3), no bias, on [32,32,131072].
+  * ``convt1d_strided``         -- the strided variant (64->64, K4, s2, p1, op1, d2,
+    with bias) that exercises per-parity tap selection.
+Initialiser bounds are the usual 1/sqrt(fan) uniform ones: fan = C_out*prod(k)
+for the transposed-conv weights (432 = 16*27, 320 = 64*5, 256 = 64*4).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+from . import synth
+
+STREAM_X, STREAM_W, STREAM_CONV_BIAS, STREAM_BIAS = 0, 1, 2, 3
+
+
+@dataclass
+class Workload:
+    name: str
+    op: str                      # "ct3d_scale_pool_bias" | "avgpool3d" | "convtranspose1d"
+    seed: int
+    tensors: dict                # name -> (shape, dist, stream)
+    params: dict = field(default_factory=dict)
+
+    def generate(self, name: str, out=None, threads=None):
+        shape, dist, stream = self.tensors[name]
+        return synth.generate(dist, shape, self.seed, stream, out=out, threads=threads)
+
+    def generate_range(self, name: str, start: int, stop: int):
+        shape, dist, stream = self.tensors[name]
+        return synth.generate_range(dist, self.seed, stream, start, stop)
+
+    def numel(self, name: str) -> int:
+        return int(math.prod(self.tensors[name][0]))
+
+    def with_input_shape(self, shape, name: str | None = None) -> "Workload":
+        """Same recipe with a different activation shape (for small parity cases)."""
+        t = dict(self.tensors)
+        s, d, st = t["x"]
+        t["x"] = (tuple(shape), d, st)
+        return Workload(name or f"{self.name}@{'x'.join(map(str, shape))}", self.op,
+                        self.seed, t, dict(self.params))
+
+
+def _u(b):
+    return ("uniform", -b, b)
+
+
+def _fused(name, xshape, seed):
+    b = 1.0 / math.sqrt(432.0)
+    return Workload(
+        name, "ct3d_scale_pool_bias", seed,
+        {
+            "x": (tuple(xshape), ("uniform", -1.0, 1.0), STREAM_X),
+            "w": ((3, 16, 3, 3, 3), _u(b), STREAM_W),
+            "conv_bias": ((16,), _u(b), STREAM_CONV_BIAS),
+            "bias": ((16,), ("normal", 0.02), STREAM_BIAS),
+        },
+        dict(c_out=16, k=(3, 3, 3), stride=(2, 2, 2), pad=(1, 1, 1), out_pad=(0, 0, 0),
+             dil=(1, 1, 1), pool_k=2, scale1=0.5, scale2=1.0),
+    )
+
+
+WORKLOADS = {
+    0: _fused("fused_tiny", (2, 3, 8, 16, 16), 0),
+    1: Workload(
+        "avgpool", "avgpool3d", 1,
+        {"x": ((16, 32, 128, 128, 256), ("normal", 1.0), STREAM_X)},
+        dict(k=(3, 3, 3), stride=(2, 2, 2), pad=(1, 1, 1), count_include_pad=1, ceil_mode=0),
+    ),
+    2: _fused("fused", (128, 3, 16, 32, 32), 2),
+    3: Workload(
+        "convt1d", "convtranspose1d", 3,
+        {
+            "x": ((32, 32, 131072), ("normal", 1.0), STREAM_X),
+            "w": ((32, 64, 5), _u(1.0 / math.sqrt(320.0)), STREAM_W),
+        },
+        dict(c_out=64, k=5, stride=1, pad=0, dil=3, out_pad=0, has_bias=False),
+    ),
+    4: Workload(
+        "convt1d_strided", "convtranspose1d", 4,
+        {
+            "x": ((16, 64, 65536), ("normal", 1.0), STREAM_X),
+            "w": ((64, 64, 4), _u(1.0 / 16.0), STREAM_W),
+            "bias": ((64,), _u(1.0 / 16.0), STREAM_BIAS),
+        },
+        dict(c_out=64, k=4, stride=2, pad=1, dil=2, out_pad=1, has_bias=True),
+    ),
+}
+
+
+def get(cfg) -> Workload:
+    if isinstance(cfg, str):
+        for w in WORKLOADS.values():
+            if w.name == cfg:
+                return w
+        raise KeyError(cfg)
+    return WORKLOADS[int(cfg)]
