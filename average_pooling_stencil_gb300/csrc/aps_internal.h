@@ -1,0 +1,75 @@
+// aps_internal.h -- host-side declarations shared by the library's translation
+// units (not part of the public ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>   // PFN_cuTensorMapEncodeTiled (type only)
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/aps.h"
+
+namespace aps {
+
+// Device address of the current device's status word (see aps_device_status).
+unsigned int *status_word();
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// Resident CTAs per SM of `func` at `threads` threads and `smem` bytes of
+// dynamic shared memory on the current device; raises the kernel's dynamic
+// shared-memory limit to `smem` first.  Cached per (device, kernel, config).
+// Returns 0 if the attribute cannot be set.
+int resident_ctas(const void *func, int threads, int smem);
+
+// cuTensorMapEncodeTiled obtained through the runtime's driver entry point
+// (no link-time dependency on libcuda).  Returns false if unavailable.
+bool encode_tiled(CUtensorMap *map, CUtensorMapDataType type, uint32_t rank, void *base,
+                  const cuuint64_t *dims, const cuuint64_t *strides_bytes,
+                  const cuuint32_t *box, const cuuint32_t *elem_strides);
+
+// Maps the last CUDA launch error to APS_OK / APS_ERR_LAUNCH.
+aps_status launch_status();
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ------------------------------------------------------------ launchers
+// Each launcher assumes validated arguments and a non-empty output.
+
+// AvgPool3d k3/s2/p1, count_include_pad, floor mode; W % 4 == 0, x 16-byte and
+// y 8-byte aligned.  Returns APS_ERR_UNSUPPORTED if the tensor map cannot be
+// built (the caller then uses the direct kernel).
+aps_status launch_avgpool3d_k3s2p1_tma(const float *x, const int64_t in[5], float *y,
+                                       const int64_t out[5], cudaStream_t st);
+
+aps_status launch_avgpool3d_direct(const float *x, const int64_t in[5], const int k[3],
+                                   const int s[3], const int p[3], int count_include_pad,
+                                   float *y, const int64_t out[5], cudaStream_t st);
+
+// Fused transposed conv (k3 s2 p1, pool 2, C_out = 16, C_in <= 8).  Returns
+// APS_ERR_UNSUPPORTED when the tile does not fit (the caller then uses the
+// direct kernel).
+aps_status launch_ct3d_pool2_fast(const float *x, const int64_t in[5], const float *w,
+                                  const float *conv_bias, const float *bias, float scale1,
+                                  float scale2, float *y, const int64_t out[5],
+                                  cudaStream_t st);
+
+aps_status launch_ct3d_pool_direct(const float *x, const int64_t in[5], const float *w,
+                                   const float *conv_bias, const float *bias, int64_t c_out,
+                                   const int k[3], const int s[3], const int p[3],
+                                   const int d[3], int pool_k, float scale1, float scale2,
+                                   float *y, const int64_t out[5], cudaStream_t st);
+
+// ConvTranspose1d, fp32.  The tiled kernel covers the (stride, taps,
+// dilation, padding mod stride) combinations compiled in and C_out % 8 == 0;
+// it returns APS_ERR_UNSUPPORTED otherwise.
+aps_status launch_convt1d_tiled(const float *x, const int64_t in[3], const float *w,
+                                const float *bias, int64_t c_out, int k, int s, int p,
+                                int d, float *y, int64_t l_out, cudaStream_t st);
+
+aps_status launch_convt1d_direct(const float *x, const int64_t in[3], const float *w,
+                                 const float *bias, int64_t c_out, int k, int s, int p,
+                                 int d, float *y, int64_t l_out, cudaStream_t st);
+
+}  // namespace aps

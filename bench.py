@@ -1,0 +1,560 @@
+#!/usr/bin/env python
+"""Benchmark of the stencil library on one GB300 (or N replicas under torchrun).
+
+Headline workload: AvgPool3d(k3, s2, p1, count_include_pad) on x fp32
+[16,32,128,128,256] (the Kimi-K2.6__l1_p46 task).  A step is one pass of the
+op over one batch; `value` is outputs/s of the whole job with the input
+resident in HBM (8.59 GB, larger than L2, so no flush is needed).  The line
+also carries:
+  * roofline -- algorithmic bytes per launch (input read once + output written
+    once) / the kernel's average CUDA-event duration on its launch stream,
+    against the measured copy bandwidth in MEASURED_PEAKS.json;
+  * e2e -- the same metric through the C ABI with host buffers: every step
+    copies the input from pinned host memory, runs the op and reads the output
+    back, all inside the timed region;
+  * cpu_baseline -- the fp64 oracle on the host cores, on a bounded sample of
+    (n, c) planes of the same workload;
+  * clocks -- nvidia-smi samples taken during the timed region;
+  * per_config -- the other four workloads (fused op tiny / full size, the two
+    ConvTranspose1d workloads) with outputs/s and their own roofline fraction.
+
+`--impl reference` times the oracle itself (the only other leg that runs
+oracle code) on the same workload and prints the same line shape.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "outputs/s and % of binding roofline (HBM GB/s or FP32/TF32 FLOP/s) per config"
+HEADLINE_CFG = 1
+SMS = 152
+FP32_LANES_PER_SM = 128
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--no-per-config", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------- helpers
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "sm_max_mhz": 2070.0}, "fallback"
+
+
+def fp32_peak_tflops(mhz):
+    """FP32 FMA peak: 152 SMs x 128 lanes x 2 FLOP per clock."""
+    return SMS * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+
+
+def numel(shape):
+    return int(math.prod(shape))
+
+
+def convt_pairs(L, L_out, K, s, p, d):
+    """Number of (i, k) pairs whose output index i*s - p + k*d lands in range
+    (the in-range taps of a transposed convolution, per channel pair)."""
+    n = 0
+    for k in range(K):
+        lo = max(0, -((k * d - p) // s))          # ceil((p - k*d) / s)
+        hi = min(L - 1, (L_out - 1 + p - k * d) // s)
+        n += max(0, hi - lo + 1)
+    return n
+
+
+class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons, in the background."""
+    FIELDS = ["timestamp", "clocks.sm", "clocks.max.sm", "power.draw",
+              "clocks_event_reasons.active", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, index, interval_ms=100):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", str(interval_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == len(self.FIELDS):
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        sel = [p for (t, p) in self.samples if t0 <= t <= t1 + 0.15]
+        if not sel:
+            sel = [p for (_, p) in self.samples[-3:]]
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+        mhz = [float(p[1]) for p in sel if re.match(r"^[\d.]+$", p[1])]
+        mx = [float(p[2]) for p in sel if re.match(r"^[\d.]+$", p[2])]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in sel for i in range(4) if p[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(mhz) if mhz else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(sel)}
+
+
+def traffic_from_profile(kernel_file, profile_name):
+    """Per-launch DRAM bytes recorded in profiles/<profile_name> for the kernel
+    source whose sha256 prefix is recorded beside it; None if absent or stale."""
+    prof = os.path.join(ROOT, "profiles", profile_name)
+    src = os.path.join(ROOT, "average_pooling_stencil_gb300", "csrc", kernel_file)
+    if not (os.path.exists(prof) and os.path.exists(src)):
+        return None
+    text = open(prof).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", text)
+    if not (m and h):
+        return None
+    cur = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return float(m.group(1)) if cur == h.group(1) else None
+
+
+# --------------------------------------------------------------- workloads
+def workload_desc(wl):
+    shp = "x".join(map(str, wl.tensors["x"][0]))
+    p = wl.params
+    if wl.op == "avgpool3d":
+        return f"avgpool3d k3 s2 p1 count_include_pad x[{shp}] fp32"
+    if wl.op == "ct3d_scale_pool_bias":
+        return (f"convtranspose3d(k3,s2,p1)+x{p['scale1']}+avgpool3d(2)+bias+x{p['scale2']} "
+                f"x[{shp}] fp32")
+    return (f"convtranspose1d K{p['k']} s{p['stride']} p{p['pad']} d{p['dil']} "
+            f"op{p['out_pad']} x[{shp}] -> C_out {p['c_out']} fp32")
+
+
+class GpuCase:
+    """Device-resident inputs/outputs of one workload plus its launch closure."""
+
+    def __init__(self, cfg, torch, aps, with_host=False):
+        from average_pooling_stencil_gb300 import workloads
+        self.cfg = cfg
+        self.wl = wl = workloads.get(cfg)
+        self.torch = torch
+        p = wl.params
+        dev = torch.device("cuda")
+        names = [n for n in ("x", "w", "conv_bias", "bias") if n in wl.tensors]
+        self.host = {}
+        self.d = {}
+        for n in names:
+            shape = wl.tensors[n][0]
+            pin = with_host and n == "x"
+            h = torch.empty(shape, dtype=torch.float32, pin_memory=pin)
+            wl.generate(n, out=h.numpy())
+            self.host[n] = h
+            self.d[n] = h.to(dev, non_blocking=False)
+        x = self.d["x"]
+        if wl.op == "avgpool3d":
+            st, oshape = aps.binding.aps_avgpool3d_out_shape(x.shape, p["k"], p["stride"],
+                                                             p["pad"], p["ceil_mode"])
+            self.flops = 27 * numel(oshape)
+            self.bound = "hbm"
+        elif wl.op == "ct3d_scale_pool_bias":
+            st, oshape = aps.binding.aps_ct3d_scale_pool_bias_out_shape(
+                x.shape, p["c_out"], p["k"], p["stride"], p["pad"], p["out_pad"], p["dil"],
+                p["pool_k"])
+            self.flops = 2 * 8 * x.shape[1] * numel(oshape)   # 8 collapsed taps per ci
+            self.bound = "hbm+alu"
+        else:
+            st, oshape = aps.binding.aps_convtranspose1d_out_shape(
+                x.shape, p["c_out"], p["k"], p["stride"], p["pad"], p["dil"], p["out_pad"])
+            pairs = convt_pairs(x.shape[2], oshape[2], p["k"], p["stride"], p["pad"], p["dil"])
+            self.flops = 2 * x.shape[0] * x.shape[1] * p["c_out"] * pairs
+            self.bound = "alu"
+        assert st == 0
+        self.oshape = oshape
+        self.y = torch.empty(oshape, device=dev, dtype=torch.float32)
+        self.bytes = 4 * (sum(numel(t.shape) for t in self.d.values()) + numel(oshape))
+        self.outputs = numel(oshape)
+        self.aps = aps
+        self.stream = torch.cuda.current_stream()
+        if with_host:
+            self.yh = torch.empty(oshape, dtype=torch.float32, pin_memory=True)
+
+    def launch(self):
+        B = self.aps.binding
+        p = self.wl.params
+        d = self.d
+        s = self.stream.cuda_stream
+        if self.wl.op == "avgpool3d":
+            st = B.aps_avgpool3d(d["x"].data_ptr(), d["x"].shape, p["k"], p["stride"], p["pad"],
+                                 p["count_include_pad"], p["ceil_mode"], self.y.data_ptr(), s)
+        elif self.wl.op == "ct3d_scale_pool_bias":
+            st = B.aps_ct3d_scale_pool_bias(
+                d["x"].data_ptr(), d["x"].shape, d["w"].data_ptr(), d["conv_bias"].data_ptr(),
+                d["bias"].data_ptr(), p["c_out"], p["k"], p["stride"], p["pad"], p["out_pad"],
+                p["dil"], p["pool_k"], p["scale1"], p["scale2"], self.y.data_ptr(), s)
+        else:
+            bias = d["bias"].data_ptr() if "bias" in d else 0
+            st = B.aps_convtranspose1d(d["x"].data_ptr(), d["x"].shape, d["w"].data_ptr(), bias,
+                                       p["c_out"], p["k"], p["stride"], p["pad"], p["dil"],
+                                       p["out_pad"], B.APS_PREC_FP32, self.y.data_ptr(), s)
+        if st != 0:
+            raise RuntimeError(f"launch failed: {B.status_string(st)}")
+
+    def e2e_step(self):
+        """Host x -> device, op, device y -> host, on the launch stream."""
+        self.d["x"].copy_(self.host["x"], non_blocking=True)
+        self.launch()
+        self.yh.copy_(self.y, non_blocking=True)
+
+
+def time_launches(torch, case, reps, flush=None):
+    """Average device time of one launch (CUDA events on the launch stream)."""
+    st = case.stream
+    if flush is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(reps):
+            case.launch()
+        e1.record(st)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / reps
+    tot = 0.0
+    for _ in range(reps):
+        flush.add_(1.0)   # a write larger than L2 between launches, outside the events
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        case.launch()
+        e1.record(st)
+        e1.synchronize()
+        tot += e0.elapsed_time(e1) / 1e3
+    return tot / reps
+
+
+def time_graph(torch, case, per_graph=100, reps=20):
+    """Launch-latency-bound workload: average launch time inside a CUDA graph."""
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        case.stream = s
+        case.launch()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(per_graph):
+                case.launch()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        g.replay()
+        e0.record(s)
+        for _ in range(reps):
+            g.replay()
+        e1.record(s)
+    e1.synchronize()
+    case.stream = torch.cuda.current_stream()
+    return e0.elapsed_time(e1) / 1e3 / (reps * per_graph)
+
+
+def roofline_for(case, t, peaks, src, clock_mhz):
+    hbm = float(peaks["hbm_gbs"])
+    gbs = case.bytes / t / 1e9
+    tfl = case.flops / t / 1e12
+    fp32 = fp32_peak_tflops(float(peaks.get("sm_max_mhz", 2070.0)))
+    if case.bound == "hbm":
+        return {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                "peak_source": src}
+    if case.bound == "alu":
+        return {"bound": "alu", "achieved": tfl, "peak": fp32, "unit": "TFLOP/s",
+                "frac": tfl / fp32,
+                "peak_source": "152 SMs x 128 FP32 lanes x 2 FLOP x max SM clock "
+                               f"{peaks.get('sm_max_mhz', 2070.0)} MHz"}
+    floor = max(case.bytes / (hbm * 1e9), case.flops / (fp32 * 1e12))
+    return {"bound": "hbm" if case.bytes / (hbm * 1e9) >= case.flops / (fp32 * 1e12) else "alu",
+            "achieved": gbs, "unit": "GB/s", "peak": hbm, "frac": floor / t,
+            "achieved_tflops": tfl, "peak_tflops": fp32,
+            "note": "frac = max(HBM floor, FP32 floor) / measured time", "peak_source": src}
+
+
+# ------------------------------------------------------------------ oracle
+def oracle_sample(cfg, seconds):
+    """Time the oracle on a bounded sample of (n, c) planes of workload `cfg`.
+    Returns (outputs per second, threads, description, outputs, seconds)."""
+    import numpy as np
+
+    import oracle
+    from average_pooling_stencil_gb300 import workloads
+    wl = workloads.get(cfg)
+    p = wl.params
+    xs = wl.tensors["x"][0]
+    N, C = xs[0], xs[1]
+    plane = numel(xs[2:])
+    threads = oracle.threads()
+    tens = {n: wl.generate(n) for n in wl.tensors if n != "x"}
+    if wl.op == "avgpool3d":
+        def run(ns, planes):
+            xb = np.stack([wl.generate_range("x", (n * C + c) * plane, (n * C + c + 1) * plane)
+                           .reshape(xs[2:]) for (n, c) in planes])[:, None]
+            t0 = time.perf_counter()
+            y = oracle.avgpool3d(xb, p["k"], p["stride"], p["pad"], p["count_include_pad"],
+                                 p["ceil_mode"])
+            return time.perf_counter() - t0, y.size
+        units = [(n, c) for n in range(N) for c in range(C)]
+    else:
+        cout = p["c_out"]
+        xfull = {}
+
+        def xrow(n):
+            if n not in xfull:
+                xfull[n] = wl.generate_range("x", n * C * plane, (n + 1) * C * plane).reshape(
+                    (1, C) + tuple(xs[2:]))
+            return xfull[n]
+
+        def run(ns, planes):
+            tot, cnt = 0.0, 0
+            for n in sorted({q[0] for q in planes}):
+                sel = [(0, co) for (m, co) in planes if m == n]
+                xb = xrow(n)
+                t0 = time.perf_counter()
+                if wl.op == "ct3d_scale_pool_bias":
+                    y = oracle.ct3d_scale_pool_bias(xb, tens["w"], tens["conv_bias"], tens["bias"],
+                                                    p["stride"], p["pad"], p["out_pad"], p["dil"],
+                                                    p["pool_k"], p["scale1"], p["scale2"], sel=sel)
+                else:
+                    y = oracle.convt(xb, tens["w"], tens.get("bias"), p["stride"], p["pad"],
+                                     p["dil"], p["out_pad"], sel=sel)
+                tot += time.perf_counter() - t0
+                cnt += y.size
+            return tot, cnt
+        units = [(n, co) for n in range(N) for co in range(cout)]
+    # calibrate on one batch of `threads` planes, then size the sample
+    k = min(len(units), max(1, threads))
+    t, cnt = run(None, units[:k])
+    per_plane = t / k
+    m = int(min(len(units), max(k, round(seconds / max(per_plane, 1e-6)))))
+    step = max(1, len(units) // m)
+    sample = units[::step][:m]
+    t, cnt = run(None, sample)
+    desc = f"{len(sample)} of {len(units)} (n, c) output planes of {workload_desc(wl)}"
+    return cnt / t, threads, desc, cnt, t
+
+
+# ------------------------------------------------------------------- legs
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    from average_pooling_stencil_gb300 import workloads
+    wl = workloads.get(HEADLINE_CFG)
+    oracle.build()
+    per_step = max(1.0, min(args.cpu_seconds, 60.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(HEADLINE_CFG, per_step)
+    vals, times, desc, threads = [], [], "", 1
+    for _ in range(args.steps):
+        v, threads, desc, cnt, t = oracle_sample(HEADLINE_CFG, per_step)
+        vals.append(v)
+        times.append(t)
+    value = sum(times) and sum(v * t for v, t in zip(vals, times)) / sum(times)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "outputs/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.mean(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(wl), "seed": wl.seed, "l2": "n/a (host)"},
+        "cpu_baseline": {"value": value, "unit": "outputs/s", "cores": threads, "kind": "oracle",
+                         "sample": f"per step: {desc}"},
+        "e2e": {"value": value, "unit": "outputs/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def run_native(args):
+    import torch
+
+    import average_pooling_stencil_gb300 as aps
+    from average_pooling_stencil_gb300 import build as aps_build
+    ws, rank, local = dist_env()
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    aps_build.build()
+    peaks, peak_src = load_peaks()
+    dev_index = local if ws > 1 else 0
+
+    def barrier():
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---- headline: each rank runs its own full workload (weak scaling)
+    case = GpuCase(HEADLINE_CFG, torch, aps, with_host=True)
+    for _ in range(max(3, args.warmup)):
+        case.launch()
+    barrier()
+    sampler = ClockSampler(dev_index, 50)
+    time.sleep(0.6)   # nvidia-smi start-up
+    st = case.stream
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    t_wall0 = time.time()
+    e0.record(st)
+    for _ in range(args.steps):
+        case.launch()
+    e1.record(st)
+    barrier()
+    t_wall1 = time.time()
+    sampler.stop()
+    t_dev = e0.elapsed_time(e1) / 1e3
+    t_max = t_dev
+    if dist:
+        tt = torch.tensor([t_dev], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_max = float(tt.item())
+    per_launch = t_dev / args.steps
+    value = ws * case.outputs * args.steps / t_max
+
+    # ---- e2e through the ABI with host buffers
+    for _ in range(2):
+        case.e2e_step()
+    barrier()
+    e2e_steps = max(1, args.e2e_steps)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(st)
+    for _ in range(e2e_steps):
+        case.e2e_step()
+    f1.record(st)
+    barrier()
+    t_e2e = f0.elapsed_time(f1) / 1e3
+    if dist:
+        tt = torch.tensor([t_e2e], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_e2e = float(tt.item())
+    e2e = {"value": ws * case.outputs * e2e_steps / t_e2e, "unit": "outputs/s",
+           "h2d_bytes_per_step": 4 * numel(case.host["x"].shape),
+           "d2h_bytes_per_step": 4 * case.outputs, "steps": e2e_steps,
+           "ms_per_step": 1e3 * t_e2e / e2e_steps}
+
+    clocks = sampler.summary(t_wall0, t_wall1)
+    roof = roofline_for(case, per_launch, peaks, peak_src, clocks.get("sm_mhz"))
+    roof["traffic"] = traffic_from_profile("avgpool3d.cu", "avgpool3d_k3s2p1_tma.md")
+    roof["algorithmic_bytes_per_launch"] = case.bytes
+    roof["kernel"] = "avgpool3d_k3s2p1_tma_kernel"
+
+    st_code, bits = aps.binding.aps_device_status(clear=True)
+    if st_code != 0 or bits != 0:
+        raise RuntimeError(f"device status {st_code} bits {bits}")
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "outputs/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_max / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": workload_desc(case.wl), "seed": case.wl.seed,
+                   "l2": "inputs larger than L2 (8.59 GB input per step), no flush",
+                   "parallelism": f"replicas{ws}" if ws > 1 else "single GPU"},
+        "roofline": roof, "e2e": e2e, "gpu_launches": args.steps, "clocks": clocks,
+    }
+    del case
+    torch.cuda.empty_cache()
+
+    # ---- per-config breakdown (rank 0)
+    if rank == 0 and not args.no_per_config:
+        per = {}
+        flush = torch.empty(64 * 1024 * 1024, device="cuda")   # 256 MB > L2
+        for cfg in (0, 2, 3, 4):
+            c = GpuCase(cfg, torch, aps)
+            for _ in range(3):
+                c.launch()
+            torch.cuda.synchronize()
+            if cfg == 0:
+                t = time_graph(torch, c)
+                how = "CUDA graph of 100 launches x 20 replays (launch-latency bound)"
+            elif cfg == 2:
+                t = time_launches(torch, c, 30, flush)
+                how = "30 launches, 256 MB L2 flush before each, events per launch"
+            else:
+                t = time_launches(torch, c, 20)
+                how = "20 back-to-back launches (input larger than L2)"
+            per[c.wl.name] = {
+                "workload": workload_desc(c.wl), "outputs_per_s": c.outputs / t,
+                "us_per_launch": 1e6 * t, "gb_per_s": c.bytes / t / 1e9,
+                "tflop_per_s": c.flops / t / 1e12, "algorithmic_bytes": c.bytes,
+                "algorithmic_flops": c.flops,
+                "roofline": roofline_for(c, t, peaks, peak_src, None), "timing": how}
+            del c
+            torch.cuda.empty_cache()
+        line["per_config"] = per
+
+    # ---- CPU baseline: the oracle on the host cores (rank 0, N = 1 only)
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        v, threads, desc, cnt, t = oracle_sample(HEADLINE_CFG, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": "outputs/s", "cores": threads,
+                                "kind": "oracle", "sample": desc, "seconds": t}
+    if rank == 0:
+        print(json.dumps(line))
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_native(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,171 @@
+/*
+ * aps.h -- C ABI of the average_pooling_stencil GB300 library (libaps.so).
+ *
+ * Three fp32 stencil ops on contiguous NC(D)HW / NCL tensors, each computed by
+ * hand-written CUDA kernels for sm_103a:
+ *
+ *   aps_ct3d_scale_pool_bias  ConvTranspose3d -> x scale1 -> AvgPool3d(pool_k)
+ *                             -> + bias[c] -> x scale2, fused so that the
+ *                             pre-pool tensor is never written
+ *                             (page Kimi-K2.6__l2_p50, the fused model and its
+ *                             27-term / 8-neighbour decomposition).
+ *   aps_avgpool3d             AvgPool3d with zero padding
+ *                             (page Kimi-K2.6__l1_p46: kernel 3, stride 2,
+ *                             padding 1, count_include_pad, divisor 27).
+ *   aps_convtranspose1d       ConvTranspose1d with stride, padding, dilation
+ *                             and output padding
+ *                             (page Kimi-K2.6__l1_p74: the gather formula
+ *                             y[o] = sum_k x[(o + p - d*k)/s] * w[k], taken only
+ *                             where the quotient is an integer in range).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensors are fp32, dense, C-contiguous.  Activations are [N, C, D, H, W]
+ *    (3-D) or [N, C, L] (1-D).  Transposed-convolution weights are
+ *    [C_in, C_out, k...] (the PyTorch ConvTranspose layout); biases are [C_out].
+ *  - Shapes are passed as int64 arrays; kernel sizes, strides, paddings,
+ *    dilations and output paddings as int arrays (one entry per spatial dim).
+ *  - Output sizes: transposed convolution (L - 1)*s - 2p + d*(k - 1) + op + 1;
+ *    pooling floor((L + 2p - k)/s) + 1 (ceil mode: ceil instead of floor, and a
+ *    last window that would start inside the right padding is dropped).
+ *  - All tensor pointers are DEVICE pointers on the current CUDA device.  The
+ *    caller owns all memory: the library never allocates, frees or
+ *    synchronises.  Outputs must not overlap inputs.  Pointers must be at
+ *    least 4-byte aligned; 16-byte alignment (plus the shape conditions stated
+ *    per op) selects the fastest kernels, never changes results beyond the
+ *    stated tolerance, and is not required.
+ *  - Launches are asynchronous and ordered on `stream` (a cudaStream_t; NULL is
+ *    the legacy default stream).  A status other than APS_OK means nothing
+ *    was launched, except APS_ERR_LAUNCH, which reports the error the CUDA
+ *    runtime gave for the launch itself.  A tensor with zero elements (N or C
+ *    equal to 0) is valid: the call returns APS_OK and launches nothing.
+ *  - Shape queries are pure host functions; they need no GPU and no CUDA
+ *    context.
+ *  - Kernels contain no unbounded waits.  A pipeline wait that exceeds its
+ *    time limit makes the kernel stop early and record APS_DEVERR_TIMEOUT in a
+ *    per-device status word read by aps_device_status().
+ */
+#ifndef APS_H
+#define APS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared without CUDA headers. */
+struct CUstream_st;
+typedef struct CUstream_st *aps_stream_t;
+
+typedef enum {
+    APS_OK = 0,
+    APS_ERR_NULL = -1,        /* a required pointer or shape array is NULL */
+    APS_ERR_SHAPE = -2,       /* a dimension or parameter is out of range, or
+                                 the output would be empty in a spatial dim */
+    APS_ERR_UNSUPPORTED = -3, /* a valid request no kernel here implements */
+    APS_ERR_ALIGN = -4,       /* a tensor pointer is not 4-byte aligned */
+    APS_ERR_LAUNCH = -5,      /* the CUDA runtime rejected the launch */
+    APS_ERR_CUDA = -6         /* another CUDA runtime call failed */
+} aps_status;
+
+/* Bits of the per-device status word (see aps_device_status). */
+#define APS_DEVERR_TIMEOUT 1u
+
+/* Precision choices of aps_convtranspose1d. */
+#define APS_PREC_FP32 0   /* fp32 FMA; max |y - exact| <= 1e-5 * (1 + |exact|) */
+#define APS_PREC_TF32 1   /* tcgen05 tensor cores, tf32 operands, fp32 accumulate;
+                             ||y - exact||_F <= 5e-3 * ||exact||_F */
+
+/* Version of this ABI (bumped on any incompatible change). */
+int aps_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *aps_status_string(int status);
+
+/* ---------------------------------------------------------------- avgpool3d
+ * y[n,c,i,j,l] = (1/div) * sum over the kD x kH x kW window starting at
+ * (i*sD - pD, j*sH - pH, l*sW - pW) of x, cells outside the input counting as
+ * zero.  div = kD*kH*kW when count_include_pad is non-zero (the window clipped
+ * at the end of the right padding in ceil mode), otherwise the number of
+ * window cells inside the input.  Kimi-K2.6__l1_p46 fixes k = 3, s = 2, p = 1,
+ * count_include_pad, floor mode, where the divisor is always 27.
+ *
+ * x: [N, C, D, H, W] device fp32.  y: [N, C, Do, Ho, Wo] device fp32 (shape
+ * from aps_avgpool3d_out_shape).  Requires k >= 1, s >= 1, 0 <= 2p <= k.
+ * Fast path: k = 3, s = 2, p = 1 in all dims, count_include_pad, floor mode,
+ * W % 4 == 0, x 16-byte and y 8-byte aligned (TMA-tiled kernel); every other
+ * valid request runs a direct-window kernel.
+ */
+aps_status aps_avgpool3d_out_shape(const int64_t in_ncdhw[5], const int k[3],
+                                   const int stride[3], const int pad[3],
+                                   int ceil_mode, int64_t out_ncdhw[5]);
+
+aps_status aps_avgpool3d(const float *x, const int64_t in_ncdhw[5], const int k[3],
+                         const int stride[3], const int pad[3], int count_include_pad,
+                         int ceil_mode, float *y, aps_stream_t stream);
+
+/* ----------------------------------------------------- ct3d_scale_pool_bias
+ * y = ((AvgPool3d_q(convT3d(x, w) + conv_bias) * scale1) + bias[c]) * scale2,
+ * written in the order of Kimi-K2.6__l2_p50's model: transposed convolution
+ * with conv_bias, multiply by scale1, average pool with kernel = stride =
+ * pool_k (no padding, floor mode), add bias[c], multiply by scale2.  Only the
+ * pooled result is written.
+ *
+ * x: [N, C_in, D, H, W]; w: [C_in, C_out, kD, kH, kW]; conv_bias: [C_out] or
+ * NULL (treated as zeros); bias: [C_out]; y: [N, C_out, Do, Ho, Wo] (shape from
+ * aps_ct3d_scale_pool_bias_out_shape).  Requires k, s, dil >= 1, pad >= 0,
+ * 0 <= out_pad < max(s, dil), pool_k >= 1.
+ * Fast path: k = 3, s = 2, p = 1, out_pad = 0, dil = 1, pool_k = 2, C_out = 16,
+ * 1 <= C_in <= 8: the pooled output then equals a 2x2x2 valid correlation of x
+ * with 8 collapsed weights per (ci, co) plus a folded bias (the page's
+ * grouping of the 27 taps by input neighbour), computed in one kernel whose
+ * CTAs collapse the weights themselves.  Every other valid geometry runs a
+ * direct per-output kernel.
+ */
+aps_status aps_ct3d_scale_pool_bias_out_shape(const int64_t in_ncdhw[5], int64_t c_out,
+                                              const int k[3], const int stride[3],
+                                              const int pad[3], const int out_pad[3],
+                                              const int dil[3], int pool_k,
+                                              int64_t out_ncdhw[5]);
+
+aps_status aps_ct3d_scale_pool_bias(const float *x, const int64_t in_ncdhw[5],
+                                    const float *w, const float *conv_bias,
+                                    const float *bias, int64_t c_out, const int k[3],
+                                    const int stride[3], const int pad[3],
+                                    const int out_pad[3], const int dil[3], int pool_k,
+                                    float scale1, float scale2, float *y,
+                                    aps_stream_t stream);
+
+/* -------------------------------------------------------- convtranspose1d
+ * y[n,co,o] = bias[co] + sum_ci sum_k w[ci,co,k] * x[n,ci,(o + p - d*k)/s], each
+ * term taken only when o + p - d*k is a multiple of s and the quotient lies in
+ * [0, L) (Kimi-K2.6__l1_p74's gather formula; weights are NOT flipped).
+ *
+ * x: [N, C_in, L]; w: [C_in, C_out, K]; bias: [C_out] or NULL (no bias);
+ * y: [N, C_out, L_out] (shape from aps_convtranspose1d_out_shape).  Requires
+ * K, s, d >= 1, p >= 0, 0 <= out_pad < max(s, d).  precision: APS_PREC_FP32 or
+ * APS_PREC_TF32 (tolerances above); APS_PREC_TF32 needs C_in % 8 == 0,
+ * C_out % 16 == 0 and C_out <= 256, otherwise APS_ERR_UNSUPPORTED.
+ */
+aps_status aps_convtranspose1d_out_shape(const int64_t in_ncl[3], int64_t c_out, int k,
+                                         int stride, int pad, int dil, int out_pad,
+                                         int64_t out_ncl[3]);
+
+aps_status aps_convtranspose1d(const float *x, const int64_t in_ncl[3], const float *w,
+                               const float *bias, int64_t c_out, int k, int stride,
+                               int pad, int dil, int out_pad, int precision, float *y,
+                               aps_stream_t stream);
+
+/* ------------------------------------------------------------ diagnostics
+ * Reads (and, if clear != 0, resets) the status word of the current device:
+ * a bitwise OR of APS_DEVERR_* recorded by kernels since the last reset.
+ * Synchronous: it waits for all prior work on the device.
+ */
+aps_status aps_device_status(unsigned int *bits, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* APS_H */

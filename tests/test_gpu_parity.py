@@ -1,0 +1,228 @@
+"""CUDA path (through the C ABI) against the fp64 oracle, element by element.
+
+Tolerance (fp32 FMA kernels): |gpu - oracle| <= 1e-5 * (1 + |oracle|) for every
+output, output shapes exact.  Small cases span several tiles and ragged tails
+and cover every kernel variant; the full-size workloads are compared on sampled
+(n, c) planes, which the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+
+import __graft_entry__
+import oracle as ora
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+from average_pooling_stencil_gb300 import binding as B  # noqa: E402
+from average_pooling_stencil_gb300 import workloads  # noqa: E402
+
+TOL = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    __graft_entry__.build()
+    assert torch.cuda.is_available()
+    torch.cuda.set_device(0)
+    B.aps_device_status(clear=True)
+    yield
+    st, bits = B.aps_device_status(clear=True)
+    assert st == 0 and bits == 0, f"device status word {bits}"
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def assert_close(got, want, tol=TOL, what=""):
+    got = np.asarray(got, dtype=np.float64)
+    assert got.shape == want.shape, (what, got.shape, want.shape)
+    assert np.isfinite(got).all(), what
+    err = np.abs(got - want)
+    bound = tol * (1.0 + np.abs(want))
+    bad = err > bound
+    if bad.any():
+        i = np.unravel_index(np.argmax(err / bound), err.shape)
+        raise AssertionError(f"{what}: {int(bad.sum())}/{err.size} outputs off; worst at {i}: "
+                             f"gpu {got[i]!r} oracle {want[i]!r}")
+
+
+def rng_inputs(seed, *shapes, lo=-1.0, hi=1.0):
+    r = np.random.default_rng(seed)
+    return [r.uniform(lo, hi, s).astype(np.float32) for s in shapes]
+
+
+# ------------------------------------------------------------------ avgpool3d
+FAST_POOL_SHAPES = [(2, 3, 9, 20, 68), (1, 2, 4, 17, 132), (1, 1, 2, 2, 4), (3, 2, 7, 5, 8),
+                    (1, 1, 1, 1, 4), (2, 1, 3, 33, 260), (1, 3, 6, 16, 256)]
+
+
+@pytest.mark.parametrize("shape", FAST_POOL_SHAPES)
+def test_avgpool_k3s2p1_tma_path(shape):
+    x = workloads.get(1).with_input_shape(shape).generate("x")
+    y = B.avgpool3d(dev(x), 3, 2, 1)
+    assert_close(y.cpu().numpy(), ora.avgpool3d(x, 3, 2, 1, 1, 0), what=f"avgpool {shape}")
+
+
+@pytest.mark.parametrize("shape", [(2, 3, 9, 20, 67), (1, 1, 5, 6, 7), (1, 2, 3, 3, 2)])
+def test_avgpool_k3s2p1_direct_path(shape):
+    x, = rng_inputs(1, shape)
+    y = B.avgpool3d(dev(x), 3, 2, 1)
+    assert_close(y.cpu().numpy(), ora.avgpool3d(x, 3, 2, 1, 1, 0), what=f"avgpool {shape}")
+
+
+def test_avgpool_unaligned_input_takes_direct_path():
+    x, = rng_inputs(2, (1 * 2 * 5 * 6 * 8 + 1,))
+    xt = dev(x)[1:].view(1, 2, 5, 6, 8)
+    assert xt.data_ptr() % 16 != 0
+    y = B.avgpool3d(xt, 3, 2, 1)
+    ref = ora.avgpool3d(x[1:].reshape(1, 2, 5, 6, 8), 3, 2, 1, 1, 0)
+    assert_close(y.cpu().numpy(), ref, what="unaligned avgpool")
+
+
+@pytest.mark.parametrize("k,s,p,cip,ceil", [
+    ((2, 3, 4), (1, 2, 3), (1, 1, 2), 1, 0), ((3, 3, 3), (2, 2, 2), (1, 1, 1), 0, 0),
+    ((3, 3, 3), (2, 2, 2), (1, 1, 1), 1, 1), ((3, 3, 3), (2, 2, 2), (1, 1, 1), 0, 1),
+    ((5, 2, 3), (3, 2, 1), (2, 0, 1), 0, 1), ((1, 1, 1), (1, 1, 1), (0, 0, 0), 1, 0)])
+def test_avgpool_general_windows(k, s, p, cip, ceil):
+    x, = rng_inputs(3, (2, 2, 7, 9, 10))
+    y = B.avgpool3d(dev(x), k, s, p, bool(cip), bool(ceil))
+    assert_close(y.cpu().numpy(), ora.avgpool3d(x, k, s, p, cip, ceil),
+                 what=f"avgpool {k} {s} {p} {cip} {ceil}")
+
+
+def test_avgpool_repeatable_bitwise():
+    x = dev(workloads.get(1).with_input_shape((2, 4, 10, 34, 132)).generate("x"))
+    a = B.avgpool3d(x, 3, 2, 1)
+    b = B.avgpool3d(x, 3, 2, 1)
+    assert torch.equal(a, b)
+
+
+@pytest.mark.slow
+def test_avgpool_full_workload_sampled_planes():
+    wl = workloads.get(1)
+    x = wl.generate("x")                                   # [16,32,128,128,256], 8.6 GB
+    xd = dev(x)
+    y = B.avgpool3d(xd, 3, 2, 1)
+    torch.cuda.synchronize()
+    sel = [(0, 0), (0, 31), (7, 13), (15, 0), (15, 31), (9, 22)]
+    ref = ora.avgpool3d(x, 3, 2, 1, 1, 0, sel=sel)
+    got = np.stack([y[n, c].cpu().numpy() for n, c in sel])
+    assert_close(got, ref, what="avgpool full workload")
+    assert torch.isfinite(y).all()
+    del xd, y
+    torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------- ct3d_scale_pool_bias
+def fused_ref(wl, x, w, cb, b, **over):
+    p = dict(wl.params, **over)
+    return ora.ct3d_scale_pool_bias(x, w, cb, b, p["stride"], p["pad"], p["out_pad"], p["dil"],
+                                    p["pool_k"], p["scale1"], p["scale2"])
+
+
+def fused_gpu(x, w, cb, b, p):
+    return B.ct3d_scale_pool_bias(dev(x), dev(w), None if cb is None else dev(cb), dev(b),
+                                  p["stride"], p["pad"], p["out_pad"], p["dil"], p["pool_k"],
+                                  p["scale1"], p["scale2"]).cpu().numpy()
+
+
+@pytest.mark.parametrize("cfg", [0, 2])
+def test_fused_workloads_all_outputs(cfg):
+    wl = workloads.get(cfg)
+    x, w, cb, b = (wl.generate(n) for n in ("x", "w", "conv_bias", "bias"))
+    assert_close(fused_gpu(x, w, cb, b, wl.params), fused_ref(wl, x, w, cb, b),
+                 what=f"fused cfg {cfg}")
+
+
+@pytest.mark.parametrize("shape", [(1, 3, 5, 7, 9), (2, 1, 2, 2, 2), (3, 8, 4, 6, 33),
+                                   (1, 2, 3, 40, 40), (2, 3, 4, 8, 32), (1, 5, 2, 3, 1030),
+                                   (1, 3, 3, 70, 20)])
+def test_fused_fast_path_shapes(shape):
+    base = workloads.get(0)
+    wl = workloads.Workload(base.name, base.op, 5, dict(base.tensors), dict(base.params))
+    wl.tensors["x"] = (shape, ("uniform", -1.0, 1.0), 0)
+    wl.tensors["w"] = ((shape[1], 16, 3, 3, 3), base.tensors["w"][1], 1)
+    x, w, cb, b = (wl.generate(n) for n in ("x", "w", "conv_bias", "bias"))
+    assert_close(fused_gpu(x, w, cb, b, wl.params), fused_ref(wl, x, w, cb, b),
+                 what=f"fused {shape}")
+
+
+def test_fused_without_conv_bias_and_other_scales():
+    wl = workloads.get(0)
+    x, w, b = (wl.generate(n) for n in ("x", "w", "bias"))
+    p = dict(wl.params, scale1=1.75, scale2=-0.3)
+    assert_close(fused_gpu(x, w, None, b, p), fused_ref(wl, x, w, None, b, scale1=1.75, scale2=-0.3),
+                 what="fused no conv bias")
+
+
+@pytest.mark.parametrize("cout,k,s,p,op,d,q", [
+    (5, (3, 2, 4), (1, 2, 3), (0, 1, 1), (0, 1, 2), (1, 2, 1), 3),
+    (16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (0, 0, 0), (1, 1, 1), 3),
+    (16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (1, 1, 1), 2),
+    (12, (3, 3, 3), (2, 2, 2), (1, 1, 1), (0, 0, 0), (1, 1, 1), 2),
+    (4, (2, 2, 2), (2, 2, 2), (0, 0, 0), (0, 0, 0), (1, 1, 1), 1)])
+def test_fused_general_geometry(cout, k, s, p, op, d, q):
+    x, = rng_inputs(7, (2, 3, 4, 5, 6))
+    w, cb, b = rng_inputs(8, (3, cout) + k, (cout,), (cout,), lo=-0.2, hi=0.2)
+    prm = dict(stride=s, pad=p, out_pad=op, dil=d, pool_k=q, scale1=0.5, scale2=1.5)
+    ref = ora.ct3d_scale_pool_bias(x, w, cb, b, s, p, op, d, q, 0.5, 1.5)
+    assert_close(fused_gpu(x, w, cb, b, prm), ref, what=f"fused general {k} {s} {p} {op} {d} {q}")
+
+
+# ------------------------------------------------------------ convtranspose1d
+CONVT_CASES = [  # (s, K, d, p, op, Cin, Cout, L, bias)
+    (1, 5, 3, 0, 0, 32, 64, 1000, False),
+    (1, 5, 3, 2, 0, 3, 16, 77, True),
+    (2, 4, 2, 1, 1, 64, 64, 513, True),
+    (2, 4, 2, 3, 1, 9, 24, 100, True),
+    (1, 3, 1, 1, 0, 17, 72, 300, False),
+    (2, 4, 1, 1, 1, 5, 8, 64, True),
+    (2, 3, 1, 1, 1, 6, 16, 50, False),
+    (1, 5, 1, 4, 0, 8, 8, 9, True),
+    (3, 2, 1, 1, 2, 4, 8, 30, True),
+    (1, 5, 3, 0, 0, 4, 12, 40, True),
+    (1, 1, 1, 0, 0, 1, 8, 1, True),
+    (4, 3, 5, 2, 3, 2, 3, 11, True),
+]
+
+
+@pytest.mark.parametrize("s,K,d,p,op,cin,cout,L,has_bias", CONVT_CASES)
+def test_convt1d_cases(s, K, d, p, op, cin, cout, L, has_bias):
+    x, = rng_inputs(11, (2, cin, L))
+    w, b = rng_inputs(12, (cin, cout, K), (cout,), lo=-0.3, hi=0.3)
+    b = b if has_bias else None
+    y = B.convtranspose1d(dev(x), dev(w), None if b is None else dev(b), s, p, d, op)
+    assert_close(y.cpu().numpy(), ora.convt(x, w, b, s, p, d, op),
+                 what=f"convt1d s{s} K{K} d{d} p{p} op{op} {cin}->{cout} L{L}")
+
+
+def test_convt1d_unaligned_output():
+    x, = rng_inputs(13, (2, 8, 129))
+    w, = rng_inputs(14, (8, 16, 5), lo=-0.3, hi=0.3)
+    L_out = 129 + 12
+    buf = torch.empty(2 * 16 * L_out + 1, device="cuda")
+    out = buf[1:].view(2, 16, L_out)
+    B.convtranspose1d(dev(x), dev(w), None, 1, 0, 3, 0, out=out)
+    assert_close(out.cpu().numpy(), ora.convt(x, w, None, 1, 0, 3, 0), what="unaligned out")
+
+
+@pytest.mark.parametrize("cfg", [3, 4])
+@pytest.mark.slow
+def test_convt1d_full_workload_sampled_planes(cfg):
+    wl = workloads.get(cfg)
+    p = wl.params
+    x, w = wl.generate("x"), wl.generate("w")
+    b = wl.generate("bias") if p["has_bias"] else None
+    y = B.convtranspose1d(dev(x), dev(w), None if b is None else dev(b), p["stride"], p["pad"],
+                          p["dil"], p["out_pad"])
+    torch.cuda.synchronize()
+    N, C = y.shape[0], y.shape[1]
+    sel = [(0, 0), (N - 1, C - 1), (N // 2, 17), (3, C // 2), (N - 1, 0)]
+    ref = ora.convt(x, w, b, p["stride"], p["pad"], p["dil"], p["out_pad"], sel=sel)
+    got = np.stack([y[n, c].cpu().numpy() for n, c in sel])
+    assert_close(got, ref, what=f"convt1d cfg {cfg}")
+    assert torch.isfinite(y).all()
+    if cfg == 4:  # no tap reaches an even output: exactly the bias
+        assert torch.equal(y[:, :, 0::2], dev(b).view(1, -1, 1).expand_as(y[:, :, 0::2]))
