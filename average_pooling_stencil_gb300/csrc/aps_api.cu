@@ -54,26 +54,51 @@ struct OccEntry {
     const void *func;
     int dev, threads, smem, n;
 };
+struct SmemLimit {
+    const void *func;
+    int dev, bytes;
+};
 constexpr int kOccEntries = 256;
 OccEntry g_occ[kOccEntries];
 int g_occ_used = 0;
+SmemLimit g_limit[kOccEntries];
+int g_limit_used = 0;
+
+// Raises (never lowers) a kernel's dynamic shared-memory limit on `dev`; the
+// limit is per kernel and device, and a call needing less must not undo it.
+bool raise_smem_limit(const void *func, int dev, int smem) {
+    int i = 0;
+    for (; i < g_limit_used; ++i)
+        if (g_limit[i].func == func && g_limit[i].dev == dev) break;
+    if (i < g_limit_used && g_limit[i].bytes >= smem) return true;
+    if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (i < g_limit_used) {
+        g_limit[i].bytes = smem;
+    } else if (g_limit_used < kOccEntries) {
+        g_limit[g_limit_used++] = SmemLimit{func, dev, smem};
+    }
+    return true;
+}
 }  // namespace
 
 int resident_ctas(const void *func, int threads, int smem) {
     const int dev = current_device();
     if (dev < 0) return 0;
     std::lock_guard<std::mutex> lock(g_mutex);
+    if (smem > 48 * 1024 && !raise_smem_limit(func, dev, smem)) return 0;
     for (int i = 0; i < g_occ_used; ++i) {
         const OccEntry &e = g_occ[i];
         if (e.func == func && e.dev == dev && e.threads == threads && e.smem == smem) return e.n;
     }
-    if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-            cudaSuccess)
-        return 0;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, func, threads, smem) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, func, threads, smem) != cudaSuccess) {
+        cudaGetLastError();
         return 0;
+    }
     if (g_occ_used < kOccEntries) g_occ[g_occ_used++] = OccEntry{func, dev, threads, smem, n};
     return n;
 }
@@ -291,7 +316,8 @@ aps_status aps_convtranspose1d(const float *x, const int64_t in[3], const float 
         return APS_ERR_ALIGN;
     if (numel(out, 3) == 0) return APS_OK;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    if (precision == APS_PREC_TF32) return APS_ERR_UNSUPPORTED;
+    if (precision == APS_PREC_TF32)
+        return launch_convt1d_tf32(x, in, w, bias, c_out, k, s, p, d, y, out[2], cs);
     if (in[1] >= 1) {
         st = launch_convt1d_tiled(x, in, w, bias, c_out, k, s, p, d, y, out[2], cs);
         if (st != APS_ERR_UNSUPPORTED) return st;

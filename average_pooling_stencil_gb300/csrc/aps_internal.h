@@ -68,6 +68,14 @@ aps_status launch_convt1d_tiled(const float *x, const int64_t in[3], const float
                                 const float *bias, int64_t c_out, int k, int s, int p,
                                 int d, float *y, int64_t l_out, cudaStream_t st);
 
+// ConvTranspose1d on the tensor cores (tf32 operands, fp32 accumulation).
+// Needs C_in % 8 == 0 (and C_in % 32 == 0 above 32), C_out % 32 == 0,
+// C_out <= 256, L % 4 == 0, x 16-byte aligned, at most 4 output classes with
+// taps; returns APS_ERR_UNSUPPORTED otherwise.
+aps_status launch_convt1d_tf32(const float *x, const int64_t in[3], const float *w,
+                               const float *bias, int64_t c_out, int k, int s, int p, int d,
+                               float *y, int64_t l_out, cudaStream_t st);
+
 aps_status launch_convt1d_direct(const float *x, const int64_t in[3], const float *w,
                                  const float *bias, int64_t c_out, int k, int s, int p,
                                  int d, float *y, int64_t l_out, cudaStream_t st);

@@ -51,7 +51,12 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--e2e-steps", type=int, default=8, help="0 skips the e2e leg")
+    ap.add_argument("--workload", type=int, default=HEADLINE_CFG,
+                    help="workload of the headline line (default: the avgpool workload)")
+    ap.add_argument("--x-shape", type=str, default=None,
+                    help="override the input shape of the headline workload (profiling "
+                         "runs on small cases), e.g. 2,32,128,128,256")
     ap.add_argument("--no-per-config", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -170,10 +175,13 @@ def workload_desc(wl):
 class GpuCase:
     """Device-resident inputs/outputs of one workload plus its launch closure."""
 
-    def __init__(self, cfg, torch, aps, with_host=False):
+    def __init__(self, cfg, torch, aps, with_host=False, x_shape=None, precision=0):
         from average_pooling_stencil_gb300 import workloads
         self.cfg = cfg
+        self.precision = precision
         self.wl = wl = workloads.get(cfg)
+        if x_shape is not None:
+            self.wl = wl = wl.with_input_shape(x_shape)
         self.torch = torch
         p = wl.params
         dev = torch.device("cuda")
@@ -204,7 +212,8 @@ class GpuCase:
                 x.shape, p["c_out"], p["k"], p["stride"], p["pad"], p["dil"], p["out_pad"])
             pairs = convt_pairs(x.shape[2], oshape[2], p["k"], p["stride"], p["pad"], p["dil"])
             self.flops = 2 * x.shape[0] * x.shape[1] * p["c_out"] * pairs
-            self.bound = "alu"
+            # fp32 FMA path is bound by the FP32 pipe; the tf32 tensor path by HBM
+            self.bound = "alu" if precision == 0 else "hbm"
         assert st == 0
         self.oshape = oshape
         self.y = torch.empty(oshape, device=dev, dtype=torch.float32)
@@ -232,7 +241,7 @@ class GpuCase:
             bias = d["bias"].data_ptr() if "bias" in d else 0
             st = B.aps_convtranspose1d(d["x"].data_ptr(), d["x"].shape, d["w"].data_ptr(), bias,
                                        p["c_out"], p["k"], p["stride"], p["pad"], p["dil"],
-                                       p["out_pad"], B.APS_PREC_FP32, self.y.data_ptr(), s)
+                                       p["out_pad"], self.precision, self.y.data_ptr(), s)
         if st != 0:
             raise RuntimeError(f"launch failed: {B.status_string(st)}")
 
@@ -312,64 +321,50 @@ def roofline_for(case, t, peaks, src, clock_mhz):
 
 
 # ------------------------------------------------------------------ oracle
-def oracle_sample(cfg, seconds):
-    """Time the oracle on a bounded sample of (n, c) planes of workload `cfg`.
-    Returns (outputs per second, threads, description, outputs, seconds)."""
+def oracle_sample(cfg, seconds, xhost=None):
+    """Time the oracle (as it stands) on a bounded sample of output planes of
+    workload `cfg`, sized to about `seconds` of CPU time.  `xhost` is the
+    workload's input already in host memory (generated from the same seed if
+    None).  Returns (outputs/s, threads, description, outputs, seconds)."""
     import numpy as np
 
     import oracle
     from average_pooling_stencil_gb300 import workloads
     wl = workloads.get(cfg)
     p = wl.params
-    xs = wl.tensors["x"][0]
+    xs = tuple(wl.tensors["x"][0])
     N, C = xs[0], xs[1]
-    plane = numel(xs[2:])
     threads = oracle.threads()
+    x = np.asarray(xhost).reshape(xs) if xhost is not None else wl.generate("x")
     tens = {n: wl.generate(n) for n in wl.tensors if n != "x"}
     if wl.op == "avgpool3d":
-        def run(ns, planes):
-            xb = np.stack([wl.generate_range("x", (n * C + c) * plane, (n * C + c + 1) * plane)
-                           .reshape(xs[2:]) for (n, c) in planes])[:, None]
-            t0 = time.perf_counter()
-            y = oracle.avgpool3d(xb, p["k"], p["stride"], p["pad"], p["count_include_pad"],
-                                 p["ceil_mode"])
-            return time.perf_counter() - t0, y.size
         units = [(n, c) for n in range(N) for c in range(C)]
+
+        def run(planes):
+            t0 = time.perf_counter()
+            y = oracle.avgpool3d(x, p["k"], p["stride"], p["pad"], p["count_include_pad"],
+                                 p["ceil_mode"], sel=planes)
+            return time.perf_counter() - t0, y.size
     else:
-        cout = p["c_out"]
-        xfull = {}
+        units = [(n, co) for n in range(N) for co in range(p["c_out"])]
 
-        def xrow(n):
-            if n not in xfull:
-                xfull[n] = wl.generate_range("x", n * C * plane, (n + 1) * C * plane).reshape(
-                    (1, C) + tuple(xs[2:]))
-            return xfull[n]
-
-        def run(ns, planes):
-            tot, cnt = 0.0, 0
-            for n in sorted({q[0] for q in planes}):
-                sel = [(0, co) for (m, co) in planes if m == n]
-                xb = xrow(n)
-                t0 = time.perf_counter()
-                if wl.op == "ct3d_scale_pool_bias":
-                    y = oracle.ct3d_scale_pool_bias(xb, tens["w"], tens["conv_bias"], tens["bias"],
-                                                    p["stride"], p["pad"], p["out_pad"], p["dil"],
-                                                    p["pool_k"], p["scale1"], p["scale2"], sel=sel)
-                else:
-                    y = oracle.convt(xb, tens["w"], tens.get("bias"), p["stride"], p["pad"],
-                                     p["dil"], p["out_pad"], sel=sel)
-                tot += time.perf_counter() - t0
-                cnt += y.size
-            return tot, cnt
-        units = [(n, co) for n in range(N) for co in range(cout)]
-    # calibrate on one batch of `threads` planes, then size the sample
+        def run(planes):
+            t0 = time.perf_counter()
+            if wl.op == "ct3d_scale_pool_bias":
+                y = oracle.ct3d_scale_pool_bias(x, tens["w"], tens["conv_bias"], tens["bias"],
+                                                p["stride"], p["pad"], p["out_pad"], p["dil"],
+                                                p["pool_k"], p["scale1"], p["scale2"], sel=planes)
+            else:
+                y = oracle.convt(x, tens["w"], tens.get("bias"), p["stride"], p["pad"], p["dil"],
+                                 p["out_pad"], sel=planes)
+            return time.perf_counter() - t0, y.size
+    # calibrate on one plane per thread, then size the sample to `seconds`
     k = min(len(units), max(1, threads))
-    t, cnt = run(None, units[:k])
-    per_plane = t / k
-    m = int(min(len(units), max(k, round(seconds / max(per_plane, 1e-6)))))
+    t, _ = run(units[:k])
+    m = int(min(len(units), max(k, round(seconds * k / max(t, 1e-6)))))
     step = max(1, len(units) // m)
     sample = units[::step][:m]
-    t, cnt = run(None, sample)
+    t, cnt = run(sample)
     desc = f"{len(sample)} of {len(units)} (n, c) output planes of {workload_desc(wl)}"
     return cnt / t, threads, desc, cnt, t
 
@@ -390,12 +385,13 @@ def run_reference(args):
     from average_pooling_stencil_gb300 import workloads
     wl = workloads.get(HEADLINE_CFG)
     oracle.build()
+    x = wl.generate("x")
     per_step = max(1.0, min(args.cpu_seconds, 60.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
-        oracle_sample(HEADLINE_CFG, per_step)
+        oracle_sample(HEADLINE_CFG, per_step, x)
     vals, times, desc, threads = [], [], "", 1
     for _ in range(args.steps):
-        v, threads, desc, cnt, t = oracle_sample(HEADLINE_CFG, per_step)
+        v, threads, desc, cnt, t = oracle_sample(HEADLINE_CFG, per_step, x)
         vals.append(v)
         times.append(t)
     value = sum(times) and sum(v * t for v, t in zip(vals, times)) / sum(times)
@@ -438,7 +434,8 @@ def run_native(args):
         torch.cuda.synchronize()
 
     # ---- headline: each rank runs its own full workload (weak scaling)
-    case = GpuCase(HEADLINE_CFG, torch, aps, with_host=True)
+    x_shape = tuple(int(v) for v in args.x_shape.split(",")) if args.x_shape else None
+    case = GpuCase(args.workload, torch, aps, with_host=args.e2e_steps > 0, x_shape=x_shape)
     for _ in range(max(3, args.warmup)):
         case.launch()
     barrier()
@@ -465,31 +462,37 @@ def run_native(args):
     value = ws * case.outputs * args.steps / t_max
 
     # ---- e2e through the ABI with host buffers
-    for _ in range(2):
-        case.e2e_step()
-    barrier()
-    e2e_steps = max(1, args.e2e_steps)
-    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    f0.record(st)
-    for _ in range(e2e_steps):
-        case.e2e_step()
-    f1.record(st)
-    barrier()
-    t_e2e = f0.elapsed_time(f1) / 1e3
-    if dist:
-        tt = torch.tensor([t_e2e], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_e2e = float(tt.item())
-    e2e = {"value": ws * case.outputs * e2e_steps / t_e2e, "unit": "outputs/s",
-           "h2d_bytes_per_step": 4 * numel(case.host["x"].shape),
-           "d2h_bytes_per_step": 4 * case.outputs, "steps": e2e_steps,
-           "ms_per_step": 1e3 * t_e2e / e2e_steps}
+    e2e = None
+    if args.e2e_steps > 0:
+        for _ in range(2):
+            case.e2e_step()
+        barrier()
+        e2e_steps = args.e2e_steps
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(st)
+        for _ in range(e2e_steps):
+            case.e2e_step()
+        f1.record(st)
+        barrier()
+        t_e2e = f0.elapsed_time(f1) / 1e3
+        if dist:
+            tt = torch.tensor([t_e2e], device="cuda")
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            t_e2e = float(tt.item())
+        e2e = {"value": ws * case.outputs * e2e_steps / t_e2e, "unit": "outputs/s",
+               "h2d_bytes_per_step": 4 * numel(case.host["x"].shape),
+               "d2h_bytes_per_step": 4 * case.outputs, "steps": e2e_steps,
+               "ms_per_step": 1e3 * t_e2e / e2e_steps}
 
     clocks = sampler.summary(t_wall0, t_wall1)
     roof = roofline_for(case, per_launch, peaks, peak_src, clocks.get("sm_mhz"))
-    roof["traffic"] = traffic_from_profile("avgpool3d.cu", "avgpool3d_k3s2p1_tma.md")
+    kernel_of = {"avgpool3d": ("avgpool3d.cu", "avgpool3d_k3s2p1_tma_kernel"),
+                 "ct3d_scale_pool_bias": ("ct3d_pool.cu", "ct3d_pool2_fast_kernel"),
+                 "convtranspose1d": ("convt1d.cu", "convt1d_tiled_kernel")}[case.wl.op]
+    roof["kernel"] = kernel_of[1]
     roof["algorithmic_bytes_per_launch"] = case.bytes
-    roof["kernel"] = "avgpool3d_k3s2p1_tma_kernel"
+    roof["traffic"] = (traffic_from_profile(kernel_of[0], "avgpool3d_k3s2p1_tma.md")
+                       if args.workload == HEADLINE_CFG and x_shape is None else None)
 
     st_code, bits = aps.binding.aps_device_status(clear=True)
     if st_code != 0 or bits != 0:
@@ -501,10 +504,12 @@ def run_native(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": workload_desc(case.wl), "seed": case.wl.seed,
-                   "l2": "inputs larger than L2 (8.59 GB input per step), no flush",
+                   "l2": ("inputs larger than L2 (8.59 GB input per step), no flush"
+                          if case.bytes > 2 * 129e6 else "input may stay in L2 (small case)"),
                    "parallelism": f"replicas{ws}" if ws > 1 else "single GPU"},
         "roofline": roof, "e2e": e2e, "gpu_launches": args.steps, "clocks": clocks,
     }
+    xhost = case.host["x"].numpy() if args.workload == HEADLINE_CFG and x_shape is None else None
     del case
     torch.cuda.empty_cache()
 
@@ -512,8 +517,8 @@ def run_native(args):
     if rank == 0 and not args.no_per_config:
         per = {}
         flush = torch.empty(64 * 1024 * 1024, device="cuda")   # 256 MB > L2
-        for cfg in (0, 2, 3, 4):
-            c = GpuCase(cfg, torch, aps)
+        for cfg, prec in ((0, 0), (2, 0), (3, 0), (4, 0), (3, 1), (4, 1)):
+            c = GpuCase(cfg, torch, aps, precision=prec)
             for _ in range(3):
                 c.launch()
             torch.cuda.synchronize()
@@ -526,8 +531,9 @@ def run_native(args):
             else:
                 t = time_launches(torch, c, 20)
                 how = "20 back-to-back launches (input larger than L2)"
-            per[c.wl.name] = {
-                "workload": workload_desc(c.wl), "outputs_per_s": c.outputs / t,
+            per[c.wl.name + ("_tf32" if prec else "")] = {
+                "workload": workload_desc(c.wl) + (" (tf32 tensor cores)" if prec else ""),
+                "outputs_per_s": c.outputs / t,
                 "us_per_launch": 1e6 * t, "gb_per_s": c.bytes / t / 1e9,
                 "tflop_per_s": c.flops / t / 1e12, "algorithmic_bytes": c.bytes,
                 "algorithmic_flops": c.flops,
@@ -538,7 +544,7 @@ def run_native(args):
 
     # ---- CPU baseline: the oracle on the host cores (rank 0, N = 1 only)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        v, threads, desc, cnt, t = oracle_sample(HEADLINE_CFG, args.cpu_seconds)
+        v, threads, desc, cnt, t = oracle_sample(HEADLINE_CFG, args.cpu_seconds, xhost)
         line["cpu_baseline"] = {"value": v, "unit": "outputs/s", "cores": threads,
                                 "kind": "oracle", "sample": desc, "seconds": t}
     if rank == 0:

@@ -226,3 +226,83 @@ def test_convt1d_full_workload_sampled_planes(cfg):
     assert torch.isfinite(y).all()
     if cfg == 4:  # no tap reaches an even output: exactly the bias
         assert torch.equal(y[:, :, 0::2], dev(b).view(1, -1, 1).expand_as(y[:, :, 0::2]))
+
+
+# ------------------------------------------- convtranspose1d, tf32 tensor cores
+def assert_frobenius(got, want, tol=5e-3, what=""):
+    got = np.asarray(got, dtype=np.float64)
+    assert got.shape == want.shape, (what, got.shape, want.shape)
+    assert np.isfinite(got).all(), what
+    rel = np.linalg.norm(got - want) / max(np.linalg.norm(want), 1e-300)
+    assert rel <= tol, f"{what}: relative Frobenius error {rel:.3e} > {tol}"
+    return rel
+
+
+TF32_CASES = [  # (s, K, d, p, op, Cin, Cout, L, bias)
+    (1, 5, 3, 0, 0, 32, 64, 1000, False),
+    (2, 4, 2, 1, 1, 64, 64, 516, True),
+    (1, 3, 1, 1, 0, 8, 32, 300, True),
+    (2, 4, 1, 1, 1, 16, 32, 64, True),
+    (3, 2, 1, 1, 2, 8, 32, 32, True),
+    (1, 2, 1, 0, 0, 32, 256, 200, True),
+    (2, 3, 3, 2, 1, 96, 64, 124, False),
+    (1, 3, 2, 1, 0, 64, 128, 160, True),
+    (1, 1, 1, 0, 0, 24, 64, 4, True),
+]
+
+
+@pytest.mark.parametrize("s,K,d,p,op,cin,cout,L,has_bias", TF32_CASES)
+def test_convt1d_tf32_cases(s, K, d, p, op, cin, cout, L, has_bias):
+    x, = rng_inputs(21, (3, cin, L))
+    w, b = rng_inputs(22, (cin, cout, K), (cout,), lo=-0.3, hi=0.3)
+    b = b if has_bias else None
+    y = B.convtranspose1d(dev(x), dev(w), None if b is None else dev(b), s, p, d, op,
+                          precision=B.APS_PREC_TF32)
+    assert_frobenius(y.cpu().numpy(), ora.convt(x, w, b, s, p, d, op),
+                     what=f"tf32 s{s} K{K} d{d} p{p} op{op} {cin}->{cout} L{L}")
+
+
+@pytest.mark.parametrize("cin,cout,L", [(12, 32, 64), (32, 48, 64), (32, 64, 66), (40, 64, 64),
+                                        (64, 256, 64)])
+def test_convt1d_tf32_unsupported_shapes(cin, cout, L):
+    x, = rng_inputs(23, (1, cin, L))
+    w, = rng_inputs(24, (cin, cout, 3))
+    with pytest.raises(B.ApsError) as e:
+        B.convtranspose1d(dev(x), dev(w), None, 1, 0, 1, 0, precision=B.APS_PREC_TF32)
+    assert e.value.status == B.APS_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("cfg", [3, 4])
+@pytest.mark.slow
+def test_convt1d_tf32_full_workload_sampled_planes(cfg):
+    wl = workloads.get(cfg)
+    p = wl.params
+    x, w = wl.generate("x"), wl.generate("w")
+    b = wl.generate("bias") if p["has_bias"] else None
+    y = B.convtranspose1d(dev(x), dev(w), None if b is None else dev(b), p["stride"], p["pad"],
+                          p["dil"], p["out_pad"], precision=B.APS_PREC_TF32)
+    torch.cuda.synchronize()
+    N, C = y.shape[0], y.shape[1]
+    sel = [(0, 0), (N - 1, C - 1), (N // 2, 17), (3, C // 2), (N - 1, 0)]
+    ref = ora.convt(x, w, b, p["stride"], p["pad"], p["dil"], p["out_pad"], sel=sel)
+    got = np.stack([y[n, c].cpu().numpy() for n, c in sel])
+    assert_frobenius(got, ref, what=f"tf32 cfg {cfg}")
+    assert torch.isfinite(y).all()
+
+
+def test_kernel_smem_limit_survives_smaller_launches():
+    """A launch that needs less dynamic shared memory must not lower the limit
+    a later, larger launch of the same kernel relies on."""
+    big = (1, 3, 3, 70, 20)     # fused tile > 48 KB of shared memory
+    small = (1, 3, 2, 3, 4)
+    base = workloads.get(0)
+    for shape in (big, small, big):
+        x, = rng_inputs(31, shape)
+        w, cb, b = (base.generate(n) for n in ("w", "conv_bias", "bias"))
+        assert_close(fused_gpu(x, w, cb, b, base.params), fused_ref(base, x, w, cb, b),
+                     what=f"fused {shape}")
+    for cin, cout, L in ((32, 64, 400), (8, 32, 64), (32, 64, 400)):
+        x, = rng_inputs(32, (2, cin, L))
+        w, = rng_inputs(33, (cin, cout, 5), lo=-0.3, hi=0.3)
+        y = B.convtranspose1d(dev(x), dev(w), None, 1, 0, 3, 0, precision=B.APS_PREC_TF32)
+        assert_frobenius(y.cpu().numpy(), ora.convt(x, w, None, 1, 0, 3, 0), what="tf32 order")
