@@ -14,20 +14,26 @@
 //  * warp 0, lane 0  -- TMA producer: for each (n, 128-position tile, 32-channel
 //    chunk) one 3-D box x[n, ci0:ci0+32, a0:a0+BW] (BW = 128 + tap span, start
 //    rounded down to 16 bytes; out-of-range cells arrive as zeros) into a
-//    4-stage ring.  Warp 0 also owns the tensor-memory allocation.
-//  * warps 2, 3, 8, 9 -- converters: transpose each raw box into the K-major,
+//    ring of up to 4 stages, and an L2 prefetch of the box 12 steps ahead (one
+//    CTA per SM holds few stages; the prefetch keeps enough bytes in flight).
+//    Warp 0 also owns the tensor-memory allocation.
+//  * warps 2, 3, 8..13 -- converters (one per 4 channels): transpose each raw
+//    box into the K-major,
 //    no-swizzle operand layout (8-row x 16-byte core matrices; rows = window
 //    positions, 4 channels per 16 bytes, one block of rows per 4 channels) and
 //    round to tf32 (cvt.rna).  Because rows are 16 bytes apart, the operand of
 //    tap k is the same buffer with its start moved by 16 bytes per row of tap
 //    offset: one transposed copy serves every tap of every class.
-//  * warp 1, lane 0  -- MMA issuer: per chunk and (class, tap), CK/8 tcgen05.mma
+//  * warp 1, lane 0  -- MMA issuer: walks a per-CTA table of descriptors and,
+//    per chunk and (class, tap), issues CK/8 tcgen05.mma
 //    kind::tf32 of 128 x C_out x 8 into the class's accumulator in tensor memory
 //    (double-buffered across tiles), then tcgen05.commit to release the
 //    operand stage and, after the last chunk, to hand the tile to the epilogue.
 //  * warps 4..7 -- epilogue: tcgen05.ld of their 32 accumulator rows, + bias,
-//    and stores of s consecutive outputs per channel (classes without taps are
-//    the bias alone), 32 lanes writing consecutive positions.
+//    into shared-memory slabs laid out like the output (class r of position
+//    m at s*m + r; residues no tap reaches hold the bias).  With stride <= 2
+//    each 16 KB slab leaves by one TMA tensor store (4 slabs in flight);
+//    otherwise by 128-bit coalesced stores of each channel's s*128 outputs.
 // Weights are rounded to tf32 once per CTA into shared memory in the same
 // K-major layout, one [C_in/4][C_out][4] block per tap.  Every wait is bounded;
 // a wait that times out records APS_DEVERR_TIMEOUT, the CTA drains what it has
@@ -41,11 +47,15 @@ namespace aps {
 namespace tc1 {
 constexpr int BM = 128;           // positions per tile (MMA M)
 constexpr int CK = 32;            // input channels per staged chunk (MMA K per chunk)
-constexpr int RAW_STAGES = 4;
+constexpr int RAW_STAGES = 4;    // at most; the launcher may use fewer to fit smem
 constexpr int XT_STAGES = 3;
 constexpr int MAX_CLASSES = 4;
 constexpr int MAX_TAPS = 8;       // taps per class
-constexpr int THREADS = 320;      // 10 warps
+constexpr int NBUF = 4;           // TMA-store staging slabs in flight
+constexpr int PREFETCH = 12;      // input boxes prefetched into L2 ahead of the loads
+constexpr int THREADS = 448;      // 14 warps
+constexpr int CONVERTERS = 8;     // converter warps: 2, 3, 8..13
+constexpr int MAX_MMA_TAB = 256;  // (chunk, class, tap, k-step) entries of one tile
 constexpr int W_PRODUCER = 0, W_MMA = 1, W_EPI0 = 4;
 
 struct Taps {
@@ -54,10 +64,12 @@ struct Taps {
     int ntaps[MAX_CLASSES];
     int tap_k[MAX_CLASSES][MAX_TAPS];  // weight tap index
     int tap_row[MAX_CLASSES][MAX_TAPS];// first window row used by tile position 0
+    int nempty;                        // residues no tap reaches (bias only)
+    int empty_r[8];
 };
 
 __device__ __forceinline__ int converter_id(int warp) {
-    return warp == 2 ? 0 : warp == 3 ? 1 : warp - 6;   // warps 2, 3, 8, 9
+    return warp == 2 ? 0 : warp == 3 ? 1 : warp - 6;   // warps 2, 3, 8..13
 }
 
 __device__ __forceinline__ uint32_t to_tf32(float v) {
@@ -111,14 +123,26 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         : "r"(taddr));
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+// 32 lanes x 16 columns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
 }  // namespace tc1
 
 __global__ void __launch_bounds__(tc1::THREADS, 1)
-    convt1d_tf32_kernel(const __grid_constant__ CUtensorMap xmap, const float *__restrict__ w,
+    convt1d_tf32_kernel(const __grid_constant__ CUtensorMap xmap,
+                        const __grid_constant__ CUtensorMap ymap, const float *__restrict__ w,
                         const float *__restrict__ bias, float *__restrict__ y, int Cin, int Cout,
                         int K, int S, int L_out, int n_mtiles, long long n_units, int win0, int BW,
-                        int tmem_cols, const __grid_constant__ tc1::Taps taps,
-                        unsigned int *status) {
+                        int tmem_cols, int RS, int vec_store, int tma_store,
+                        const __grid_constant__ tc1::Taps taps, unsigned int *status) {
     using namespace tc1;
     extern __shared__ __align__(1024) unsigned char smem[];
     const int CKr = Cin < CK ? Cin : CK;          // channels per chunk
@@ -130,26 +154,41 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
     const uint32_t RAW_STRIDE = (RAW_BYTES + 1023) & ~1023u;
     unsigned char *xt = smem;
     unsigned char *raw = xt + XT_STAGES * XT_STRIDE;
-    float *wt = reinterpret_cast<float *>(raw + RAW_STAGES * RAW_STRIDE);   // [K][Cin/4][Cout][4]
+    float *wt = reinterpret_cast<float *>(raw + RS * RAW_STRIDE);   // [K][Cin/4][Cout][4]
     float *bs = wt + (size_t)K * Cin * Cout;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(bs + ((Cout + 1) & ~1));
+    const int OROW = BM * S + 4;                   // staged output row (one channel)
+    const int SLAB = S == 1 ? 32 : 16;             // channels per TMA-stored slab
+    // epilogue staging, 1 KB aligned (offset from the shared array so the
+    // compiler keeps shared-memory stores): NBUF dense [SLAB][BM*S] slabs for
+    // TMA stores, or one [32][OROW] block
+    const uint32_t ost_off =
+        ((uint32_t)(reinterpret_cast<unsigned char *>(bs + Cout) - smem) + 1023u) & ~1023u;
+    float *ost = reinterpret_cast<float *>(smem + ost_off);
+    const int ost_floats = tma_store ? NBUF * SLAB * BM * S : 32 * OROW;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ost + ost_floats);
     uint64_t *raw_full = bars, *raw_empty = raw_full + RAW_STAGES;
     uint64_t *xt_full = raw_empty + RAW_STAGES, *xt_empty = xt_full + XT_STAGES;
     uint64_t *acc_full = xt_empty + XT_STAGES, *acc_empty = acc_full + 2;
     uint64_t *drain = acc_empty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    // MMA descriptor tables: B descriptors per (chunk, entry); per entry the A
+    // offset (16-byte units, low 16 bits), class (bits 16..23) and a flag (bit
+    // 31) for the first MMA of its class, which overwrites the accumulator
+    uint64_t *tab_b = reinterpret_cast<uint64_t *>(tmem_slot + 2);
+    uint32_t *tab_a = reinterpret_cast<uint32_t *>(tab_b + MAX_MMA_TAB);
     __shared__ volatile int abort_flag;
+    __shared__ volatile int epi_ok[4];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // ---- set-up: barriers, tensor memory, tf32 weights, bias
     if (threadIdx.x == 0) {
-        for (int s = 0; s < RAW_STAGES; ++s) {
+        for (int s = 0; s < RS; ++s) {
             mbar_init(&raw_full[s], 1);
-            mbar_init(&raw_empty[s], 4);
+            mbar_init(&raw_empty[s], CONVERTERS);
         }
         for (int s = 0; s < XT_STAGES; ++s) {
-            mbar_init(&xt_full[s], 4);
+            mbar_init(&xt_full[s], CONVERTERS);
             mbar_init(&xt_empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -184,6 +223,25 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
         }
         for (int c = threadIdx.x; c < Cout; c += THREADS) bs[c] = bias ? __ldg(bias + c) : 0.f;
     }
+    int n_ent = 0;   // MMAs per chunk
+    for (int c = 0; c < taps.nclass; ++c) n_ent += taps.ntaps[c] * (CKr / 8);
+    if (warp == W_MMA && lane == 0) {
+        const uint32_t LBO_W = (uint32_t)Cout * 16;
+        const uint32_t wt_addr = smem_u32(wt);
+        int e = 0;
+        for (int c = 0; c < taps.nclass; ++c)
+            for (int t = 0; t < taps.ntaps[c]; ++t)
+                for (int j = 0; j < CKr / 8; ++j, ++e) {
+                    const uint32_t aoff = ((uint32_t)taps.tap_row[c][t] * 16 + 2 * j * LBO_X) >> 4;
+                    tab_a[e] = aoff | ((uint32_t)c << 16) | ((t == 0 && j == 0) ? 0x80000000u : 0u);
+                    for (int ch = 0; ch < nchunks; ++ch) {
+                        const uint32_t cb = (uint32_t)(ch * CKr + 8 * j) / 4;
+                        const uint32_t wk =
+                            wt_addr + (uint32_t)taps.tap_k[c][t] * (Cin / 4) * LBO_W + cb * LBO_W;
+                        tab_b[ch * n_ent + e] = tc1::umma_desc(wk, LBO_W, 128);
+                    }
+                }
+    }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc1::tc_fence_before();
     __syncthreads();
@@ -194,6 +252,16 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             tma_prefetch_desc(&xmap);
+            // L2 prefetch runs PREFETCH boxes ahead of the loads, so the smem
+            // ring's few stages are refilled from L2 rather than from HBM.
+            auto prefetch = [&](uint32_t j) {
+                const long long pu = blockIdx.x + (long long)(j / nchunks) * gridDim.x;
+                if (pu >= n_units) return;
+                const int pn = (int)(pu / n_mtiles);
+                const int pmt = (int)(pu - (long long)pn * n_mtiles);
+                tma_prefetch_3d(&xmap, pmt * BM + win0, (int)(j % nchunks) * CKr, pn);
+            };
+            for (uint32_t j = 0; j < (uint32_t)PREFETCH; ++j) prefetch(j);
             uint32_t it = 0;
             bool ok = true;
             for (long long u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
@@ -201,9 +269,9 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
                 const int mt = (int)(u - (long long)n * n_mtiles);
                 const int a0 = mt * BM + win0;
                 for (int ch = 0; ch < nchunks; ++ch, ++it) {
-                    const uint32_t s = it % RAW_STAGES;
-                    if (it >= (uint32_t)RAW_STAGES &&
-                        !mbar_wait(&raw_empty[s], ((it / RAW_STAGES) & 1u) ^ 1u)) {
+                    prefetch(it + PREFETCH);
+                    const uint32_t s = it % RS;
+                    if (it >= (uint32_t)RS && !mbar_wait(&raw_empty[s], ((it / RS) & 1u) ^ 1u)) {
                         record_error(status, APS_DEVERR_TIMEOUT);
                         abort_flag = 1;
                         ok = false;
@@ -215,18 +283,18 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
                 }
             }
             // boxes still in flight land before the CTA goes on to exit
-            const uint32_t first = it > (uint32_t)RAW_STAGES ? it - RAW_STAGES : 0u;
+            const uint32_t first = it > (uint32_t)RS ? it - RS : 0u;
             for (uint32_t j = first; j < it; ++j)
-                if (!mbar_wait(&raw_full[j % RAW_STAGES], (j / RAW_STAGES) & 1u)) break;
+                if (!mbar_wait(&raw_full[j % RS], (j / RS) & 1u)) break;
         }
     } else if (warp == W_MMA) {
         // ------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc = (1u << 4) | (2u << 7) | (2u << 10) |
                                    ((uint32_t)(Cout >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
-            const uint32_t xt_addr = smem_u32(xt);
-            const uint32_t wt_addr = smem_u32(wt);
-            const uint32_t LBO_W = (uint32_t)Cout * 16;
+            uint64_t a_stage[XT_STAGES];
+            for (int st = 0; st < XT_STAGES; ++st)
+                a_stage[st] = tc1::umma_desc(smem_u32(xt) + st * XT_STRIDE, LBO_X, 128);
             uint32_t it = 0, tile = 0;
             bool issued = false;
             for (long long u = blockIdx.x; u < n_units && !abort_flag; u += gridDim.x, ++tile) {
@@ -237,6 +305,7 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
                     break;
                 }
                 tc1::tc_fence_after();
+                const uint32_t dbase = tmem_base + b * taps.nclass * (uint32_t)Cout;
                 bool fail = false;
                 for (int ch = 0; ch < nchunks; ++ch, ++it) {
                     const uint32_t s = it % XT_STAGES;
@@ -247,21 +316,16 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
                         break;
                     }
                     tc1::tc_fence_after();
-                    const uint32_t xs = xt_addr + s * XT_STRIDE;
-                    for (int c = 0; c < taps.nclass; ++c) {
-                        const uint32_t d = tmem_base + (b * taps.nclass + c) * (uint32_t)Cout;
-                        for (int t = 0; t < taps.ntaps[c]; ++t) {
-                            const uint32_t arow = xs + (uint32_t)taps.tap_row[c][t] * 16;
-                            const uint32_t wk = wt_addr + (uint32_t)taps.tap_k[c][t] * (Cin / 4) * LBO_W;
-                            for (int j = 0; j < CKr / 8; ++j) {
-                                const uint64_t ad = tc1::umma_desc(arow + 2 * j * LBO_X, LBO_X, 128);
-                                const uint32_t cb = (uint32_t)(ch * CKr + 8 * j) / 4;
-                                const uint64_t bd = tc1::umma_desc(wk + cb * LBO_W, LBO_W, 128);
-                                tc1::umma_tf32(d, ad, bd, idesc, (ch | t | j) ? 1u : 0u);
-                                issued = true;
-                            }
-                        }
+                    const uint64_t abase = s == 0 ? a_stage[0] : (s == 1 ? a_stage[1] : a_stage[2]);
+                    const uint64_t *bt = tab_b + ch * n_ent;
+#pragma unroll 4
+                    for (int e = 0; e < n_ent; ++e) {
+                        const uint32_t ae = tab_a[e];
+                        const uint32_t acc = (ch != 0 || !(ae >> 31)) ? 1u : 0u;
+                        tc1::umma_tf32(dbase + ((ae >> 16) & 0xFFu) * (uint32_t)Cout,
+                                       abase + (ae & 0xFFFFu), bt[e], idesc, acc);
                     }
+                    issued = true;
                     tc1::umma_commit(&xt_empty[s]);
                 }
                 if (fail) break;
@@ -275,12 +339,25 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
         }
     } else if (warp >= W_EPI0 && warp < W_EPI0 + 4) {
         // ------------------------------------------------------ epilogue
+        // Per 32-channel slab: each class's accumulator columns (+ bias) go to
+        // their residue slots of a [32][BM*S] staging block, the bias-only
+        // residues are filled in, and the block leaves as 128-bit stores of
+        // consecutive outputs (each channel's BM*S outputs are contiguous).
         const int q = warp - W_EPI0;   // tensor-memory lane quadrant (= warp % 4)
         const int row = q * 32 + lane;
-        uint32_t tile = 0;
-        for (long long u = blockIdx.x; u < n_units && !abort_flag; u += gridDim.x, ++tile) {
+        const int etid = q * 32 + lane;
+        const int span = BM * S;       // outputs of one channel in a tile
+        uint32_t tile = 0, slab = 0;
+        for (long long u = blockIdx.x; u < n_units; u += gridDim.x, ++tile) {
             const uint32_t b = tile & 1u;
-            if (!mbar_wait(&acc_full[b], (tile >> 1) & 1u)) {
+            // The four warps meet at named barriers below, so they must agree on
+            // whether to go on: each posts its wait result, all read all four.
+            const bool ok = mbar_wait(&acc_full[b], (tile >> 1) & 1u);
+            if (lane == 0) epi_ok[q] = ok ? 1 : 0;
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            const bool all_ok = epi_ok[0] && epi_ok[1] && epi_ok[2] && epi_ok[3];
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (!all_ok) {
                 record_error(status, APS_DEVERR_TIMEOUT);
                 abort_flag = 1;
                 break;
@@ -288,57 +365,121 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
             tc1::tc_fence_after();
             const int n = (int)(u / n_mtiles);
             const int mt = (int)(u - (long long)n * n_mtiles);
-            const long long o_base = (long long)(mt * BM + row) * S;   // output of residue 0
-            const bool any = o_base < L_out;
-            float *yn = y + (long long)n * Cout * L_out;
-            for (int c0 = 0; c0 < Cout; c0 += 32) {
-                float v[MAX_CLASSES][32];
+            const long long o0 = (long long)mt * span;
+            if (tma_store) {
+                for (int c0 = 0; c0 < Cout; c0 += SLAB, ++slab) {
+                    float *st_buf = ost + (slab % NBUF) * (SLAB * span);
+                    // the store issued from this buffer NBUF slabs ago has read it
+                    if (etid == 0) bulk_wait_read<NBUF - 1>();
+                    asm volatile("bar.sync 1, 128;" ::: "memory");
+                    for (int c = 0; c < taps.nclass; ++c) {
+                        const uint32_t col = tmem_base + ((uint32_t)(q * 32) << 16) +
+                                             (b * taps.nclass + c) * (uint32_t)Cout + c0;
+                        float *dst = st_buf + S * row + taps.cls_r[c];
+                        const float4 *b4 = reinterpret_cast<const float4 *>(bs + c0);
+                        if (SLAB == 32) {
+                            uint32_t r[32];
+                            tc1::tmem_ld32(col, r);
 #pragma unroll
-                for (int c = 0; c < MAX_CLASSES; ++c) {
-                    if (c < taps.nclass) {
-                        uint32_t r[32];
-                        tc1::tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) +
-                                           (b * taps.nclass + c) * (uint32_t)Cout + c0,
-                                       r);
+                            for (int j = 0; j < 32; j += 4) {
+                                const float4 bv = b4[j / 4];
+                                dst[(j + 0) * span] = __uint_as_float(r[j + 0]) + bv.x;
+                                dst[(j + 1) * span] = __uint_as_float(r[j + 1]) + bv.y;
+                                dst[(j + 2) * span] = __uint_as_float(r[j + 2]) + bv.z;
+                                dst[(j + 3) * span] = __uint_as_float(r[j + 3]) + bv.w;
+                            }
+                        } else {
+                            uint32_t r[16];
+                            tc1::tmem_ld16(col, r);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) v[c][j] = __uint_as_float(r[j]);
-                    }
-                }
-                if (!any) continue;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int co = c0 + j;
-                    const float bv = bs[co];
-                    float *yp = yn + (long long)co * L_out + o_base;
-                    if (S == 1) {
-                        yp[0] = v[0][j] + bv;
-                    } else {
-                        for (int r = 0; r < S; ++r) {
-                            if (o_base + r >= L_out) break;
-                            float val = bv;
-#pragma unroll
-                            for (int c = 0; c < MAX_CLASSES; ++c)
-                                if (c < taps.nclass && taps.cls_r[c] == r) val += v[c][j];
-                            yp[r] = val;
+                            for (int j = 0; j < 16; j += 4) {
+                                const float4 bv = b4[j / 4];
+                                dst[(j + 0) * span] = __uint_as_float(r[j + 0]) + bv.x;
+                                dst[(j + 1) * span] = __uint_as_float(r[j + 1]) + bv.y;
+                                dst[(j + 2) * span] = __uint_as_float(r[j + 2]) + bv.z;
+                                dst[(j + 3) * span] = __uint_as_float(r[j + 3]) + bv.w;
+                            }
                         }
                     }
+                    for (int e = 0; e < taps.nempty; ++e) {
+                        float *dst = st_buf + S * row + taps.empty_r[e];
+                        for (int j = 0; j < SLAB; ++j) dst[j * span] = bs[c0 + j];
+                    }
+                    if (c0 + SLAB >= Cout) {
+                        // accumulator fully read: the MMA may start the next tile on it
+                        tc1::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&acc_empty[b]);
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    asm volatile("bar.sync 1, 128;" ::: "memory");
+                    if (etid == 0) {
+                        tma_store_3d(&ymap, st_buf, (int)o0, c0, n);
+                        bulk_commit();
+                    }
                 }
+                continue;
             }
-            tc1::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[b]);
+            float *yn = y + (long long)n * Cout * L_out;
+            for (int c0 = 0; c0 < Cout; c0 += 32) {
+                for (int c = 0; c < taps.nclass; ++c) {
+                    uint32_t r[32];
+                    tc1::tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) +
+                                       (b * taps.nclass + c) * (uint32_t)Cout + c0,
+                                   r);
+                    float *dst = ost + S * row + taps.cls_r[c];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) dst[j * OROW] = __uint_as_float(r[j]) + bs[c0 + j];
+                }
+                for (int e = 0; e < taps.nempty; ++e) {
+                    float *dst = ost + S * row + taps.empty_r[e];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) dst[j * OROW] = bs[c0 + j];
+                }
+                if (c0 + 32 >= Cout) {
+                    tc1::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&acc_empty[b]);
+                }
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                if (vec_store) {
+                    const int per_row = span / 4;
+                    for (int idx = etid; idx < 32 * per_row; idx += 128) {
+                        const int cl = idx / per_row, qv = idx - cl * per_row;
+                        const long long o = o0 + 4 * qv;
+                        if (o >= L_out) continue;
+                        const float4 v = *reinterpret_cast<const float4 *>(ost + cl * OROW + 4 * qv);
+                        float *yp = yn + (long long)(c0 + cl) * L_out + o;
+                        if (o + 4 <= L_out) {
+                            *reinterpret_cast<float4 *>(yp) = v;
+                        } else {
+                            yp[0] = v.x;
+                            if (o + 1 < L_out) yp[1] = v.y;
+                            if (o + 2 < L_out) yp[2] = v.z;
+                        }
+                    }
+                } else {
+                    for (int idx = etid; idx < 32 * span; idx += 128) {
+                        const int cl = idx / span, t = idx - cl * span;
+                        if (o0 + t < L_out) yn[(long long)(c0 + cl) * L_out + o0 + t] = ost[cl * OROW + t];
+                    }
+                }
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+            }
         }
+        // stores issued from shared memory complete before the CTA exits
+        if (tma_store && etid == 0) bulk_wait<0>();
     } else {
         // ------------------------------------------------------ converters
-        const int ctid = converter_id(warp) * 32 + lane;
+        // converter warp cb owns channels 4cb..4cb+3 of every chunk
+        const int cb = converter_id(warp);
         const int pblocks = BW / 4;
-        const int nblocks = (CKr / 4) * pblocks;
         uint32_t it = 0;
         for (long long u = blockIdx.x; u < n_units && !abort_flag; u += gridDim.x) {
             bool fail = false;
             for (int ch = 0; ch < nchunks; ++ch, ++it) {
-                const uint32_t rs = it % RAW_STAGES, xs = it % XT_STAGES;
-                if (!mbar_wait(&raw_full[rs], (it / RAW_STAGES) & 1u) ||
+                const uint32_t rs = it % RS, xs = it % XT_STAGES;
+                if (!mbar_wait(&raw_full[rs], (it / RS) & 1u) ||
                     (it >= (uint32_t)XT_STAGES &&
                      !mbar_wait(&xt_empty[xs], ((it / XT_STAGES) & 1u) ^ 1u))) {
                     record_error(status, APS_DEVERR_TIMEOUT);
@@ -346,27 +487,24 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
                     fail = true;
                     break;
                 }
-                const float *src = reinterpret_cast<const float *>(raw + rs * RAW_STRIDE);
-                unsigned char *dst = xt + xs * XT_STRIDE;
-                for (int blk = ctid; blk < nblocks; blk += 128) {
-                    const int cb = blk / pblocks, pb = blk - cb * pblocks;
-                    const float *s0 = src + (size_t)(4 * cb) * BW + 4 * pb;
-                    const float4 r0 = *reinterpret_cast<const float4 *>(s0);
-                    const float4 r1 = *reinterpret_cast<const float4 *>(s0 + BW);
-                    const float4 r2 = *reinterpret_cast<const float4 *>(s0 + 2 * BW);
-                    const float4 r3 = *reinterpret_cast<const float4 *>(s0 + 3 * BW);
-                    const float a[4][4] = {{r0.x, r0.y, r0.z, r0.w}, {r1.x, r1.y, r1.z, r1.w},
-                                           {r2.x, r2.y, r2.z, r2.w}, {r3.x, r3.y, r3.z, r3.w}};
-                    unsigned char *d0 = dst + cb * LBO_X + (size_t)(4 * pb) * 16;
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        const int j = (jj + pb) & 3;   // rotate to spread banks
-                        uint4 v;
-                        v.x = tc1::to_tf32(a[0][j]);
-                        v.y = tc1::to_tf32(a[1][j]);
-                        v.z = tc1::to_tf32(a[2][j]);
-                        v.w = tc1::to_tf32(a[3][j]);
-                        *reinterpret_cast<uint4 *>(d0 + j * 16) = v;
+                if (cb < CKr / 4) {
+                    const float *s0 = reinterpret_cast<const float *>(raw + rs * RAW_STRIDE) +
+                                      (size_t)(4 * cb) * BW;
+                    unsigned char *d0 = xt + xs * XT_STRIDE + cb * LBO_X;
+                    for (int pb = lane; pb < pblocks; pb += 32) {
+                        const float4 r0 = *reinterpret_cast<const float4 *>(s0 + 4 * pb);
+                        const float4 r1 = *reinterpret_cast<const float4 *>(s0 + BW + 4 * pb);
+                        const float4 r2 = *reinterpret_cast<const float4 *>(s0 + 2 * BW + 4 * pb);
+                        const float4 r3 = *reinterpret_cast<const float4 *>(s0 + 3 * BW + 4 * pb);
+                        uint4 *dp = reinterpret_cast<uint4 *>(d0 + (size_t)(4 * pb) * 16);
+                        dp[0] = make_uint4(tc1::to_tf32(r0.x), tc1::to_tf32(r1.x), tc1::to_tf32(r2.x),
+                                           tc1::to_tf32(r3.x));
+                        dp[1] = make_uint4(tc1::to_tf32(r0.y), tc1::to_tf32(r1.y), tc1::to_tf32(r2.y),
+                                           tc1::to_tf32(r3.y));
+                        dp[2] = make_uint4(tc1::to_tf32(r0.z), tc1::to_tf32(r1.z), tc1::to_tf32(r2.z),
+                                           tc1::to_tf32(r3.z));
+                        dp[3] = make_uint4(tc1::to_tf32(r0.w), tc1::to_tf32(r1.w), tc1::to_tf32(r2.w),
+                                           tc1::to_tf32(r3.w));
                     }
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -433,6 +571,11 @@ aps_status launch_convt1d_tf32(const float *x, const int64_t in[3], const float 
         }
     }
     if (taps.nclass == 0) return APS_ERR_UNSUPPORTED;
+    for (int r = 0; r < s; ++r) {
+        bool has = false;
+        for (int c = 0; c < taps.nclass; ++c) has = has || taps.cls_r[c] == r;
+        if (!has) taps.empty_r[taps.nempty++] = r;
+    }
     // window of a tile at m0: inputs m0 + ph + emin .. m0 + 127 + ph + emax, start
     // rounded down to a multiple of 4 (16-byte TMA coordinate)
     const int lo = ph + emin;
@@ -451,9 +594,23 @@ aps_status launch_convt1d_tf32(const float *x, const int64_t in[3], const float 
     const uint32_t XT_STRIDE = ((uint32_t)(CKr / 4) * LBO_X + 1023) & ~1023u;
     const uint32_t RAW_STRIDE = ((uint32_t)CKr * BW * 4 + 1023) & ~1023u;
     const size_t w_bytes = (size_t)k * Cin * c_out * 4;
-    const size_t smem = XT_STAGES * XT_STRIDE + RAW_STAGES * RAW_STRIDE + w_bytes +
-                        ((c_out + 1) & ~1) * 4 + (2 * RAW_STAGES + 2 * XT_STAGES + 5) * 8 + 16;
-    if (smem > 227 * 1024) return APS_ERR_UNSUPPORTED;
+    // the output leaves by TMA store when a tile's outputs form a <= 256-wide box
+    // and the output rows are 16-byte strided
+    const int tma_store = (s <= 2 && l_out % 4 == 0) ? 1 : 0;
+    const size_t ost_bytes = tma_store ? (size_t)NBUF * (s == 1 ? 32 : 16) * BM * s * 4
+                                       : (size_t)32 * (BM * s + 4) * 4;
+    int n_ent = 0;
+    for (int c = 0; c < taps.nclass; ++c) n_ent += taps.ntaps[c] * (CKr / 8);
+    if (n_ent * (int)(Cin / CKr) > MAX_MMA_TAB) return APS_ERR_UNSUPPORTED;
+    const size_t fixed = XT_STAGES * XT_STRIDE + w_bytes + (size_t)c_out * 4 + 1024 + ost_bytes +
+                         (2 * RAW_STAGES + 2 * XT_STAGES + 5) * 8 + 16 + MAX_MMA_TAB * 8 +
+                         MAX_MMA_TAB * 4;
+    // 227 KB per CTA, less the 1 KB of static shared memory the kernel declares
+    const size_t budget = 227 * 1024 - 1024;
+    int RS = RAW_STAGES;
+    while (RS > 2 && fixed + RS * RAW_STRIDE > budget) --RS;
+    const size_t smem = fixed + RS * RAW_STRIDE;
+    if (smem > budget) return APS_ERR_UNSUPPORTED;
 
     CUtensorMap map;
     const cuuint64_t dims[3] = {(cuuint64_t)L, (cuuint64_t)Cin, (cuuint64_t)N};
@@ -464,15 +621,26 @@ aps_status launch_convt1d_tf32(const float *x, const int64_t in[3], const float 
                       strides, box, estr))
         return APS_ERR_UNSUPPORTED;
 
+    CUtensorMap ymap;
+    if (tma_store) {
+        const cuuint64_t ydims[3] = {(cuuint64_t)l_out, (cuuint64_t)c_out, (cuuint64_t)N};
+        const cuuint64_t ystr[2] = {(cuuint64_t)(l_out * 4), (cuuint64_t)(c_out * l_out * 4)};
+        const cuuint32_t ybox[3] = {(cuuint32_t)(BM * s), (cuuint32_t)(s == 1 ? 32 : 16), 1};
+        if (!encode_tiled(&ymap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, y, ydims, ystr, ybox, estr))
+            return APS_ERR_UNSUPPORTED;
+    } else {
+        ymap = map;   // unused
+    }
     const int per_sm = resident_ctas((const void *)convt1d_tf32_kernel, THREADS, (int)smem);
     if (per_sm < 1) return APS_ERR_UNSUPPORTED;
     const int64_t M = ceil_div(l_out, s);
     const int n_mtiles = (int)ceil_div(M, BM);
     const long long n_units = (long long)N * n_mtiles;
     const long long grid = std::min<long long>(n_units, (long long)sm_count());
+    const int vec = (l_out % 4 == 0) && (reinterpret_cast<uintptr_t>(y) % 16 == 0);
     convt1d_tf32_kernel<<<(unsigned)grid, THREADS, smem, st>>>(
-        map, w, bias, y, (int)Cin, (int)c_out, k, s, (int)l_out, n_mtiles, n_units, win0, BW,
-        cols, taps, status_word());
+        map, ymap, w, bias, y, (int)Cin, (int)c_out, k, s, (int)l_out, n_mtiles, n_units, win0,
+        BW, cols, RS, vec, tma_store, taps, status_word());
     return launch_status();
 }
 

@@ -54,6 +54,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=8, help="0 skips the e2e leg")
     ap.add_argument("--workload", type=int, default=HEADLINE_CFG,
                     help="workload of the headline line (default: the avgpool workload)")
+    ap.add_argument("--precision", choices=["fp32", "tf32"], default="fp32",
+                    help="ConvTranspose1d precision of the headline workload")
     ap.add_argument("--x-shape", type=str, default=None,
                     help="override the input shape of the headline workload (profiling "
                          "runs on small cases), e.g. 2,32,128,128,256")
@@ -435,7 +437,8 @@ def run_native(args):
 
     # ---- headline: each rank runs its own full workload (weak scaling)
     x_shape = tuple(int(v) for v in args.x_shape.split(",")) if args.x_shape else None
-    case = GpuCase(args.workload, torch, aps, with_host=args.e2e_steps > 0, x_shape=x_shape)
+    case = GpuCase(args.workload, torch, aps, with_host=args.e2e_steps > 0, x_shape=x_shape,
+                   precision=1 if args.precision == "tf32" else 0)
     for _ in range(max(3, args.warmup)):
         case.launch()
     barrier()
@@ -488,7 +491,8 @@ def run_native(args):
     roof = roofline_for(case, per_launch, peaks, peak_src, clocks.get("sm_mhz"))
     kernel_of = {"avgpool3d": ("avgpool3d.cu", "avgpool3d_k3s2p1_tma_kernel"),
                  "ct3d_scale_pool_bias": ("ct3d_pool.cu", "ct3d_pool2_fast_kernel"),
-                 "convtranspose1d": ("convt1d.cu", "convt1d_tiled_kernel")}[case.wl.op]
+                 "convtranspose1d": (("convt1d_tc.cu", "convt1d_tf32_kernel") if case.precision
+                                     else ("convt1d.cu", "convt1d_tiled_kernel"))}[case.wl.op]
     roof["kernel"] = kernel_of[1]
     roof["algorithmic_bytes_per_launch"] = case.bytes
     roof["traffic"] = (traffic_from_profile(kernel_of[0], "avgpool3d_k3s2p1_tma.md")
