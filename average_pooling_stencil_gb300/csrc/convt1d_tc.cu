@@ -17,7 +17,7 @@
 //    ring of up to 4 stages, and an L2 prefetch of the box 12 steps ahead (one
 //    CTA per SM holds few stages; the prefetch keeps enough bytes in flight).
 //    Warp 0 also owns the tensor-memory allocation.
-//  * warps 2, 3, 8..13 -- converters (one per 4 channels): transpose each raw
+//  * warps 2, 3, 12..17 -- converters (one per 4 channels): transpose each raw
 //    box into the K-major,
 //    no-swizzle operand layout (8-row x 16-byte core matrices; rows = window
 //    positions, 4 channels per 16 bytes, one block of rows per 4 channels) and
@@ -27,12 +27,14 @@
 //  * warp 1, lane 0  -- MMA issuer: walks a per-CTA table of descriptors and,
 //    per chunk and (class, tap), issues CK/8 tcgen05.mma
 //    kind::tf32 of 128 x C_out x 8 into the class's accumulator in tensor memory
-//    (double-buffered across tiles), then tcgen05.commit to release the
+//    (a ring of up to 8 tiles' accumulators, as many as 512 columns hold, so the
+//    epilogue's latency never stalls the MMAs), then tcgen05.commit to release the
 //    operand stage and, after the last chunk, to hand the tile to the epilogue.
-//  * warps 4..7 -- epilogue: tcgen05.ld of their 32 accumulator rows, + bias,
+//  * warps 4..11 -- epilogue, two groups of four taking alternate slabs:
+//    tcgen05.ld of their 32 accumulator rows, + bias,
 //    into shared-memory slabs laid out like the output (class r of position
 //    m at s*m + r; residues no tap reaches hold the bias).  With stride <= 2
-//    each 16 KB slab leaves by one TMA tensor store (4 slabs in flight);
+//    each 16 KB slab leaves by one TMA tensor store (2 per group in flight);
 //    otherwise by 128-bit coalesced stores of each channel's s*128 outputs.
 // Weights are rounded to tf32 once per CTA into shared memory in the same
 // K-major layout, one [C_in/4][C_out][4] block per tap.  Every wait is bounded;
@@ -51,10 +53,12 @@ constexpr int RAW_STAGES = 4;    // at most; the launcher may use fewer to fit s
 constexpr int XT_STAGES = 3;
 constexpr int MAX_CLASSES = 4;
 constexpr int MAX_TAPS = 8;       // taps per class
-constexpr int NBUF = 4;           // TMA-store staging slabs in flight
+constexpr int NBUF = 4;           // TMA-store staging slabs in flight (at most; 2 if smem is short)
+constexpr int MAX_ACC = 8;        // accumulator buffers in tensor memory (at most)
 constexpr int PREFETCH = 12;      // input boxes prefetched into L2 ahead of the loads
-constexpr int THREADS = 448;      // 14 warps
-constexpr int CONVERTERS = 8;     // converter warps: 2, 3, 8..13
+constexpr int THREADS = 576;      // 18 warps
+constexpr int CONVERTERS = 8;     // converter warps: 2, 3, 12..17
+constexpr int EPI_WARPS = 8;      // two epilogue groups of four warps: 4..7 and 8..11
 constexpr int MAX_MMA_TAB = 256;  // (chunk, class, tap, k-step) entries of one tile
 constexpr int W_PRODUCER = 0, W_MMA = 1, W_EPI0 = 4;
 
@@ -69,7 +73,11 @@ struct Taps {
 };
 
 __device__ __forceinline__ int converter_id(int warp) {
-    return warp == 2 ? 0 : warp == 3 ? 1 : warp - 6;   // warps 2, 3, 8..13
+    return warp == 2 ? 0 : warp == 3 ? 1 : warp - 10;   // warps 2, 3, 12..17
+}
+
+__device__ __forceinline__ void named_bar(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 __device__ __forceinline__ uint32_t to_tf32(float v) {
@@ -141,7 +149,8 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
                         const __grid_constant__ CUtensorMap ymap, const float *__restrict__ w,
                         const float *__restrict__ bias, float *__restrict__ y, int Cin, int Cout,
                         int K, int S, int L_out, int n_mtiles, long long n_units, int win0, int BW,
-                        int tmem_cols, int RS, int vec_store, int tma_store,
+                        int tmem_cols, int nacc, int RS, int nbuf, int dgroups, int vec_store,
+                        int tma_store,
                         const __grid_constant__ tc1::Taps taps, unsigned int *status) {
     using namespace tc1;
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -164,12 +173,12 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
     const uint32_t ost_off =
         ((uint32_t)(reinterpret_cast<unsigned char *>(bs + Cout) - smem) + 1023u) & ~1023u;
     float *ost = reinterpret_cast<float *>(smem + ost_off);
-    const int ost_floats = tma_store ? NBUF * SLAB * BM * S : 32 * OROW;
+    const int ost_floats = tma_store ? nbuf * SLAB * BM * S : dgroups * 32 * OROW;
     uint64_t *bars = reinterpret_cast<uint64_t *>(ost + ost_floats);
     uint64_t *raw_full = bars, *raw_empty = raw_full + RAW_STAGES;
     uint64_t *xt_full = raw_empty + RAW_STAGES, *xt_empty = xt_full + XT_STAGES;
-    uint64_t *acc_full = xt_empty + XT_STAGES, *acc_empty = acc_full + 2;
-    uint64_t *drain = acc_empty + 2;
+    uint64_t *acc_full = xt_empty + XT_STAGES, *acc_empty = acc_full + MAX_ACC;
+    uint64_t *drain = acc_empty + MAX_ACC;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     // MMA descriptor tables: B descriptors per (chunk, entry); per entry the A
     // offset (16-byte units, low 16 bits), class (bits 16..23) and a flag (bit
@@ -177,7 +186,7 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
     uint64_t *tab_b = reinterpret_cast<uint64_t *>(tmem_slot + 2);
     uint32_t *tab_a = reinterpret_cast<uint32_t *>(tab_b + MAX_MMA_TAB);
     __shared__ volatile int abort_flag;
-    __shared__ volatile int epi_ok[4];
+    __shared__ volatile int epi_ok[2][4];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -191,9 +200,9 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
             mbar_init(&xt_full[s], CONVERTERS);
             mbar_init(&xt_empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < nacc; ++b) {
             mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], 4);
+            mbar_init(&acc_empty[b], EPI_WARPS);
         }
         mbar_init(drain, 1);
         abort_flag = 0;
@@ -298,8 +307,9 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
             uint32_t it = 0, tile = 0;
             bool issued = false;
             for (long long u = blockIdx.x; u < n_units && !abort_flag; u += gridDim.x, ++tile) {
-                const uint32_t b = tile & 1u;
-                if (tile >= 2 && !mbar_wait(&acc_empty[b], ((tile >> 1) & 1u) ^ 1u)) {
+                const uint32_t b = tile % (uint32_t)nacc;
+                if (tile >= (uint32_t)nacc &&
+                    !mbar_wait(&acc_empty[b], ((tile / nacc) & 1u) ^ 1u)) {
                     record_error(status, APS_DEVERR_TIMEOUT);
                     abort_flag = 1;
                     break;
@@ -337,26 +347,38 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
                 mbar_wait(drain, 0);
             }
         }
-    } else if (warp >= W_EPI0 && warp < W_EPI0 + 4) {
+    } else if (warp >= W_EPI0 && warp < W_EPI0 + EPI_WARPS) {
         // ------------------------------------------------------ epilogue
-        // Per 32-channel slab: each class's accumulator columns (+ bias) go to
-        // their residue slots of a [32][BM*S] staging block, the bias-only
-        // residues are filled in, and the block leaves as 128-bit stores of
-        // consecutive outputs (each channel's BM*S outputs are contiguous).
-        const int q = warp - W_EPI0;   // tensor-memory lane quadrant (= warp % 4)
+        // Two independent groups of four warps (one warp per tensor-memory lane
+        // quadrant each) take alternate slabs of a tile, so two slabs are in
+        // flight at once.  Per slab: each class's accumulator columns (+ bias)
+        // go to their residue slots of a dense [SLAB][BM*S] staging block, the
+        // bias-only residues are filled in, and the block leaves by one TMA
+        // store (or, when the output rows are not 16-byte strided or s > 2, by
+        // 128-bit coalesced stores from group 0).
+        const int g = (warp - W_EPI0) >> 2;    // epilogue group
+        const int q = warp & 3;                // tensor-memory lane quadrant
         const int row = q * 32 + lane;
-        const int etid = q * 32 + lane;
-        const int span = BM * S;       // outputs of one channel in a tile
-        uint32_t tile = 0, slab = 0;
+        const int gtid = q * 32 + lane;        // thread index within the group
+        const int bar_id = 1 + g;
+        const int span = BM * S;               // outputs of one channel in a tile
+        const int nslab = tma_store ? Cout / SLAB : Cout / 32;
+        const int nbg = nbuf / 2;              // staging slabs per group (1 or 2)
+        auto release = [&](uint32_t b) {       // this warp is done reading the accumulator
+            tc1::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[b]);
+        };
+        uint32_t tile = 0, gs = 0;
         for (long long u = blockIdx.x; u < n_units; u += gridDim.x, ++tile) {
-            const uint32_t b = tile & 1u;
-            // The four warps meet at named barriers below, so they must agree on
-            // whether to go on: each posts its wait result, all read all four.
-            const bool ok = mbar_wait(&acc_full[b], (tile >> 1) & 1u);
-            if (lane == 0) epi_ok[q] = ok ? 1 : 0;
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            const bool all_ok = epi_ok[0] && epi_ok[1] && epi_ok[2] && epi_ok[3];
-            asm volatile("bar.sync 1, 128;" ::: "memory");
+            const uint32_t b = tile % (uint32_t)nacc;
+            // The group's warps meet at named barriers below, so they must agree
+            // on whether to go on: each posts its wait result, all read all four.
+            const bool ok = mbar_wait(&acc_full[b], (tile / nacc) & 1u);
+            if (lane == 0) epi_ok[g][q] = ok ? 1 : 0;
+            named_bar(bar_id, 128);
+            const bool all_ok = epi_ok[g][0] && epi_ok[g][1] && epi_ok[g][2] && epi_ok[g][3];
+            named_bar(bar_id, 128);
             if (!all_ok) {
                 record_error(status, APS_DEVERR_TIMEOUT);
                 abort_flag = 1;
@@ -367,11 +389,17 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
             const int mt = (int)(u - (long long)n * n_mtiles);
             const long long o0 = (long long)mt * span;
             if (tma_store) {
-                for (int c0 = 0; c0 < Cout; c0 += SLAB, ++slab) {
-                    float *st_buf = ost + (slab % NBUF) * (SLAB * span);
-                    // the store issued from this buffer NBUF slabs ago has read it
-                    if (etid == 0) bulk_wait_read<NBUF - 1>();
-                    asm volatile("bar.sync 1, 128;" ::: "memory");
+                for (int i = g; i < nslab; i += 2, ++gs) {
+                    const int c0 = i * SLAB;
+                    float *st_buf = ost + (g * nbg + gs % nbg) * (SLAB * span);
+                    // the store issued from this buffer nbg slabs ago has read it
+                    if (gtid == 0) {
+                        if (nbg >= 2)
+                            bulk_wait_read<1>();
+                        else
+                            bulk_wait_read<0>();
+                    }
+                    named_bar(bar_id, 128);
                     for (int c = 0; c < taps.nclass; ++c) {
                         const uint32_t col = tmem_base + ((uint32_t)(q * 32) << 16) +
                                              (b * taps.nclass + c) * (uint32_t)Cout + c0;
@@ -405,50 +433,47 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
                         float *dst = st_buf + S * row + taps.empty_r[e];
                         for (int j = 0; j < SLAB; ++j) dst[j * span] = bs[c0 + j];
                     }
-                    if (c0 + SLAB >= Cout) {
-                        // accumulator fully read: the MMA may start the next tile on it
-                        tc1::tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&acc_empty[b]);
-                    }
+                    if (i + 2 >= nslab) release(b);   // last slab of this group
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    asm volatile("bar.sync 1, 128;" ::: "memory");
-                    if (etid == 0) {
+                    named_bar(bar_id, 128);
+                    if (gtid == 0) {
                         tma_store_3d(&ymap, st_buf, (int)o0, c0, n);
                         bulk_commit();
                     }
                 }
+                if (g >= nslab) release(b);           // no slab for this group
                 continue;
             }
+            // direct stores: group g (of dgroups, 1 or 2 as shared memory allows)
+            // stages 32-channel slabs i = g, g+dgroups, ... in its own [32][OROW]
+            // block and writes them with 128-bit stores
             float *yn = y + (long long)n * Cout * L_out;
-            for (int c0 = 0; c0 < Cout; c0 += 32) {
+            float *gst = ost + g * 32 * OROW;
+            for (int i = g; i < nslab && g < dgroups; i += dgroups) {
+                const int c0 = i * 32;
                 for (int c = 0; c < taps.nclass; ++c) {
                     uint32_t r[32];
                     tc1::tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) +
                                        (b * taps.nclass + c) * (uint32_t)Cout + c0,
                                    r);
-                    float *dst = ost + S * row + taps.cls_r[c];
+                    float *dst = gst + S * row + taps.cls_r[c];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) dst[j * OROW] = __uint_as_float(r[j]) + bs[c0 + j];
                 }
                 for (int e = 0; e < taps.nempty; ++e) {
-                    float *dst = ost + S * row + taps.empty_r[e];
+                    float *dst = gst + S * row + taps.empty_r[e];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) dst[j * OROW] = bs[c0 + j];
                 }
-                if (c0 + 32 >= Cout) {
-                    tc1::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&acc_empty[b]);
-                }
-                asm volatile("bar.sync 1, 128;" ::: "memory");
+                if (i + dgroups >= nslab) release(b);
+                named_bar(bar_id, 128);
                 if (vec_store) {
                     const int per_row = span / 4;
-                    for (int idx = etid; idx < 32 * per_row; idx += 128) {
+                    for (int idx = gtid; idx < 32 * per_row; idx += 128) {
                         const int cl = idx / per_row, qv = idx - cl * per_row;
                         const long long o = o0 + 4 * qv;
                         if (o >= L_out) continue;
-                        const float4 v = *reinterpret_cast<const float4 *>(ost + cl * OROW + 4 * qv);
+                        const float4 v = *reinterpret_cast<const float4 *>(gst + cl * OROW + 4 * qv);
                         float *yp = yn + (long long)(c0 + cl) * L_out + o;
                         if (o + 4 <= L_out) {
                             *reinterpret_cast<float4 *>(yp) = v;
@@ -459,16 +484,17 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
                         }
                     }
                 } else {
-                    for (int idx = etid; idx < 32 * span; idx += 128) {
+                    for (int idx = gtid; idx < 32 * span; idx += 128) {
                         const int cl = idx / span, t = idx - cl * span;
-                        if (o0 + t < L_out) yn[(long long)(c0 + cl) * L_out + o0 + t] = ost[cl * OROW + t];
+                        if (o0 + t < L_out) yn[(long long)(c0 + cl) * L_out + o0 + t] = gst[cl * OROW + t];
                     }
                 }
-                asm volatile("bar.sync 1, 128;" ::: "memory");
+                named_bar(bar_id, 128);
             }
+            if (g >= nslab || g >= dgroups) release(b);
         }
         // stores issued from shared memory complete before the CTA exits
-        if (tma_store && etid == 0) bulk_wait<0>();
+        if (tma_store && gtid == 0) bulk_wait<0>();
     } else {
         // ------------------------------------------------------ converters
         // converter warp cb owns channels 4cb..4cb+3 of every chunk
@@ -585,31 +611,49 @@ aps_status launch_convt1d_tf32(const float *x, const int64_t in[3], const float 
     if (BW > 256) return APS_ERR_UNSUPPORTED;
     for (int c = 0; c < taps.nclass; ++c)
         for (int t = 0; t < taps.ntaps[c]; ++t) taps.tap_row[c][t] = ph + ce[c][t] - win0;
+    // as many accumulator buffers as fit in the 512 tensor-memory columns (>= 2)
+    int nacc = 512 / (taps.nclass * (int)c_out);
+    if (nacc > MAX_ACC) nacc = MAX_ACC;
+    if (nacc < 2) return APS_ERR_UNSUPPORTED;
     int cols = 32;
-    while (cols < 2 * taps.nclass * (int)c_out) cols *= 2;
-    if (cols > 512) return APS_ERR_UNSUPPORTED;
+    while (cols < nacc * taps.nclass * (int)c_out) cols *= 2;
 
     const int CKr = Cin < CK ? (int)Cin : CK;
     const uint32_t LBO_X = (uint32_t)BW * 16 + 16;
     const uint32_t XT_STRIDE = ((uint32_t)(CKr / 4) * LBO_X + 1023) & ~1023u;
     const uint32_t RAW_STRIDE = ((uint32_t)CKr * BW * 4 + 1023) & ~1023u;
     const size_t w_bytes = (size_t)k * Cin * c_out * 4;
+    int n_ent = 0;   // MMAs per chunk; the descriptor table holds them for every chunk
+    for (int c = 0; c < taps.nclass; ++c) n_ent += taps.ntaps[c] * (CKr / 8);
+    if (n_ent * (int)(Cin / CKr) > MAX_MMA_TAB) return APS_ERR_UNSUPPORTED;
     // the output leaves by TMA store when a tile's outputs form a <= 256-wide box
     // and the output rows are 16-byte strided
     const int tma_store = (s <= 2 && l_out % 4 == 0) ? 1 : 0;
-    const size_t ost_bytes = tma_store ? (size_t)NBUF * (s == 1 ? 32 : 16) * BM * s * 4
-                                       : (size_t)32 * (BM * s + 4) * 4;
-    int n_ent = 0;
-    for (int c = 0; c < taps.nclass; ++c) n_ent += taps.ntaps[c] * (CKr / 8);
-    if (n_ent * (int)(Cin / CKr) > MAX_MMA_TAB) return APS_ERR_UNSUPPORTED;
-    const size_t fixed = XT_STAGES * XT_STRIDE + w_bytes + (size_t)c_out * 4 + 1024 + ost_bytes +
-                         (2 * RAW_STAGES + 2 * XT_STAGES + 5) * 8 + 16 + MAX_MMA_TAB * 8 +
-                         MAX_MMA_TAB * 4;
     // 227 KB per CTA, less the 1 KB of static shared memory the kernel declares
     const size_t budget = 227 * 1024 - 1024;
-    int RS = RAW_STAGES;
-    while (RS > 2 && fixed + RS * RAW_STRIDE > budget) --RS;
-    const size_t smem = fixed + RS * RAW_STRIDE;
+    // deepest input ring and store staging that fit: 4 staging slabs if the
+    // raw ring can still hold 2 stages, otherwise 2
+    // (for direct stores: two epilogue groups' staging blocks, else one)
+    int RS = RAW_STAGES, nbuf = tma_store ? NBUF : 0, dgroups = tma_store ? 0 : 2;
+    size_t smem = 0;
+    for (;;) {
+        const size_t ost_bytes = tma_store ? (size_t)nbuf * (s == 1 ? 32 : 16) * BM * s * 4
+                                           : (size_t)dgroups * 32 * (BM * s + 4) * 4;
+        const size_t fixed = XT_STAGES * XT_STRIDE + w_bytes + (size_t)c_out * 4 + 1024 +
+                             ost_bytes + (2 * RAW_STAGES + 2 * XT_STAGES + 2 * MAX_ACC + 1) * 8 +
+                             16 + MAX_MMA_TAB * 8 + MAX_MMA_TAB * 4;
+        RS = RAW_STAGES;
+        while (RS > 2 && fixed + RS * RAW_STRIDE > budget) --RS;
+        smem = fixed + RS * RAW_STRIDE;
+        if (smem <= budget) break;
+        if (tma_store && nbuf == 4) {
+            nbuf = 2;
+        } else if (!tma_store && dgroups == 2) {
+            dgroups = 1;
+        } else {
+            break;
+        }
+    }
     if (smem > budget) return APS_ERR_UNSUPPORTED;
 
     CUtensorMap map;
@@ -640,7 +684,7 @@ aps_status launch_convt1d_tf32(const float *x, const int64_t in[3], const float 
     const int vec = (l_out % 4 == 0) && (reinterpret_cast<uintptr_t>(y) % 16 == 0);
     convt1d_tf32_kernel<<<(unsigned)grid, THREADS, smem, st>>>(
         map, ymap, w, bias, y, (int)Cin, (int)c_out, k, s, (int)l_out, n_mtiles, n_units, win0,
-        BW, cols, RS, vec, tma_store, taps, status_word());
+        BW, cols, nacc, RS, nbuf, dgroups, vec, tma_store, taps, status_word());
     return launch_status();
 }
 
