@@ -49,37 +49,116 @@ constexpr int MAX_PTS = THREADS * P;          // points per segment
 constexpr int XTILE_MAX = 12288;              // floats per staged segment (48 KB)
 }  // namespace ct3
 
+// One segment of rows of one (n, d) output plane from the staged input xt
+// ([C_in][2 planes][PT floats], rows of W): PJ points per thread (strided by
+// the block size, so each store instruction of a warp covers 32 consecutive
+// outputs) x all 16 channels.  CIN_T / W_T fix C_in / W at compile time (0:
+// run time) so that every neighbour offset folds into an immediate.
+template <int PJ, int CIN_T, int W_T>
+__device__ __forceinline__ void fused_segment(const float *__restrict__ xt,
+                                              const float *__restrict__ wsm,
+                                              const float *__restrict__ bsm, float *yt,
+                                              long long cstride, int npts, int Cin_rt, int W_rt,
+                                              int PT) {
+    using namespace ct3;
+    const int Cin = CIN_T ? CIN_T : Cin_rt;
+    const int W = W_T ? W_T : W_rt;
+    const int Wo = W - 1;
+    const int tid = threadIdx.x;
+    int base[PJ];
+    bool valid[PJ];
+#pragma unroll
+    for (int j = 0; j < PJ; ++j) {
+        const int s = tid + j * THREADS;
+        valid[j] = s < npts;
+        const int ss = valid[j] ? s : 0;
+        const int ohl = ss / Wo;
+        base[j] = ohl * W + (ss - ohl * Wo);
+    }
+    float acc[COUT][PJ];
+#pragma unroll
+    for (int co = 0; co < COUT; ++co)
+#pragma unroll
+        for (int j = 0; j < PJ; ++j) acc[co][j] = bsm[co];
+
+#pragma unroll 1
+    for (int ci = 0; ci < Cin; ++ci) {
+        float xv[PJ][8];
+        const float *x0 = xt + (ci * 2) * PT;
+        const float *x1 = x0 + PT;
+#pragma unroll
+        for (int j = 0; j < PJ; ++j) {
+            xv[j][0] = x0[base[j]];
+            xv[j][1] = x0[base[j] + 1];
+            xv[j][2] = x0[base[j] + W];
+            xv[j][3] = x0[base[j] + W + 1];
+            xv[j][4] = x1[base[j]];
+            xv[j][5] = x1[base[j] + 1];
+            xv[j][6] = x1[base[j] + W];
+            xv[j][7] = x1[base[j] + W + 1];
+        }
+        const float4 *wq = reinterpret_cast<const float4 *>(wsm + ci * COUT * 8);
+#pragma unroll
+        for (int co = 0; co < COUT; ++co) {
+            const float4 wl = wq[2 * co], wh = wq[2 * co + 1];
+#pragma unroll
+            for (int j = 0; j < PJ; ++j) {
+                float t = acc[co][j];
+                t = fmaf(xv[j][0], wl.x, t);
+                t = fmaf(xv[j][1], wl.y, t);
+                t = fmaf(xv[j][2], wl.z, t);
+                t = fmaf(xv[j][3], wl.w, t);
+                t = fmaf(xv[j][4], wh.x, t);
+                t = fmaf(xv[j][5], wh.y, t);
+                t = fmaf(xv[j][6], wh.z, t);
+                t = fmaf(xv[j][7], wh.w, t);
+                acc[co][j] = t;
+            }
+        }
+    }
+#pragma unroll
+    for (int co = 0; co < COUT; ++co) {
+        float *yc = yt + co * cstride;
+#pragma unroll
+        for (int j = 0; j < PJ; ++j)
+            if (valid[j]) yc[j * THREADS] = acc[co][j];
+    }
+}
+
+template <int CIN_T, int W_T>
 __global__ void __launch_bounds__(ct3::THREADS, 2)
     ct3d_pool2_fast_kernel(const float *__restrict__ x, const float *__restrict__ w,
                            const float *__restrict__ conv_bias, const float *__restrict__ bias,
-                           float scale1, float scale2, float *__restrict__ y, int Cin, int D,
-                           int H, int W, int TH, long long total_rows, int vec16) {
+                           float scale1, float scale2, float *__restrict__ y, int Cin_rt, int D,
+                           int H, int W_rt, int TH, int PT, long long total_rows, int vec16) {
     using namespace ct3;
+    const int Cin = CIN_T ? CIN_T : Cin_rt;
+    const int W = W_T ? W_T : W_rt;
     extern __shared__ __align__(16) float sm[];
     float *wsm = sm;                               // [Cin][16][8]
     float *bsm = sm + CIN_MAX * COUT * 8;          // [16]
-    const int tile_floats = Cin * 2 * (TH + 1) * W;
+    const int tile_floats = Cin * 2 * PT;
     float *xs0 = bsm + COUT;                       // two staging buffers
     float *xs1 = xs0 + ((tile_floats + 3) & ~3);
     const int Do = D - 1, Ho = H - 1, Wo = W - 1;
     const int tid = threadIdx.x;
 
-    // ---- collapsed weights and folded bias (the page's 8-group sums)
-    const double wscale = (double)scale1 * (double)scale2 * 0.125;
+    // ---- collapsed weights and folded bias (the page's 8-group sums), fp32
+    const float wscale = scale1 * scale2 * 0.125f;
     for (int i = tid; i < Cin * COUT * 8; i += THREADS) {
         const int ci = i / (COUT * 8), co = (i / 8) % COUT, g = i % 8;
         const int a = g >> 2, b = (g >> 1) & 1, c = g & 1;
         const float *wp = w + (size_t)(ci * COUT + co) * 27;
-        double acc = 0.0;
+        float acc = 0.f;
         for (int kd = a ? 0 : 1; kd <= (a ? 0 : 2); ++kd)
             for (int kh = b ? 0 : 1; kh <= (b ? 0 : 2); ++kh)
                 for (int kw = c ? 0 : 1; kw <= (c ? 0 : 2); ++kw)
-                    acc += (double)wp[kd * 9 + kh * 3 + kw];
-        wsm[i] = (float)(acc * wscale);
+                    acc += __ldg(wp + kd * 9 + kh * 3 + kw);
+        wsm[i] = acc * wscale;
     }
     if (tid < COUT) {
-        const double cb = conv_bias ? (double)conv_bias[tid] : 0.0;
-        bsm[tid] = (float)((cb * (double)scale1 + (double)bias[tid]) * (double)scale2);
+        const float cb = conv_bias ? __ldg(conv_bias + tid) : 0.f;
+        bsm[tid] = fmaf(cb, scale1, __ldg(bias + tid)) * scale2;
     }
 
     // ---- this CTA's range of output rows
@@ -95,7 +174,7 @@ __global__ void __launch_bounds__(ct3::THREADS, 2)
         for (int ci = 0; ci < Cin; ++ci)
             for (int a = 0; a < 2; ++a) {
                 const float *src = x + ((((n * Cin + ci) * D + od + a) * H) + oh0) * (long long)W;
-                float *d = dst + (ci * 2 + a) * (TH + 1) * W;
+                float *d = dst + (ci * 2 + a) * PT;
                 if (vec16) {
                     for (int e = tid * 4; e < count; e += THREADS * 4) cp_async_16(d + e, src + e);
                 } else {
@@ -117,6 +196,8 @@ __global__ void __launch_bounds__(ct3::THREADS, 2)
     }
     cp_async_commit();
     int buf = 0;
+    const long long plane_out = (long long)Ho * Wo;
+    const long long cstride = (long long)Do * plane_out;
     while (r < r_end) {
         const long long rn = r + rows;
         int rows_n = 0;
@@ -133,68 +214,15 @@ __global__ void __launch_bounds__(ct3::THREADS, 2)
         const long long plane = r / Ho;
         const int oh0 = (int)(r % Ho);
         const int npts = rows * Wo;
-        const int PT = (TH + 1) * W;
-        int base[P];
-        bool valid[P];
-#pragma unroll
-        for (int j = 0; j < P; ++j) {
-            const int s = tid + j * THREADS;
-            valid[j] = s < npts;
-            const int ss = valid[j] ? s : 0;
-            const int ohl = ss / Wo;
-            base[j] = ohl * W + (ss - ohl * Wo);
-        }
-        float acc[COUT][P];
-#pragma unroll
-        for (int co = 0; co < COUT; ++co)
-#pragma unroll
-            for (int j = 0; j < P; ++j) acc[co][j] = bsm[co];
-
-#pragma unroll 1
-        for (int ci = 0; ci < Cin; ++ci) {
-            float xv[P][8];
-            const float *x0 = xt + (ci * 2) * PT;
-            const float *x1 = x0 + PT;
-#pragma unroll
-            for (int j = 0; j < P; ++j) {
-                xv[j][0] = x0[base[j]];
-                xv[j][1] = x0[base[j] + 1];
-                xv[j][2] = x0[base[j] + W];
-                xv[j][3] = x0[base[j] + W + 1];
-                xv[j][4] = x1[base[j]];
-                xv[j][5] = x1[base[j] + 1];
-                xv[j][6] = x1[base[j] + W];
-                xv[j][7] = x1[base[j] + W + 1];
-            }
-            const float4 *wq = reinterpret_cast<const float4 *>(wsm + ci * COUT * 8);
-#pragma unroll
-            for (int co = 0; co < COUT; ++co) {
-                const float4 wl = wq[2 * co], wh = wq[2 * co + 1];
-#pragma unroll
-                for (int j = 0; j < P; ++j) {
-                    float t = acc[co][j];
-                    t = fmaf(xv[j][0], wl.x, t);
-                    t = fmaf(xv[j][1], wl.y, t);
-                    t = fmaf(xv[j][2], wl.z, t);
-                    t = fmaf(xv[j][3], wl.w, t);
-                    t = fmaf(xv[j][4], wh.x, t);
-                    t = fmaf(xv[j][5], wh.y, t);
-                    t = fmaf(xv[j][6], wh.z, t);
-                    t = fmaf(xv[j][7], wh.w, t);
-                    acc[co][j] = t;
-                }
-            }
-        }
         const long long n = plane / Do;
         const long long od = plane - n * Do;
-        const long long plane_out = (long long)Ho * Wo;
-        float *yb = y + ((n * COUT) * Do + od) * plane_out + (long long)oh0 * Wo;
-#pragma unroll
-        for (int co = 0; co < COUT; ++co) {
-            float *yc = yb + (long long)co * Do * plane_out;
-#pragma unroll
-            for (int j = 0; j < P; ++j)
-                if (valid[j]) yc[tid + j * THREADS] = acc[co][j];
+        float *yt = y + ((n * COUT) * Do + od) * plane_out + (long long)oh0 * Wo + tid;
+        // only as many point slots per thread as the segment needs (block-uniform)
+        switch ((npts + THREADS - 1) / THREADS) {
+            case 1: fused_segment<1, CIN_T, W_T>(xt, wsm, bsm, yt, cstride, npts, Cin, W, PT); break;
+            case 2: fused_segment<2, CIN_T, W_T>(xt, wsm, bsm, yt, cstride, npts, Cin, W, PT); break;
+            case 3: fused_segment<3, CIN_T, W_T>(xt, wsm, bsm, yt, cstride, npts, Cin, W, PT); break;
+            default: fused_segment<4, CIN_T, W_T>(xt, wsm, bsm, yt, cstride, npts, Cin, W, PT); break;
         }
         __syncthreads();   // buffer `buf` is restaged two segments later
         r = rn;
@@ -204,30 +232,48 @@ __global__ void __launch_bounds__(ct3::THREADS, 2)
     cp_async_wait<0>();
 }
 
-aps_status launch_ct3d_pool2_fast(const float *x, const int64_t in[5], const float *w,
-                                  const float *conv_bias, const float *bias, float scale1,
-                                  float scale2, float *y, const int64_t out[5],
-                                  cudaStream_t st) {
+template <int CIN_T, int W_T>
+static aps_status launch_fused_fast(const float *x, const int64_t in[5], const float *w,
+                                    const float *conv_bias, const float *bias, float scale1,
+                                    float scale2, float *y, const int64_t out[5], cudaStream_t st) {
     using namespace ct3;
     const int64_t N = in[0], Cin = in[1], D = in[2], H = in[3], W = in[4];
-    if (Cin < 1 || Cin > CIN_MAX || D < 2 || H < 2 || W < 2 || W > MAX_PTS) return APS_ERR_UNSUPPORTED;
     const int64_t Do = out[2], Ho = out[3], Wo = out[4];
     int64_t TH = std::min<int64_t>(Ho, MAX_PTS / Wo);
     TH = std::min<int64_t>(TH, XTILE_MAX / (Cin * 2 * W) - 1);
     if (TH < 1) return APS_ERR_UNSUPPORTED;
-    const int64_t tile_floats = Cin * 2 * (TH + 1) * W;
+    // staged floats per (ci, input plane): fixed at compile time for a fixed W
+    const int64_t PT = W_T ? (MAX_PTS / (W_T - 1) + 1) * W_T : (TH + 1) * W;
+    if (Cin * 2 * PT > XTILE_MAX) return APS_ERR_UNSUPPORTED;
+    const int64_t tile_floats = Cin * 2 * PT;
     const int smem = (int)((CIN_MAX * COUT * 8 + COUT + 2 * ((tile_floats + 3) & ~3)) * 4);
-    const int per_sm = resident_ctas((const void *)ct3d_pool2_fast_kernel, THREADS, smem);
+    const auto kern = ct3d_pool2_fast_kernel<CIN_T, W_T>;
+    const int per_sm = resident_ctas((const void *)kern, THREADS, smem);
     if (per_sm < 1) return APS_ERR_CUDA;
     const long long total_rows = N * Do * Ho;
     const long long pts = total_rows * Wo;
     long long grid = std::min<long long>((long long)sm_count() * per_sm, ceil_div(pts, THREADS));
     grid = std::max<long long>(grid, 1);
     const int vec16 = (W % 4 == 0) && (reinterpret_cast<uintptr_t>(x) % 16 == 0);
-    ct3d_pool2_fast_kernel<<<(unsigned)grid, THREADS, smem, st>>>(
-        x, w, conv_bias, bias, scale1, scale2, y, (int)Cin, (int)D, (int)H, (int)W, (int)TH,
-        total_rows, vec16);
+    kern<<<(unsigned)grid, THREADS, smem, st>>>(x, w, conv_bias, bias, scale1, scale2, y,
+                                                (int)Cin, (int)D, (int)H, (int)W, (int)TH,
+                                                (int)PT, total_rows, vec16);
     return launch_status();
+}
+
+aps_status launch_ct3d_pool2_fast(const float *x, const int64_t in[5], const float *w,
+                                  const float *conv_bias, const float *bias, float scale1,
+                                  float scale2, float *y, const int64_t out[5],
+                                  cudaStream_t st) {
+    using namespace ct3;
+    const int64_t Cin = in[1], D = in[2], H = in[3], W = in[4];
+    if (Cin < 1 || Cin > CIN_MAX || D < 2 || H < 2 || W < 2 || W > MAX_PTS) return APS_ERR_UNSUPPORTED;
+    // the pages' shapes (3 input channels, rows of 32 and 16) run fully specialised
+    if (Cin == 3 && W == 32)
+        return launch_fused_fast<3, 32>(x, in, w, conv_bias, bias, scale1, scale2, y, out, st);
+    if (Cin == 3 && W == 16)
+        return launch_fused_fast<3, 16>(x, in, w, conv_bias, bias, scale1, scale2, y, out, st);
+    return launch_fused_fast<0, 0>(x, in, w, conv_bias, bias, scale1, scale2, y, out, st);
 }
 
 // ------------------------------------------------------------ direct kernel
