@@ -499,7 +499,6 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
         // ------------------------------------------------------ converters
         // converter warp cb owns channels 4cb..4cb+3 of every chunk
         const int cb = converter_id(warp);
-        const int pblocks = BW / 4;
         uint32_t it = 0;
         for (long long u = blockIdx.x; u < n_units && !abort_flag; u += gridDim.x) {
             bool fail = false;
@@ -516,22 +515,15 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
                 if (cb < CKr / 4) {
                     const float *s0 = reinterpret_cast<const float *>(raw + rs * RAW_STRIDE) +
                                       (size_t)(4 * cb) * BW;
-                    unsigned char *d0 = xt + xs * XT_STRIDE + cb * LBO_X;
-                    for (int pb = lane; pb < pblocks; pb += 32) {
-                        const float4 r0 = *reinterpret_cast<const float4 *>(s0 + 4 * pb);
-                        const float4 r1 = *reinterpret_cast<const float4 *>(s0 + BW + 4 * pb);
-                        const float4 r2 = *reinterpret_cast<const float4 *>(s0 + 2 * BW + 4 * pb);
-                        const float4 r3 = *reinterpret_cast<const float4 *>(s0 + 3 * BW + 4 * pb);
-                        uint4 *dp = reinterpret_cast<uint4 *>(d0 + (size_t)(4 * pb) * 16);
-                        dp[0] = make_uint4(tc1::to_tf32(r0.x), tc1::to_tf32(r1.x), tc1::to_tf32(r2.x),
-                                           tc1::to_tf32(r3.x));
-                        dp[1] = make_uint4(tc1::to_tf32(r0.y), tc1::to_tf32(r1.y), tc1::to_tf32(r2.y),
-                                           tc1::to_tf32(r3.y));
-                        dp[2] = make_uint4(tc1::to_tf32(r0.z), tc1::to_tf32(r1.z), tc1::to_tf32(r2.z),
-                                           tc1::to_tf32(r3.z));
-                        dp[3] = make_uint4(tc1::to_tf32(r0.w), tc1::to_tf32(r1.w), tc1::to_tf32(r2.w),
-                                           tc1::to_tf32(r3.w));
-                    }
+                    // lane -> positions lane, lane+32, ...: the four channel reads
+                    // and the 16-byte row writes of a warp are each contiguous, so
+                    // neither has bank conflicts
+                    uint4 *d0 = reinterpret_cast<uint4 *>(xt + xs * XT_STRIDE + cb * LBO_X);
+#pragma unroll 2
+                    for (int pos = lane; pos < BW; pos += 32)
+                        d0[pos] = make_uint4(tc1::to_tf32(s0[pos]), tc1::to_tf32(s0[BW + pos]),
+                                             tc1::to_tf32(s0[2 * BW + pos]),
+                                             tc1::to_tf32(s0[3 * BW + pos]));
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
