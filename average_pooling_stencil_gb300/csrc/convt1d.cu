@@ -15,17 +15,22 @@
 // all and is just the bias).
 //
 // Tiled kernel (GB300): a CTA computes 64 output channels x 32*Q positions of m
-// (all s classes, i.e. 32*Q*s consecutive outputs) for one batch row, where Q
-// is 8 divided by the number of classes that have taps (8 for stride 1 and
-// for the stride-2, dilation-2 case).  Input
-// channels stream through shared memory in chunks of 8 with double-buffered
-// cp.async: the x window of the chunk (256 + span samples, zero-filled outside
-// [0, L)) and its weights, stored [ci][k][co] so a thread's 8 channels are two
-// float4 broadcast reads.  A warp owns 8 output channels and each lane Q
-// consecutive m: per input channel the lane loads its window (Q + span samples,
-// shared-memory rows padded by one word per 32 so the stride-8 lane pattern is
-// conflict-free) into registers and does 8 x Q x K' FMAs per class from it.
-// Results leave as 128-bit stores of Q*s consecutive outputs per channel.
+// (all s classes, i.e. 32*Q*s consecutive outputs) per unit, where Q is 8
+// divided by the number of classes that have taps; it is persistent and walks
+// (batch row, m-tile) units.  A warp owns 8 output channels and each lane Q
+// consecutive m.  Input channels stream through shared memory in chunks of 8
+// with one continuous double-buffered cp.async pipeline over the CTA's
+// (unit, chunk) sequence: warp w stages channel w of the chunk's window
+// (32*Q + span samples, zero outside [0, L)).  Window rows are padded by one
+// word per Q samples, so lane l's j-th window register sits at row offset
+// (Q+1)*l + j + j/Q -- an immediate per j -- and, Q+1 being odd, the 32 lanes
+// hit 32 different banks.  The weights, stored [ci][k][co] so a warp's 8
+// channels are two float4 broadcast reads, are either resident for the whole
+// CTA (loaded once) or, when the CTA's [C_in][K][64] slab is too large, staged
+// with each chunk.  Accumulators are kept in channel pairs and updated with the
+// packed fp32x2 FMA (two exactly rounded fp32 FMAs per instruction), which
+// halves the FMA issue slots.  Results leave as 128-bit stores of Q*s
+// consecutive outputs per channel.
 //
 // Direct kernel: one thread per output evaluating the formula as written, for
 // any (s, K, d, p).
@@ -40,7 +45,10 @@ constexpr int THREADS = 256;
 constexpr int WARPS = THREADS / 32;
 constexpr int CO_T = 8;                 // output channels per warp
 constexpr int CO_B = WARPS * CO_T;      // 64 output channels per CTA
-constexpr int CI_C = 8;                 // input channels per staged chunk
+constexpr int CI_C = WARPS;             // input channels per staged chunk (one per warp)
+// Resident weights while the CTA's shared memory stays within this, so that
+// two CTAs share an SM.
+constexpr int RESIDENT_SMEM = 110 * 1024;
 
 __host__ __device__ constexpr int floordiv(int a, int b) {
     return (a >= 0) ? a / b : -((-a + b - 1) / b);
@@ -78,137 +86,182 @@ struct Taps {
     }
     // m positions per lane: 8 accumulators per channel whatever the stride
     static constexpr int Q = nclasses() > 1 ? 8 / nclasses() : 8;
-    static constexpr int TM = 32 * Q;                    // m positions per CTA
+    static constexpr int TM = 32 * Q;                    // m positions per CTA unit
     static constexpr int E_MIN = any() ? emin() : 0;
     static constexpr int SPAN = any() ? emax() - emin() : 0;
     static constexpr int XW = TM + SPAN;                 // window samples per channel
-    static constexpr int XW_PAD = XW + XW / 32 + 1;      // padded row length
+    static constexpr int XP = XW + XW / Q + 1;           // padded row (one word per Q)
+    static constexpr int XS = CI_C * XP;                 // floats per window stage
+    static constexpr int WC = CI_C * K * CO_B;           // floats of one chunk's weights
 };
-
-__device__ __forceinline__ int padidx(int j) { return j + (j >> 5); }
 }  // namespace ct1
 
-template <int S, int K, int DIL, int PL>
+template <int S, int K, int DIL, int PL, bool RES>
 __global__ void __launch_bounds__(ct1::THREADS, 2)
     convt1d_tiled_kernel(const float *__restrict__ x, const float *__restrict__ w,
                          const float *__restrict__ bias, float *__restrict__ y, int Cin,
-                         int Cout, int L, int L_out, int ph, int vec_store) {
+                         int Cout, int L, int L_out, int ph, int n_mtiles, long long n_units,
+                         int vec_store) {
     using namespace ct1;
     using T = Taps<S, K, DIL, PL>;
-    constexpr int XW = T::XW, XW_PAD = T::XW_PAD, SPAN = T::SPAN, E_MIN = T::E_MIN;
-    constexpr int Q = T::Q, TM = T::TM;
-    constexpr int XS = CI_C * XW_PAD;             // floats per x stage
-    constexpr int WS = CI_C * K * CO_B;           // floats per w stage
+    constexpr int XW = T::XW, XP = T::XP, XS = T::XS, WC = T::WC;
+    constexpr int SPAN = T::SPAN, E_MIN = T::E_MIN, Q = T::Q, TM = T::TM;
     extern __shared__ __align__(16) float sm[];
-    float *xs = sm;                 // [2][CI_C][XW_PAD]
-    float *ws = sm + 2 * XS;        // [2][CI_C][K][CO_B]
+    // resident: ws = [Cin][K][CO_B]; staged: ws = [2][CI_C][K][CO_B]
+    float *ws = sm;
+    float *xs = sm + (RES ? (size_t)Cin * K * CO_B : (size_t)2 * WC);   // [2][CI_C][XP]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const long long m0 = (long long)blockIdx.x * TM;
     const int co_base = blockIdx.y * CO_B;
-    const long long n = blockIdx.z;
-    const long long i_lo = m0 + ph + E_MIN;       // input index of window sample 0
-    const float *xn = x + n * (long long)Cin * L;
+    const int nchunks = (Cin + CI_C - 1) / CI_C;
 
-    auto stage = [&](int c0, int b) {
-        float *xd = xs + b * XS;
-        float *wd = ws + b * WS;
-        const int nci = min(CI_C, Cin - c0);
-        for (int e = tid; e < CI_C * XW; e += THREADS) {
-            const int cl = e / XW, j = e - cl * XW;
-            const long long i = i_lo + j;
-            const bool in = cl < nci && i >= 0 && i < L;
-            const float *src = in ? xn + (long long)(c0 + cl) * L + i : x;
-            float *dst = xd + cl * XW_PAD + padidx(j);
-            asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)),
-                         "l"(src), "r"(in ? 4 : 0)
-                         : "memory");
-        }
-        for (int e = tid; e < CI_C * CO_B * K; e += THREADS) {
-            // global order [ci][co][k]; shared order [ci][k][co]
+    // weights of input channels c0 .. c0+nci-1: global [ci][co][k] -> shared
+    // [ci - c0][k][co] (zeros for channels past C_out)
+    auto load_w = [&](int c0, int nci, float *dst, bool async) {
+        for (int e = tid; e < nci * CO_B * K; e += THREADS) {
             const int cl = e / (CO_B * K), rem = e - cl * (CO_B * K);
             const int col = rem / K, k = rem - col * K;
             const int co = co_base + col;
-            const bool in = cl < nci && co < Cout;
+            const bool in = co < Cout;
             const float *src = in ? w + ((long long)(c0 + cl) * Cout + co) * K + k : w;
-            float *dst = wd + (cl * K + k) * CO_B + col;
-            asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)),
-                         "l"(src), "r"(in ? 4 : 0)
+            float *d = dst + (cl * K + k) * CO_B + col;
+            if (async)
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(d)),
+                             "l"(src), "r"(in ? 4 : 0)
+                             : "memory");
+            else
+                *d = in ? __ldg(src) : 0.f;
+        }
+    };
+    if (RES) load_w(0, Cin, ws, false);
+
+    // Stage chunk c0 of a unit into buffer b: warp w copies channel c0 + w of
+    // the window.  The unit is given by its batch row's first input channel
+    // (xn) and its window start i_lo; samples j in [j_lo, j_hi) lie inside
+    // [0, L), the rest are zeros.
+    auto stage = [&](const float *xn, long long i_lo, int c0, int b) {
+        if (!RES) load_w(c0, min(CI_C, Cin - c0), ws + b * WC, true);
+        const long long rem = (long long)L - i_lo;   // samples left in the row
+        const int j_lo = i_lo >= 0 ? 0 : (-i_lo < XW ? (int)-i_lo : XW);
+        const int j_hi = rem <= 0 ? 0 : (rem < XW ? (int)rem : XW);
+        const bool chan = c0 + warp < Cin;
+        const float *src = xn + (long long)(chan ? c0 + warp : 0) * L + i_lo + lane;
+        const uint32_t dst = smem_u32(xs + b * XS + warp * XP + lane + lane / Q);
+#pragma unroll 3
+        for (int j = lane, t = 0; j < XW; j += 32, ++t) {
+            const bool in = chan && j >= j_lo && j < j_hi;
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(
+                             dst + 4u * (uint32_t)(t * (32 + 32 / Q))),
+                         "l"(in ? src + 32 * t : x), "r"(in ? 4 : 0)
                          : "memory");
         }
     };
+    auto unit_origin = [&](long long u, const float *&xn, long long &i_lo) {
+        const long long n = u / n_mtiles;
+        xn = x + n * Cin * (long long)L;
+        i_lo = (u - n * n_mtiles) * TM + ph + E_MIN;
+    };
 
-    float acc[CO_T][Q][S];
-#pragma unroll
-    for (int c = 0; c < CO_T; ++c)
-#pragma unroll
-        for (int q = 0; q < Q; ++q)
-#pragma unroll
-            for (int r = 0; r < S; ++r) acc[c][q][r] = 0.f;
-
-    const int nchunks = (Cin + CI_C - 1) / CI_C;
-    stage(0, 0);
+    // accumulators in channel pairs: one packed FMA updates channels 2c2 and
+    // 2c2+1 of one position
+    float2 acc[CO_T / 2][Q][S];
+    long long u = blockIdx.x;
+    int ch = 0, b = 0;
+    const float *xn = x, *xn_next = x;
+    long long i_lo = 0, i_lo_next = 0;
+    if (u < n_units) {
+        unit_origin(u, xn, i_lo);
+        stage(xn, i_lo, 0, 0);
+    }
     cp_async_commit();
-    for (int ch = 0; ch < nchunks; ++ch) {
-        const int b = ch & 1;
-        if (ch + 1 < nchunks) stage((ch + 1) * CI_C, b ^ 1);
+    while (u < n_units) {
+        long long un = u;
+        int chn = ch + 1;
+        xn_next = xn;
+        i_lo_next = i_lo;
+        if (chn == nchunks) {
+            chn = 0;
+            un = u + gridDim.x;
+            if (un < n_units) unit_origin(un, xn_next, i_lo_next);
+        }
+        if (un < n_units) stage(xn_next, i_lo_next, chn * CI_C, b ^ 1);
         cp_async_commit();
         cp_async_wait<1>();
         __syncthreads();
-        const float *xb = xs + b * XS;
-        const float *wb = ws + b * WS + warp * CO_T;
+        if (ch == 0) {
+#pragma unroll
+            for (int c2 = 0; c2 < CO_T / 2; ++c2)
+#pragma unroll
+                for (int q = 0; q < Q; ++q)
+#pragma unroll
+                    for (int r = 0; r < S; ++r) acc[c2][q][r] = make_float2(0.f, 0.f);
+        }
+        const float *xl = xs + b * XS + (Q + 1) * lane;
+        const float *wb = (RES ? ws + (size_t)ch * WC : ws + b * WC) + warp * CO_T;
         const int nci = min(CI_C, Cin - ch * CI_C);
 #pragma unroll 1
         for (int cl = 0; cl < nci; ++cl) {
             float xr[Q + SPAN];
-            const float *xrow = xb + cl * XW_PAD;
 #pragma unroll
-            for (int j = 0; j < Q + SPAN; ++j) xr[j] = xrow[padidx(lane * Q + j)];
+            for (int j = 0; j < Q + SPAN; ++j) xr[j] = xl[cl * XP + j + j / Q];
 #pragma unroll
             for (int k = 0; k < K; ++k) {
                 const float4 wa = *reinterpret_cast<const float4 *>(wb + (cl * K + k) * CO_B);
                 const float4 wc = *reinterpret_cast<const float4 *>(wb + (cl * K + k) * CO_B + 4);
-                const float wv[CO_T] = {wa.x, wa.y, wa.z, wa.w, wc.x, wc.y, wc.z, wc.w};
+                const float2 wp[CO_T / 2] = {make_float2(wa.x, wa.y), make_float2(wa.z, wa.w),
+                                             make_float2(wc.x, wc.y), make_float2(wc.z, wc.w)};
 #pragma unroll
                 for (int r = 0; r < S; ++r) {
                     if (!T::has(r, k)) continue;
                     const int off = T::e(r, k) - E_MIN;
 #pragma unroll
-                    for (int q = 0; q < Q; ++q)
+                    for (int c2 = 0; c2 < CO_T / 2; ++c2)
 #pragma unroll
-                        for (int c = 0; c < CO_T; ++c)
-                            acc[c][q][r] = fmaf(xr[q + off], wv[c], acc[c][q][r]);
+                        for (int q = 0; q < Q; ++q)
+                            acc[c2][q][r] = __ffma2_rn(make_float2(xr[q + off], xr[q + off]),
+                                                       wp[c2], acc[c2][q][r]);
                 }
             }
         }
-        __syncthreads();
+        __syncthreads();   // buffer b is free for the stage issued next iteration
+        if (ch == nchunks - 1) {
+            // ---- epilogue: bias, then Q*S consecutive outputs per channel
+            const long long n = u / n_mtiles;
+            const long long m0 = (u - n * n_mtiles) * TM;
+            const long long o0 = (m0 + (long long)lane * Q) * S;
+#pragma unroll
+            for (int c = 0; c < CO_T; ++c) {
+                const int co = co_base + warp * CO_T + c;
+                if (co >= Cout) break;
+                const float bv = bias ? __ldg(bias + co) : 0.f;
+                float v[Q * S];
+#pragma unroll
+                for (int q = 0; q < Q; ++q)
+#pragma unroll
+                    for (int r = 0; r < S; ++r) {
+                        const float a = (c & 1) ? acc[c / 2][q][r].y : acc[c / 2][q][r].x;
+                        v[q * S + r] = T::class_has_taps(r) ? a + bv : bv;
+                    }
+                float *yp = y + (n * Cout + co) * (long long)L_out + o0;
+                if (vec_store && o0 + Q * S <= L_out) {
+#pragma unroll
+                    for (int t = 0; t < Q * S; t += 4)
+                        *reinterpret_cast<float4 *>(yp + t) =
+                            make_float4(v[t], v[t + 1], v[t + 2], v[t + 3]);
+                } else {
+#pragma unroll
+                    for (int t = 0; t < Q * S; ++t)
+                        if (o0 + t < L_out) yp[t] = v[t];
+                }
+            }
+        }
+        u = un;
+        ch = chn;
+        b ^= 1;
+        xn = xn_next;
+        i_lo = i_lo_next;
     }
     cp_async_wait<0>();
-
-    // ---- epilogue: bias, then 8*S consecutive outputs per channel
-    const long long o0 = (m0 + (long long)lane * Q) * S;
-#pragma unroll
-    for (int c = 0; c < CO_T; ++c) {
-        const int co = co_base + warp * CO_T + c;
-        if (co >= Cout) break;
-        const float bv = bias ? __ldg(bias + co) : 0.f;
-        float v[Q * S];
-#pragma unroll
-        for (int q = 0; q < Q; ++q)
-#pragma unroll
-            for (int r = 0; r < S; ++r)
-                v[q * S + r] = T::class_has_taps(r) ? acc[c][q][r] + bv : bv;
-        float *yp = y + (n * Cout + co) * (long long)L_out + o0;
-        if (vec_store && o0 + Q * S <= L_out) {
-#pragma unroll
-            for (int t = 0; t < Q * S; t += 4)
-                *reinterpret_cast<float4 *>(yp + t) = make_float4(v[t], v[t + 1], v[t + 2], v[t + 3]);
-        } else {
-#pragma unroll
-            for (int t = 0; t < Q * S; ++t)
-                if (o0 + t < L_out) yp[t] = v[t];
-        }
-    }
 }
 
 template <int S, int K, int DIL, int PL>
@@ -217,15 +270,26 @@ static aps_status launch_tiled(const float *x, const int64_t in[3], const float 
                                int64_t l_out, cudaStream_t st) {
     using namespace ct1;
     using T = Taps<S, K, DIL, PL>;
-    const int smem = (2 * CI_C * T::XW_PAD + 2 * CI_C * K * CO_B) * 4;
-    const auto kern = convt1d_tiled_kernel<S, K, DIL, PL>;
-    if (resident_ctas((const void *)kern, THREADS, smem) < 1) return APS_ERR_CUDA;
     const int64_t M = ceil_div(l_out, S);
-    const int64_t gx = ceil_div(M, T::TM), gy = ceil_div(c_out, CO_B), gz = in[0];
-    if (gx >= ((int64_t)1 << 31) || gy > 65535 || gz > 65535) return APS_ERR_UNSUPPORTED;
+    const int64_t gy = ceil_div(c_out, CO_B), n_mtiles = ceil_div(M, T::TM);
+    if (gy > 65535 || n_mtiles >= ((int64_t)1 << 31)) return APS_ERR_UNSUPPORTED;
+    const long long n_units = (long long)in[0] * n_mtiles;
     const int vec = (l_out % 4 == 0) && (reinterpret_cast<uintptr_t>(y) % 16 == 0);
-    kern<<<dim3((unsigned)gx, (unsigned)gy, (unsigned)gz), THREADS, smem, st>>>(
-        x, w, bias, y, (int)in[1], (int)c_out, (int)in[2], (int)l_out, (p - PL) / S, vec);
+    // resident weights when the CTA's slab and two window stages leave room for
+    // two CTAs per SM, otherwise weights staged with each chunk
+    const int64_t rsmem = (in[1] * K * CO_B + 2 * T::XS) * 4;
+    const int ssmem = (2 * T::WC + 2 * T::XS) * 4;
+    const bool res = rsmem <= RESIDENT_SMEM;
+    const auto kern = res ? convt1d_tiled_kernel<S, K, DIL, PL, true>
+                          : convt1d_tiled_kernel<S, K, DIL, PL, false>;
+    const int smem = res ? (int)rsmem : ssmem;
+    const int per_sm = resident_ctas((const void *)kern, THREADS, smem);
+    if (per_sm < 1) return APS_ERR_CUDA;
+    const long long slots = std::max<long long>(1, (long long)per_sm * sm_count() / gy);
+    const long long gx = std::min<long long>(n_units, slots);
+    kern<<<dim3((unsigned)gx, (unsigned)gy, 1), THREADS, (size_t)smem, st>>>(
+        x, w, bias, y, (int)in[1], (int)c_out, (int)in[2], (int)l_out, (p - PL) / S,
+        (int)n_mtiles, n_units, vec);
     return launch_status();
 }
 
