@@ -17,24 +17,27 @@
 // chain in exact arithmetic; in fp32 it differs by rounding only (the page
 // argues the reassociation is far inside an fp32 tolerance).
 //
-// Design (GB300): every CTA collapses the weights itself (C_in*16*27 loads,
-// computed in double, rounded once) into shared memory, so the op is one
-// kernel with no scratch buffer and no host access to the weights.  The
-// output rows of all (n, d) planes form one flat range that is split evenly
-// across a persistent grid; a CTA walks its range in segments of <= TH rows of
-// one plane.  A segment's input (C_in x 2 planes x (rows+1) x W) is staged in
-// shared memory with cp.async, double-buffered so the next segment loads while
-// this one computes.  Each thread owns up to 4 output points of the segment
-// (strided by the block size, so every store instruction of a warp writes 32
-// consecutive floats) and all 16 output channels: per input channel it reads
-// the 8 neighbours of each point once and applies them to 16 channels with
-// broadcast float4 weight reads (16 FMAs per shared-memory load).
+// Design (GB300): one CTA of 4 warps per unit = (batch row, output plane,
+// block of 16 output rows, block of 32 output columns).  The unit's input --
+// C_in channels x 2 planes x 17 rows x (32 or 36) columns -- arrives by one
+// 4-D TMA box (zero-filled outside the tensor), or by 4-byte cp.async when the
+// rows are not 16-byte strided.  While it is in flight the CTA collapses the
+// weights itself (C_in*16*27 loads) into shared memory, so the op is one
+// kernel with no scratch buffer and no host access to the weights.  Lane l
+// owns output column l and warp w output rows 4w..4w+3 of the block, all 16
+// channels: per input channel a thread reads its 2 x 5 x 2 input window once
+// (32 consecutive words per warp load: no bank conflicts) and applies each of
+// the 8 taps to its 4 rows with broadcast float4 weight reads.  Accumulators
+// are channel pairs updated with the packed fp32x2 FMA (two exactly rounded
+// fp32 FMAs per instruction).  Each store instruction of a warp writes one
+// output row segment of 32 consecutive floats.
 //
 // General path: one thread per pooled output evaluates the literal chain with
 // the gather form of the transposed convolution, tap k taken where
 // (o + pad - dil*k) is a non-negative multiple of the stride below the input
 // size in each dim.
 #include <algorithm>
+#include <cstring>
 
 #include "aps_dev.cuh"
 #include "aps_internal.h"
@@ -43,110 +46,103 @@ namespace aps {
 namespace ct3 {
 constexpr int COUT = 16;
 constexpr int CIN_MAX = 8;
-constexpr int THREADS = 256;
-constexpr int P = 4;                          // output points per thread
-constexpr int MAX_PTS = THREADS * P;          // points per segment
-constexpr int XTILE_MAX = 12288;              // floats per staged segment (48 KB)
+constexpr int WARPS = 4;
+constexpr int THREADS = 32 * WARPS;
+constexpr int RPT = 4;                 // output rows per thread
+constexpr int TOH = WARPS * RPT;       // output rows per unit
+constexpr int TOW = 32;                // output columns per unit (one per lane)
+constexpr int XR = TOH + 1;            // input rows per staged plane
+constexpr int SLACK = 64;              // floats after the stage: idle lanes may read past a row
 }  // namespace ct3
 
-// One segment of rows of one (n, d) output plane from the staged input xt
-// ([C_in][2 planes][PT floats], rows of W): PJ points per thread (strided by
-// the block size, so each store instruction of a warp covers 32 consecutive
-// outputs) x all 16 channels.  CIN_T / W_T fix C_in / W at compile time (0:
-// run time) so that every neighbour offset folds into an immediate.
-template <int PJ, int CIN_T, int W_T>
-__device__ __forceinline__ void fused_segment(const float *__restrict__ xt,
-                                              const float *__restrict__ wsm,
-                                              const float *__restrict__ bsm, float *yt,
-                                              long long cstride, int npts, int Cin_rt, int W_rt,
-                                              int PT) {
-    using namespace ct3;
-    const int Cin = CIN_T ? CIN_T : Cin_rt;
-    const int W = W_T ? W_T : W_rt;
-    const int Wo = W - 1;
-    const int tid = threadIdx.x;
-    int base[PJ];
-    bool valid[PJ];
-#pragma unroll
-    for (int j = 0; j < PJ; ++j) {
-        const int s = tid + j * THREADS;
-        valid[j] = s < npts;
-        const int ss = valid[j] ? s : 0;
-        const int ohl = ss / Wo;
-        base[j] = ohl * W + (ss - ohl * Wo);
-    }
-    float acc[COUT][PJ];
-#pragma unroll
-    for (int co = 0; co < COUT; ++co)
-#pragma unroll
-        for (int j = 0; j < PJ; ++j) acc[co][j] = bsm[co];
-
-#pragma unroll 1
-    for (int ci = 0; ci < Cin; ++ci) {
-        float xv[PJ][8];
-        const float *x0 = xt + (ci * 2) * PT;
-        const float *x1 = x0 + PT;
-#pragma unroll
-        for (int j = 0; j < PJ; ++j) {
-            xv[j][0] = x0[base[j]];
-            xv[j][1] = x0[base[j] + 1];
-            xv[j][2] = x0[base[j] + W];
-            xv[j][3] = x0[base[j] + W + 1];
-            xv[j][4] = x1[base[j]];
-            xv[j][5] = x1[base[j] + 1];
-            xv[j][6] = x1[base[j] + W];
-            xv[j][7] = x1[base[j] + W + 1];
-        }
-        const float4 *wq = reinterpret_cast<const float4 *>(wsm + ci * COUT * 8);
-#pragma unroll
-        for (int co = 0; co < COUT; ++co) {
-            const float4 wl = wq[2 * co], wh = wq[2 * co + 1];
-#pragma unroll
-            for (int j = 0; j < PJ; ++j) {
-                float t = acc[co][j];
-                t = fmaf(xv[j][0], wl.x, t);
-                t = fmaf(xv[j][1], wl.y, t);
-                t = fmaf(xv[j][2], wl.z, t);
-                t = fmaf(xv[j][3], wl.w, t);
-                t = fmaf(xv[j][4], wh.x, t);
-                t = fmaf(xv[j][5], wh.y, t);
-                t = fmaf(xv[j][6], wh.z, t);
-                t = fmaf(xv[j][7], wh.w, t);
-                acc[co][j] = t;
-            }
-        }
-    }
-#pragma unroll
-    for (int co = 0; co < COUT; ++co) {
-        float *yc = yt + co * cstride;
-#pragma unroll
-        for (int j = 0; j < PJ; ++j)
-            if (valid[j]) yc[j * THREADS] = acc[co][j];
-    }
-}
-
-template <int CIN_T, int W_T>
-__global__ void __launch_bounds__(ct3::THREADS, 2)
-    ct3d_pool2_fast_kernel(const float *__restrict__ x, const float *__restrict__ w,
+// BW_T: staged row length (columns) fixed at compile time (0: run time), so
+// that every window offset folds into an immediate.
+template <int BW_T>
+__global__ void __launch_bounds__(ct3::THREADS, BW_T ? 4 : 3)
+    ct3d_pool2_fast_kernel(const __grid_constant__ CUtensorMap xmap, int use_tma,
+                           const float *__restrict__ x, const float *__restrict__ w,
                            const float *__restrict__ conv_bias, const float *__restrict__ bias,
-                           float scale1, float scale2, float *__restrict__ y, int Cin_rt, int D,
-                           int H, int W_rt, int TH, int PT, long long total_rows, int vec16) {
+                           float scale1, float scale2, float *__restrict__ y, int Cin, int D,
+                           int H, int W, int BW_rt, int n_owb, long long total_rows,
+                           unsigned int *status) {
     using namespace ct3;
-    const int Cin = CIN_T ? CIN_T : Cin_rt;
-    const int W = W_T ? W_T : W_rt;
-    extern __shared__ __align__(16) float sm[];
-    float *wsm = sm;                               // [Cin][16][8]
-    float *bsm = sm + CIN_MAX * COUT * 8;          // [16]
-    const int tile_floats = Cin * 2 * PT;
-    float *xs0 = bsm + COUT;                       // two staging buffers
-    float *xs1 = xs0 + ((tile_floats + 3) & ~3);
+    const int BW = BW_T ? BW_T : BW_rt;
     const int Do = D - 1, Ho = H - 1, Wo = W - 1;
-    const int tid = threadIdx.x;
+    extern __shared__ __align__(128) float sm[];
+    const int stage_floats = Cin * 2 * XR * BW;
+    const int stage_stride = (stage_floats + SLACK + 31) & ~31;   // 128-byte aligned stages
+    float *xs = sm;                                  // [2][Cin][2][XR][BW]
+    float *wsm = xs + 2 * stage_stride;              // [Cin][8][16]
+    float *bsm = wsm + CIN_MAX * 8 * COUT;           // [16]
+    uint64_t *bar = reinterpret_cast<uint64_t *>(bsm + COUT);   // [2]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-    // ---- collapsed weights and folded bias (the page's 8-group sums), fp32
+    // this CTA's share of the flat output-row space (n, od, column block, oh)
+    const long long r_begin = total_rows * blockIdx.x / gridDim.x;
+    const long long r_end = total_rows * (blockIdx.x + 1) / gridDim.x;
+    struct Seg {
+        long long n;
+        int od, ow0, oh0, rows;
+    };
+    auto segment = [&](long long r) {
+        Seg g;
+        g.oh0 = (int)(r % Ho);
+        long long t = r / Ho;
+        g.ow0 = (int)(t % n_owb) * TOW;
+        t /= n_owb;
+        g.od = (int)(t % Do);
+        g.n = t / Do;
+        const long long left = r_end - r;
+        const int cap = TOH < Ho - g.oh0 ? TOH : Ho - g.oh0;
+        g.rows = left < cap ? (int)left : cap;
+        return g;
+    };
+    // input window of a segment into stage b: TMA box (thread 0), or element
+    // copies with zero fill (all threads)
+    auto stage = [&](const Seg &g, int b) {
+        float *dst = xs + b * stage_stride;
+        if (use_tma) {
+            if (tid == 0) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive_expect_tx(&bar[b], (uint32_t)stage_floats * 4u);
+                tma_load_4d(dst, &xmap, &bar[b], g.ow0, g.oh0, g.od, (int)(g.n * Cin));
+            }
+        } else {
+            for (int e = tid; e < stage_floats; e += THREADS) {
+                const int col = e % BW;
+                int t = e / BW;
+                const int r = t % XR;
+                t /= XR;
+                const int a = t & 1, ci = t >> 1;
+                const int ih = g.oh0 + r, iw = g.ow0 + col;
+                const bool in = ih < H && iw < W;
+                const float *src =
+                    in ? x + (((g.n * Cin + ci) * D + g.od + a) * (long long)H + ih) * W + iw : x;
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(
+                                 smem_u32(dst + e)),
+                             "l"(src), "r"(in ? 4 : 0)
+                             : "memory");
+            }
+            cp_async_commit();
+        }
+    };
+
+    if (tid == 0 && use_tma) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    Seg cur{};
+    if (r_begin < r_end) {
+        cur = segment(r_begin);
+        stage(cur, 0);
+    }
+
+    // ---- collapsed weights [ci][a*4+b*2+c][co] and folded bias, once per CTA
     const float wscale = scale1 * scale2 * 0.125f;
-    for (int i = tid; i < Cin * COUT * 8; i += THREADS) {
-        const int ci = i / (COUT * 8), co = (i / 8) % COUT, g = i % 8;
+    for (int i = tid; i < Cin * 8 * COUT; i += THREADS) {
+        const int co = i % COUT, g = (i / COUT) % 8, ci = i / (8 * COUT);
         const int a = g >> 2, b = (g >> 1) & 1, c = g & 1;
         const float *wp = w + (size_t)(ci * COUT + co) * 27;
         float acc = 0.f;
@@ -160,105 +156,97 @@ __global__ void __launch_bounds__(ct3::THREADS, 2)
         const float cb = conv_bias ? __ldg(conv_bias + tid) : 0.f;
         bsm[tid] = fmaf(cb, scale1, __ldg(bias + tid)) * scale2;
     }
+    __syncthreads();
 
-    // ---- this CTA's range of output rows
-    const long long r_begin = total_rows * blockIdx.x / gridDim.x;
-    const long long r_end = total_rows * (blockIdx.x + 1) / gridDim.x;
+    const long long plane = (long long)Ho * Wo;
+    const long long cstride = (long long)Do * plane;   // between output channels
+    for (long long r = r_begin, k = 0; r < r_end; ++k) {
+        const int b = (int)(k & 1);
+        // prefetch the next segment into the other stage (freed by the barrier
+        // that ended the previous iteration)
+        Seg nxt{};
+        const bool more = r + cur.rows < r_end;
+        if (more) {
+            nxt = segment(r + cur.rows);
+            stage(nxt, b ^ 1);
+        }
+        bool ok = true;
+        if (use_tma) {
+            ok = mbar_wait(&bar[b], (uint32_t)(k >> 1) & 1u);
+        } else {
+            if (more)
+                cp_async_wait<1>();
+            else
+                cp_async_wait<0>();
+        }
+        if (__syncthreads_or(!ok)) {
+            // a copy never landed: note it, let the prefetch (if any) finish or
+            // time out, and stop
+            if (tid == 0) {
+                record_error(status, APS_DEVERR_TIMEOUT);
+                if (use_tma && more) mbar_wait(&bar[b ^ 1], (uint32_t)((k + 1) >> 1) & 1u);
+            }
+            return;
+        }
 
-    // Stage segment (plane, oh0, rows) into dst: for each (ci, a) the input
-    // rows oh0 .. oh0+rows of plane od+a, which are contiguous in memory.
-    auto stage = [&](long long plane, int oh0, int rows, float *dst) {
-        const long long n = plane / Do;
-        const int od = (int)(plane - n * Do);
-        const int count = (rows + 1) * W;
-        for (int ci = 0; ci < Cin; ++ci)
-            for (int a = 0; a < 2; ++a) {
-                const float *src = x + ((((n * Cin + ci) * D + od + a) * H) + oh0) * (long long)W;
-                float *d = dst + (ci * 2 + a) * PT;
-                if (vec16) {
-                    for (int e = tid * 4; e < count; e += THREADS * 4) cp_async_16(d + e, src + e);
-                } else {
-                    for (int e = tid; e < count; e += THREADS) cp_async_4(d + e, src + e);
+        // ---- 4 rows x 16 channels per thread
+        float2 acc[COUT / 2][RPT];
+#pragma unroll
+        for (int c2 = 0; c2 < COUT / 2; ++c2) {
+            const float2 bv = make_float2(bsm[2 * c2], bsm[2 * c2 + 1]);
+#pragma unroll
+            for (int i = 0; i < RPT; ++i) acc[c2][i] = bv;
+        }
+        const float *xb = xs + b * stage_stride;
+#pragma unroll 1
+        for (int ci = 0; ci < Cin; ++ci) {
+            const float *xp = xb + (ci * 2 * XR + RPT * warp) * BW + lane;
+            float xv[2][RPT + 1][2];
+#pragma unroll
+            for (int a = 0; a < 2; ++a)
+#pragma unroll
+                for (int rr = 0; rr <= RPT; ++rr)
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) xv[a][rr][c] = xp[(a * XR + rr) * BW + c];
+            const float4 *wq = reinterpret_cast<const float4 *>(wsm + ci * 8 * COUT);
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+                const int a = g >> 2, bb = (g >> 1) & 1, c = g & 1;
+                const float4 w0 = wq[4 * g], w1 = wq[4 * g + 1], w2 = wq[4 * g + 2],
+                             w3 = wq[4 * g + 3];
+                const float2 wp[COUT / 2] = {make_float2(w0.x, w0.y), make_float2(w0.z, w0.w),
+                                             make_float2(w1.x, w1.y), make_float2(w1.z, w1.w),
+                                             make_float2(w2.x, w2.y), make_float2(w2.z, w2.w),
+                                             make_float2(w3.x, w3.y), make_float2(w3.z, w3.w)};
+#pragma unroll
+                for (int i = 0; i < RPT; ++i) {
+                    const float xg = xv[a][i + bb][c];
+#pragma unroll
+                    for (int c2 = 0; c2 < COUT / 2; ++c2)
+                        acc[c2][i] = __ffma2_rn(make_float2(xg, xg), wp[c2], acc[c2][i]);
                 }
             }
-    };
-    auto next_segment = [&](long long r, int &rows) {
-        const int oh0 = (int)(r % Ho);
-        const int cap = TH < Ho - oh0 ? TH : Ho - oh0;
-        rows = (long long)cap < r_end - r ? cap : (int)(r_end - r);
-    };
-
-    long long r = r_begin;
-    int rows = 0;
-    if (r < r_end) {
-        next_segment(r, rows);
-        stage(r / Ho, (int)(r % Ho), rows, xs0);
-    }
-    cp_async_commit();
-    int buf = 0;
-    const long long plane_out = (long long)Ho * Wo;
-    const long long cstride = (long long)Do * plane_out;
-    while (r < r_end) {
-        const long long rn = r + rows;
-        int rows_n = 0;
-        if (rn < r_end) {
-            next_segment(rn, rows_n);
-            stage(rn / Ho, (int)(rn % Ho), rows_n, buf ? xs0 : xs1);
         }
-        cp_async_commit();
-        cp_async_wait<1>();
-        __syncthreads();
 
-        // ---- compute segment (plane, oh0, rows) from buffer `buf`
-        const float *xt = buf ? xs1 : xs0;
-        const long long plane = r / Ho;
-        const int oh0 = (int)(r % Ho);
-        const int npts = rows * Wo;
-        const long long n = plane / Do;
-        const long long od = plane - n * Do;
-        float *yt = y + ((n * COUT) * Do + od) * plane_out + (long long)oh0 * Wo + tid;
-        // only as many point slots per thread as the segment needs (block-uniform)
-        switch ((npts + THREADS - 1) / THREADS) {
-            case 1: fused_segment<1, CIN_T, W_T>(xt, wsm, bsm, yt, cstride, npts, Cin, W, PT); break;
-            case 2: fused_segment<2, CIN_T, W_T>(xt, wsm, bsm, yt, cstride, npts, Cin, W, PT); break;
-            case 3: fused_segment<3, CIN_T, W_T>(xt, wsm, bsm, yt, cstride, npts, Cin, W, PT); break;
-            default: fused_segment<4, CIN_T, W_T>(xt, wsm, bsm, yt, cstride, npts, Cin, W, PT); break;
+        // ---- stores: per (channel, row) a warp writes up to 32 consecutive floats
+        const int ow = cur.ow0 + lane;
+        if (ow < Wo) {
+            float *yp = y + ((cur.n * COUT) * Do + cur.od) * plane + (long long)cur.oh0 * Wo + ow;
+#pragma unroll
+            for (int i = 0; i < RPT; ++i) {
+                const int row = RPT * warp + i;
+                if (row >= cur.rows) break;
+#pragma unroll
+                for (int c2 = 0; c2 < COUT / 2; ++c2) {
+                    yp[(2 * c2) * cstride + (long long)row * Wo] = acc[c2][i].x;
+                    yp[(2 * c2 + 1) * cstride + (long long)row * Wo] = acc[c2][i].y;
+                }
+            }
         }
-        __syncthreads();   // buffer `buf` is restaged two segments later
-        r = rn;
-        rows = rows_n;
-        buf ^= 1;
+        __syncthreads();   // stage b is restaged two segments later
+        r += cur.rows;
+        cur = nxt;
     }
-    cp_async_wait<0>();
-}
-
-template <int CIN_T, int W_T>
-static aps_status launch_fused_fast(const float *x, const int64_t in[5], const float *w,
-                                    const float *conv_bias, const float *bias, float scale1,
-                                    float scale2, float *y, const int64_t out[5], cudaStream_t st) {
-    using namespace ct3;
-    const int64_t N = in[0], Cin = in[1], D = in[2], H = in[3], W = in[4];
-    const int64_t Do = out[2], Ho = out[3], Wo = out[4];
-    int64_t TH = std::min<int64_t>(Ho, MAX_PTS / Wo);
-    TH = std::min<int64_t>(TH, XTILE_MAX / (Cin * 2 * W) - 1);
-    if (TH < 1) return APS_ERR_UNSUPPORTED;
-    // staged floats per (ci, input plane): fixed at compile time for a fixed W
-    const int64_t PT = W_T ? (MAX_PTS / (W_T - 1) + 1) * W_T : (TH + 1) * W;
-    if (Cin * 2 * PT > XTILE_MAX) return APS_ERR_UNSUPPORTED;
-    const int64_t tile_floats = Cin * 2 * PT;
-    const int smem = (int)((CIN_MAX * COUT * 8 + COUT + 2 * ((tile_floats + 3) & ~3)) * 4);
-    const auto kern = ct3d_pool2_fast_kernel<CIN_T, W_T>;
-    const int per_sm = resident_ctas((const void *)kern, THREADS, smem);
-    if (per_sm < 1) return APS_ERR_CUDA;
-    const long long total_rows = N * Do * Ho;
-    const long long pts = total_rows * Wo;
-    long long grid = std::min<long long>((long long)sm_count() * per_sm, ceil_div(pts, THREADS));
-    grid = std::max<long long>(grid, 1);
-    const int vec16 = (W % 4 == 0) && (reinterpret_cast<uintptr_t>(x) % 16 == 0);
-    kern<<<(unsigned)grid, THREADS, smem, st>>>(x, w, conv_bias, bias, scale1, scale2, y,
-                                                (int)Cin, (int)D, (int)H, (int)W, (int)TH,
-                                                (int)PT, total_rows, vec16);
-    return launch_status();
 }
 
 aps_status launch_ct3d_pool2_fast(const float *x, const int64_t in[5], const float *w,
@@ -266,14 +254,46 @@ aps_status launch_ct3d_pool2_fast(const float *x, const int64_t in[5], const flo
                                   float scale2, float *y, const int64_t out[5],
                                   cudaStream_t st) {
     using namespace ct3;
-    const int64_t Cin = in[1], D = in[2], H = in[3], W = in[4];
-    if (Cin < 1 || Cin > CIN_MAX || D < 2 || H < 2 || W < 2 || W > MAX_PTS) return APS_ERR_UNSUPPORTED;
-    // the pages' shapes (3 input channels, rows of 32 and 16) run fully specialised
-    if (Cin == 3 && W == 32)
-        return launch_fused_fast<3, 32>(x, in, w, conv_bias, bias, scale1, scale2, y, out, st);
-    if (Cin == 3 && W == 16)
-        return launch_fused_fast<3, 16>(x, in, w, conv_bias, bias, scale1, scale2, y, out, st);
-    return launch_fused_fast<0, 0>(x, in, w, conv_bias, bias, scale1, scale2, y, out, st);
+    const int64_t N = in[0], Cin = in[1], D = in[2], H = in[3], W = in[4];
+    if (Cin < 1 || Cin > CIN_MAX || D < 2 || H < 2 || W < 2 || D >= (1 << 30) ||
+        H >= (1 << 30) || W >= (1 << 30) || N * Cin >= (1ll << 31))
+        return APS_ERR_UNSUPPORTED;
+    const int64_t Do = out[2], Ho = out[3], Wo = out[4];
+    const int64_t n_owb = ceil_div(Wo, TOW);
+    const long long total_rows = N * Do * n_owb * Ho;
+    // staged columns: a block's 32 outputs need 33 inputs; a single block
+    // (W <= 32) needs only W
+    const int BW = W <= TOW ? (int)((W + 3) & ~3) : TOW + 4;
+    const int use_tma = (W % 4 == 0) && (reinterpret_cast<uintptr_t>(x) % 16 == 0);
+    CUtensorMap map;
+    if (use_tma) {
+        const cuuint64_t dims[4] = {(cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)D,
+                                    (cuuint64_t)(N * Cin)};
+        const cuuint64_t strides[3] = {(cuuint64_t)(W * 4), (cuuint64_t)(H * W * 4),
+                                       (cuuint64_t)(D * H * W * 4)};
+        const cuuint32_t box[4] = {(cuuint32_t)BW, (cuuint32_t)XR, 2, (cuuint32_t)Cin};
+        const cuuint32_t estr[4] = {1, 1, 1, 1};
+        if (!encode_tiled(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(x), dims,
+                          strides, box, estr))
+            return APS_ERR_UNSUPPORTED;
+    } else {
+        std::memset(&map, 0, sizeof(map));
+    }
+    const int64_t stage_stride = (Cin * 2 * XR * BW + SLACK + 31) & ~31;
+    const size_t smem = (size_t)(2 * stage_stride + CIN_MAX * 8 * COUT + COUT) * 4 + 16;
+    const auto kern = BW == 32 ? ct3d_pool2_fast_kernel<32>
+                    : BW == 36 ? ct3d_pool2_fast_kernel<36>
+                    : BW == 16 ? ct3d_pool2_fast_kernel<16>
+                               : ct3d_pool2_fast_kernel<0>;
+    const int per_sm = resident_ctas((const void *)kern, THREADS, (int)smem);
+    if (per_sm < 1) return APS_ERR_CUDA;
+    // persistent: one CTA per resident slot, each with at least a few rows
+    const long long grid = std::max<long long>(
+        1, std::min<long long>((long long)per_sm * sm_count(), ceil_div(total_rows, RPT)));
+    kern<<<(unsigned)grid, THREADS, smem, st>>>(map, use_tma, x, w, conv_bias, bias, scale1,
+                                                 scale2, y, (int)Cin, (int)D, (int)H, (int)W,
+                                                 BW, (int)n_owb, total_rows, status_word());
+    return launch_status();
 }
 
 // ------------------------------------------------------------ direct kernel
