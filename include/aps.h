@@ -145,8 +145,14 @@ aps_status aps_ct3d_scale_pool_bias(const float *x, const int64_t in_ncdhw[5],
  * x: [N, C_in, L]; w: [C_in, C_out, K]; bias: [C_out] or NULL (no bias);
  * y: [N, C_out, L_out] (shape from aps_convtranspose1d_out_shape).  Requires
  * K, s, d >= 1, p >= 0, 0 <= out_pad < max(s, d).  precision: APS_PREC_FP32 or
- * APS_PREC_TF32 (tolerances above); APS_PREC_TF32 needs C_in % 8 == 0,
- * C_out % 16 == 0 and C_out <= 256, otherwise APS_ERR_UNSUPPORTED.
+ * APS_PREC_TF32 (tolerances above).  APS_PREC_TF32 returns APS_ERR_UNSUPPORTED
+ * (nothing launched) unless: C_in % 8 == 0 and, above 32, C_in % 32 == 0;
+ * C_out % 32 == 0 and (number of output residues mod s that some tap reaches)
+ * x C_out <= 256; L % 4 == 0 and x 16-byte aligned; s <= 8, at most 4
+ * reached residues with at most 8 taps each; the tap span d*(K-1)/s <= 124;
+ * K * C_in <= 2048 (the per-tile MMA descriptor table);
+ * and the weights (K*C_in*C_out*4 bytes) plus the staging buffers fit in one
+ * CTA's 227 KB of shared memory.  APS_PREC_FP32 accepts every valid shape.
  */
 aps_status aps_convtranspose1d_out_shape(const int64_t in_ncl[3], int64_t c_out, int k,
                                          int stride, int pad, int dil, int out_pad,
