@@ -46,6 +46,10 @@ FP32_LANES_PER_SM = 128
 
 
 def parse_args():
+    return parse_args_from(sys.argv[1:])
+
+
+def parse_args_from(argv):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
@@ -63,7 +67,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle sample")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 # ----------------------------------------------------------------- helpers
@@ -372,6 +376,23 @@ def oracle_sample(cfg, seconds, xhost=None):
 
 
 # ------------------------------------------------------------------- legs
+def max_over_ranks(dist, value, device):
+    """The largest `value` over all ranks (the job's time), or `value` itself
+    when the run is not distributed."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world_size, units_per_rank_step, steps, t_max):
+    """Units all ranks processed per second: every rank runs the same full
+    workload (weak scaling) and the job takes as long as its slowest rank."""
+    return world_size * units_per_rank_step * steps / t_max
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -456,13 +477,9 @@ def run_native(args):
     t_wall1 = time.time()
     sampler.stop()
     t_dev = e0.elapsed_time(e1) / 1e3
-    t_max = t_dev
-    if dist:
-        tt = torch.tensor([t_dev], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_max = float(tt.item())
+    t_max = max_over_ranks(dist, t_dev, "cuda")
     per_launch = t_dev / args.steps
-    value = ws * case.outputs * args.steps / t_max
+    value = whole_job_rate(ws, case.outputs, args.steps, t_max)
 
     # ---- e2e through the ABI with host buffers
     e2e = None
@@ -477,12 +494,8 @@ def run_native(args):
             case.e2e_step()
         f1.record(st)
         barrier()
-        t_e2e = f0.elapsed_time(f1) / 1e3
-        if dist:
-            tt = torch.tensor([t_e2e], device="cuda")
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            t_e2e = float(tt.item())
-        e2e = {"value": ws * case.outputs * e2e_steps / t_e2e, "unit": "outputs/s",
+        t_e2e = max_over_ranks(dist, f0.elapsed_time(f1) / 1e3, "cuda")
+        e2e = {"value": whole_job_rate(ws, case.outputs, e2e_steps, t_e2e), "unit": "outputs/s",
                "h2d_bytes_per_step": 4 * numel(case.host["x"].shape),
                "d2h_bytes_per_step": 4 * case.outputs, "steps": e2e_steps,
                "ms_per_step": 1e3 * t_e2e / e2e_steps}
