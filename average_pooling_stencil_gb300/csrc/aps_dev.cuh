@@ -129,6 +129,15 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void 
         "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
+// Untiled bulk copy of `bytes` from shared to global memory (bulk-group
+// completion).  Both addresses 16-byte aligned, bytes a multiple of 16; the
+// source must have been made visible to the async proxy first.
+__device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                     reinterpret_cast<uint64_t>(gdst)),
+                 "r"(smem_u32(ssrc)), "r"(bytes)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

@@ -46,60 +46,70 @@ namespace aps {
 namespace ct3 {
 constexpr int COUT = 16;
 constexpr int CIN_MAX = 8;
-constexpr int WARPS = 4;
+constexpr int WARPS = 8;
 constexpr int THREADS = 32 * WARPS;
 constexpr int RPT = 4;                 // output rows per thread
-constexpr int TOH = WARPS * RPT;       // output rows per unit
+constexpr int TOH = WARPS * RPT;       // output rows per unit (at most)
 constexpr int TOW = 32;                // output columns per unit (one per lane)
-constexpr int XR = TOH + 1;            // input rows per staged plane
-constexpr int SLACK = 64;              // floats after the stage: idle lanes may read past a row
+constexpr int SLACK = 64;              // floats after a stage: lanes past the last column read on
+// Floats one stage occupies: the staged window plus the rows a warp whose
+// rows end inside the unit may still read (up to row 4*WARPS), plus slack.
+__host__ __device__ inline int stage_stride_of(int Cin, int XR, int BW) {
+    return (Cin * 2 * XR * BW + (TOH + 1 - XR) * BW + SLACK + 31) & ~31;
+}
+// Floats of one channel's output staging: a unit's RB x WB outputs, 16-byte
+// aligned, plus 3 for the shift that gives the run the alignment of its
+// destination.
+__host__ __device__ inline int chan_stride_of(int RB, int WB) {
+    return ((RB * WB + 3) & ~3) + 4;
+}
 }  // namespace ct3
 
 // BW_T: staged row length (columns) fixed at compile time (0: run time), so
 // that every window offset folds into an immediate.
 template <int BW_T>
-__global__ void __launch_bounds__(ct3::THREADS, BW_T ? 4 : 3)
+__global__ void __launch_bounds__(ct3::THREADS, BW_T ? 2 : 1)
     ct3d_pool2_fast_kernel(const __grid_constant__ CUtensorMap xmap, int use_tma,
                            const float *__restrict__ x, const float *__restrict__ w,
                            const float *__restrict__ conv_bias, const float *__restrict__ bias,
                            float scale1, float scale2, float *__restrict__ y, int Cin, int D,
-                           int H, int W, int BW_rt, int n_owb, long long total_rows,
-                           unsigned int *status) {
+                           int H, int W, int BW_rt, int XR, int RB, int WB, int n_ohb,
+                           int n_owb, long long n_units, unsigned int *status) {
     using namespace ct3;
     const int BW = BW_T ? BW_T : BW_rt;
     const int Do = D - 1, Ho = H - 1, Wo = W - 1;
     extern __shared__ __align__(128) float sm[];
     const int stage_floats = Cin * 2 * XR * BW;
-    const int stage_stride = (stage_floats + SLACK + 31) & ~31;   // 128-byte aligned stages
+    const int stage_stride = stage_stride_of(Cin, XR, BW);   // 128-byte aligned stages
     float *xs = sm;                                  // [2][Cin][2][XR][BW]
-    float *wsm = xs + 2 * stage_stride;              // [Cin][8][16]
-    float *bsm = wsm + CIN_MAX * 8 * COUT;           // [16]
-    uint64_t *bar = reinterpret_cast<uint64_t *>(bsm + COUT);   // [2]
+    const int CH = chan_stride_of(RB, WB);
+    float *ost = xs + 2 * stage_stride;              // [16][CH] output staging
+    float *wsm = ost + ((COUT * CH + 31) & ~31);     // [Cin][8][16]
+    float *bsm = wsm + Cin * 8 * COUT;               // [16]
+    uint64_t *bar = reinterpret_cast<uint64_t *>(bsm + COUT);   // [2], 8-byte aligned
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-    // this CTA's share of the flat output-row space (n, od, column block, oh)
-    const long long r_begin = total_rows * blockIdx.x / gridDim.x;
-    const long long r_end = total_rows * (blockIdx.x + 1) / gridDim.x;
-    struct Seg {
+    struct Unit {
         long long n;
-        int od, ow0, oh0, rows;
+        int od, oh0, ow0, rows, cols;
     };
-    auto segment = [&](long long r) {
-        Seg g;
-        g.oh0 = (int)(r % Ho);
-        long long t = r / Ho;
-        g.ow0 = (int)(t % n_owb) * TOW;
-        t /= n_owb;
+    auto unit = [&](long long u) {
+        Unit g;
+        const int owb = (int)(u % n_owb);
+        long long t = u / n_owb;
+        const int ohb = (int)(t % n_ohb);
+        t /= n_ohb;
         g.od = (int)(t % Do);
         g.n = t / Do;
-        const long long left = r_end - r;
-        const int cap = TOH < Ho - g.oh0 ? TOH : Ho - g.oh0;
-        g.rows = left < cap ? (int)left : cap;
+        g.oh0 = ohb * RB;
+        g.ow0 = owb * WB;
+        g.rows = Ho - g.oh0 < RB ? Ho - g.oh0 : RB;
+        g.cols = Wo - g.ow0 < WB ? Wo - g.ow0 : WB;
         return g;
     };
-    // input window of a segment into stage b: TMA box (thread 0), or element
+    // input window of a unit into stage b: TMA box (thread 0), or element
     // copies with zero fill (all threads)
-    auto stage = [&](const Seg &g, int b) {
+    auto stage = [&](const Unit &g, int b) {
         float *dst = xs + b * stage_stride;
         if (use_tma) {
             if (tid == 0) {
@@ -133,9 +143,9 @@ __global__ void __launch_bounds__(ct3::THREADS, BW_T ? 4 : 3)
         mbar_fence_init();
     }
     __syncthreads();
-    Seg cur{};
-    if (r_begin < r_end) {
-        cur = segment(r_begin);
+    Unit cur{};
+    if ((long long)blockIdx.x < n_units) {
+        cur = unit(blockIdx.x);
         stage(cur, 0);
     }
 
@@ -160,16 +170,15 @@ __global__ void __launch_bounds__(ct3::THREADS, BW_T ? 4 : 3)
 
     const long long plane = (long long)Ho * Wo;
     const long long cstride = (long long)Do * plane;   // between output channels
-    for (long long r = r_begin, k = 0; r < r_end; ++k) {
+    long long k = 0;
+    // units are dealt round-robin, so at any time the grid works on a narrow,
+    // contiguous window of the output
+    for (long long u = blockIdx.x; u < n_units; u += gridDim.x, ++k) {
         const int b = (int)(k & 1);
-        // prefetch the next segment into the other stage (freed by the barrier
+        // prefetch the next unit into the other stage (freed by the barrier
         // that ended the previous iteration)
-        Seg nxt{};
-        const bool more = r + cur.rows < r_end;
-        if (more) {
-            nxt = segment(r + cur.rows);
-            stage(nxt, b ^ 1);
-        }
+        const bool more = u + gridDim.x < n_units;
+        if (more) stage(unit(u + gridDim.x), b ^ 1);
         bool ok = true;
         if (use_tma) {
             ok = mbar_wait(&bar[b], (uint32_t)(k >> 1) & 1u);
@@ -180,11 +189,12 @@ __global__ void __launch_bounds__(ct3::THREADS, BW_T ? 4 : 3)
                 cp_async_wait<0>();
         }
         if (__syncthreads_or(!ok)) {
-            // a copy never landed: note it, let the prefetch (if any) finish or
-            // time out, and stop
+            // a copy never landed: note it, let the prefetch (if any) and the
+            // output copies finish or time out, and stop
             if (tid == 0) {
                 record_error(status, APS_DEVERR_TIMEOUT);
                 if (use_tma && more) mbar_wait(&bar[b ^ 1], (uint32_t)((k + 1) >> 1) & 1u);
+                bulk_wait<0>();
             }
             return;
         }
@@ -198,8 +208,9 @@ __global__ void __launch_bounds__(ct3::THREADS, BW_T ? 4 : 3)
             for (int i = 0; i < RPT; ++i) acc[c2][i] = bv;
         }
         const float *xb = xs + b * stage_stride;
+        const int nci = RPT * warp < cur.rows ? Cin : 0;   // warps past the unit's rows idle
 #pragma unroll 1
-        for (int ci = 0; ci < Cin; ++ci) {
+        for (int ci = 0; ci < nci; ++ci) {
             const float *xp = xb + (ci * 2 * XR + RPT * warp) * BW + lane;
             float xv[2][RPT + 1][2];
 #pragma unroll
@@ -228,25 +239,69 @@ __global__ void __launch_bounds__(ct3::THREADS, BW_T ? 4 : 3)
             }
         }
 
-        // ---- stores: per (channel, row) a warp writes up to 32 consecutive floats
-        const int ow = cur.ow0 + lane;
-        if (ow < Wo) {
-            float *yp = y + ((cur.n * COUT) * Do + cur.od) * plane + (long long)cur.oh0 * Wo + ow;
+        // ---- outputs.  With whole output rows in the unit (WB == Wo) the unit's
+        // outputs of channel co are one run, contiguous in y; it is staged at
+        // ost + co*CH + off (off = its destination's float offset mod 4, so
+        // both sides share 16-byte alignment), its aligned middle leaves by one
+        // bulk copy and the at most 3 + 3 head and tail floats by plain stores.
+        // Otherwise the staging rows are WB long and rows leave by plain stores.
+        const bool runs = WB == Wo;
+        const float *y_unit = y + ((cur.n * COUT) * Do + cur.od) * plane + (long long)cur.oh0 * Wo;
+        const uint32_t a0 = runs ? (uint32_t)(reinterpret_cast<uintptr_t>(y_unit) >> 2) & 3u : 0u;
+        const uint32_t ac = runs ? (uint32_t)cstride & 3u : 0u;
+        // the bulk copies of the previous unit have read the staging block
+        if (tid == 0) bulk_wait_read<0>();
+        __syncthreads();
+        if (lane < cur.cols) {
 #pragma unroll
             for (int i = 0; i < RPT; ++i) {
                 const int row = RPT * warp + i;
                 if (row >= cur.rows) break;
 #pragma unroll
                 for (int c2 = 0; c2 < COUT / 2; ++c2) {
-                    yp[(2 * c2) * cstride + (long long)row * Wo] = acc[c2][i].x;
-                    yp[(2 * c2 + 1) * cstride + (long long)row * Wo] = acc[c2][i].y;
+                    const int c0 = 2 * c2, c1 = 2 * c2 + 1;
+                    ost[c0 * CH + ((a0 + c0 * ac) & 3u) + row * WB + lane] = acc[c2][i].x;
+                    ost[c1 * CH + ((a0 + c1 * ac) & 3u) + row * WB + lane] = acc[c2][i].y;
                 }
             }
         }
-        __syncthreads();   // stage b is restaged two segments later
-        r += cur.rows;
-        cur = nxt;
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncthreads();
+        if (runs) {
+            const int run = cur.rows * Wo;
+            if (tid == 0) {
+                for (int co = 0; co < COUT; ++co) {
+                    const uint32_t off = (a0 + co * ac) & 3u, h = (4u - off) & 3u;
+                    const int mid = run > (int)h ? (run - (int)h) & ~3 : 0;
+                    if (mid > 0)
+                        bulk_store(const_cast<float *>(y_unit) + co * cstride + h,
+                                   ost + co * CH + off + h, (uint32_t)mid * 4u);
+                }
+                bulk_commit();
+            }
+            for (int co = warp; co < COUT; co += WARPS) {
+                const uint32_t off = (a0 + co * ac) & 3u, h = (4u - off) & 3u;
+                const int head = run < (int)h ? run : (int)h;
+                const int mid = run > (int)h ? (run - (int)h) & ~3 : 0;
+                const int tail0 = head + mid;
+                float *yc = const_cast<float *>(y_unit) + co * cstride;
+                const float *sc = ost + co * CH + off;
+                if (lane < head) yc[lane] = sc[lane];
+                if (tail0 + lane < run) yc[tail0 + lane] = sc[tail0 + lane];
+            }
+        } else {
+            for (int co = warp; co < COUT; co += WARPS) {
+                float *yc = const_cast<float *>(y_unit) + co * cstride;
+                const float *sc = ost + co * CH;
+                if (lane < cur.cols)
+                    for (int r = 0; r < cur.rows; ++r)
+                        yc[(long long)r * Wo + cur.ow0 + lane] = sc[r * WB + lane];
+            }
+        }
+        if (more) cur = unit(u + gridDim.x);
     }
+    // the output copies are complete before the CTA exits
+    if (tid == 0) bulk_wait<0>();
 }
 
 aps_status launch_ct3d_pool2_fast(const float *x, const int64_t in[5], const float *w,
@@ -259,11 +314,13 @@ aps_status launch_ct3d_pool2_fast(const float *x, const int64_t in[5], const flo
         H >= (1 << 30) || W >= (1 << 30) || N * Cin >= (1ll << 31))
         return APS_ERR_UNSUPPORTED;
     const int64_t Do = out[2], Ho = out[3], Wo = out[4];
-    const int64_t n_owb = ceil_div(Wo, TOW);
-    const long long total_rows = N * Do * n_owb * Ho;
-    // staged columns: a block's 32 outputs need 33 inputs; a single block
-    // (W <= 32) needs only W
-    const int BW = W <= TOW ? (int)((W + 3) & ~3) : TOW + 4;
+    // a unit: up to 32 output rows x 32 output columns of one (n, od) plane
+    const int RB = (int)std::min<int64_t>(Ho, TOH), WB = (int)std::min<int64_t>(Wo, TOW);
+    const int64_t n_ohb = ceil_div(Ho, RB), n_owb = ceil_div(Wo, WB);
+    const long long n_units = N * Do * n_ohb * n_owb;
+    // staged input: rows RB+1, columns WB+1 rounded up to a multiple of 4
+    const int XR = RB + 1;
+    const int BW = (WB + 1 + 3) & ~3;
     const int use_tma = (W % 4 == 0) && (reinterpret_cast<uintptr_t>(x) % 16 == 0);
     CUtensorMap map;
     if (use_tma) {
@@ -279,20 +336,21 @@ aps_status launch_ct3d_pool2_fast(const float *x, const int64_t in[5], const flo
     } else {
         std::memset(&map, 0, sizeof(map));
     }
-    const int64_t stage_stride = (Cin * 2 * XR * BW + SLACK + 31) & ~31;
-    const size_t smem = (size_t)(2 * stage_stride + CIN_MAX * 8 * COUT + COUT) * 4 + 16;
+    const int64_t stage_stride = stage_stride_of((int)Cin, XR, BW);
+    const int64_t ost_floats = (COUT * chan_stride_of(RB, WB) + 31) & ~31;
+    const size_t smem =
+        (size_t)(2 * stage_stride + ost_floats + Cin * 8 * COUT + COUT) * 4 + 16;
     const auto kern = BW == 32 ? ct3d_pool2_fast_kernel<32>
                     : BW == 36 ? ct3d_pool2_fast_kernel<36>
                     : BW == 16 ? ct3d_pool2_fast_kernel<16>
                                : ct3d_pool2_fast_kernel<0>;
     const int per_sm = resident_ctas((const void *)kern, THREADS, (int)smem);
-    if (per_sm < 1) return APS_ERR_CUDA;
-    // persistent: one CTA per resident slot, each with at least a few rows
-    const long long grid = std::max<long long>(
-        1, std::min<long long>((long long)per_sm * sm_count(), ceil_div(total_rows, RPT)));
+    if (per_sm < 1) return APS_ERR_UNSUPPORTED;
+    const long long grid = std::min<long long>((long long)per_sm * sm_count(), n_units);
     kern<<<(unsigned)grid, THREADS, smem, st>>>(map, use_tma, x, w, conv_bias, bias, scale1,
-                                                 scale2, y, (int)Cin, (int)D, (int)H, (int)W,
-                                                 BW, (int)n_owb, total_rows, status_word());
+                                                 scale2, y, (int)Cin, (int)D, (int)H, (int)W, BW,
+                                                 XR, RB, WB, (int)n_ohb, (int)n_owb, n_units,
+                                                 status_word());
     return launch_status();
 }
 
