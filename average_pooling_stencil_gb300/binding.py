@@ -36,6 +36,7 @@ APS_PREC_TF32 = 1
 EXPORTS = [
     "aps_abi_version", "aps_status_string", "aps_avgpool3d_out_shape", "aps_avgpool3d",
     "aps_ct3d_scale_pool_bias_out_shape", "aps_ct3d_scale_pool_bias",
+    "aps_convtranspose3d_out_shape", "aps_convtranspose3d",
     "aps_convtranspose1d_out_shape", "aps_convtranspose1d", "aps_device_status",
 ]
 
@@ -71,6 +72,10 @@ def lib():
         L.aps_ct3d_scale_pool_bias.argtypes = [_VP, _VP, _VP, _VP, _VP, ctypes.c_int64, _VP, _VP,
                                                _VP, _VP, _VP, ctypes.c_int, ctypes.c_float,
                                                ctypes.c_float, _VP, _VP]
+        L.aps_convtranspose3d_out_shape.argtypes = [_VP, ctypes.c_int64, _VP, _VP, _VP, _VP, _VP,
+                                                    _VP]
+        L.aps_convtranspose3d.argtypes = [_VP, _VP, _VP, _VP, ctypes.c_int64, _VP, _VP, _VP, _VP,
+                                          _VP, _VP, _VP]
         L.aps_convtranspose1d_out_shape.argtypes = [_VP, ctypes.c_int64] + [ctypes.c_int] * 5 + [_VP]
         L.aps_convtranspose1d.argtypes = [_VP, _VP, _VP, _VP, ctypes.c_int64] + \
             [ctypes.c_int] * 6 + [_VP, _VP]
@@ -128,6 +133,20 @@ def aps_ct3d_scale_pool_bias(x_ptr, in_ncdhw, w_ptr, conv_bias_ptr, bias_ptr, c_
         _VP(x_ptr), _I64_5(*in_ncdhw), _VP(w_ptr), _VP(conv_bias_ptr), _VP(bias_ptr),
         int(c_out), _i3(k), _i3(stride), _i3(pad), _i3(out_pad), _i3(dil), int(pool_k),
         float(scale1), float(scale2), _VP(y_ptr), _VP(stream))
+
+
+def aps_convtranspose3d_out_shape(in_ncdhw, c_out, k, stride, pad, dil, out_pad):
+    out = _I64_5()
+    st = lib().aps_convtranspose3d_out_shape(_I64_5(*in_ncdhw), int(c_out), _i3(k), _i3(stride),
+                                             _i3(pad), _i3(dil), _i3(out_pad), out)
+    return st, tuple(out)
+
+
+def aps_convtranspose3d(x_ptr, in_ncdhw, w_ptr, bias_ptr, c_out, k, stride, pad, dil, out_pad,
+                        y_ptr, stream=0) -> int:
+    return lib().aps_convtranspose3d(_VP(x_ptr), _I64_5(*in_ncdhw), _VP(w_ptr), _VP(bias_ptr),
+                                     int(c_out), _i3(k), _i3(stride), _i3(pad), _i3(dil),
+                                     _i3(out_pad), _VP(y_ptr), _VP(stream))
 
 
 def aps_convtranspose1d_out_shape(in_ncl, c_out, k, stride, pad, dil, out_pad):
@@ -217,6 +236,37 @@ def ct3d_scale_pool_bias(x, weight, conv_bias, bias, stride=2, padding=1, output
                                   dilation, pool_k, scale1, scale2, y.data_ptr(), _stream(stream))
     if st != APS_OK:
         raise ApsError(st, "aps_ct3d_scale_pool_bias")
+    return y
+
+
+def convtranspose3d(x, weight, bias=None, stride=2, padding=1, dilation=1, output_padding=0,
+                    out=None, stream=None):
+    """ConvTranspose3d on device tensors through the C ABI; returns (or fills)
+    y [N, C_out, Do, Ho, Wo]."""
+    import torch
+    _check_tensor(x, "x")
+    _check_tensor(weight, "weight")
+    if bias is not None:
+        _check_tensor(bias, "bias")
+    if x.dim() != 5 or weight.dim() != 5:
+        raise ValueError("x and weight must be 5-D")
+    c_out = weight.shape[1]
+    k = tuple(weight.shape[2:])
+    st, oshape = aps_convtranspose3d_out_shape(x.shape, c_out, k, stride, padding, dilation,
+                                               output_padding)
+    if st != APS_OK:
+        raise ApsError(st, "aps_convtranspose3d_out_shape")
+    if weight.shape[0] != x.shape[1] or (bias is not None and bias.numel() != c_out):
+        raise ValueError("weight / bias shapes do not match x and C_out")
+    y = out if out is not None else torch.empty(oshape, device=x.device, dtype=torch.float32)
+    _check_tensor(y, "out")
+    if tuple(y.shape) != oshape:
+        raise ValueError(f"out has shape {tuple(y.shape)}, expected {oshape}")
+    st = aps_convtranspose3d(x.data_ptr(), x.shape, weight.data_ptr(), _ptr(bias), c_out, k,
+                             stride, padding, dilation, output_padding, y.data_ptr(),
+                             _stream(stream))
+    if st != APS_OK:
+        raise ApsError(st, "aps_convtranspose3d")
     return y
 
 

@@ -287,6 +287,47 @@ aps_status aps_ct3d_scale_pool_bias(const float *x, const int64_t in[5], const f
                                    scale1, scale2, y, out, cs);
 }
 
+// -------------------------------------------------------- convtranspose3d
+aps_status aps_convtranspose3d_out_shape(const int64_t in[5], int64_t c_out, const int k[3],
+                                         const int s[3], const int p[3], const int d[3],
+                                         const int op[3], int64_t out[5]) {
+    if (!in || !k || !s || !p || !d || !op || !out) return APS_ERR_NULL;
+    if (!dims_ok(in, 5) || c_out < 1 || c_out > kMaxElems) return APS_ERR_SHAPE;
+    aps_status st = conv_params_ok(k, s, p, op, d, 3);
+    if (st != APS_OK) return st;
+    int64_t o[5] = {in[0], c_out, 0, 0, 0};
+    for (int i = 0; i < 3; ++i) {
+        if (in[2 + i] < 1) return APS_ERR_SHAPE;
+        o[2 + i] = convt_len(in[2 + i], k[i], s[i], p[i], d[i], op[i]);
+        if (o[2 + i] <= 0) return APS_ERR_SHAPE;
+    }
+    if (!dims_ok(o, 5)) return APS_ERR_SHAPE;
+    for (int i = 0; i < 5; ++i) out[i] = o[i];
+    return APS_OK;
+}
+
+aps_status aps_convtranspose3d(const float *x, const int64_t in[5], const float *w,
+                               const float *bias, int64_t c_out, const int k[3],
+                               const int s[3], const int p[3], const int d[3], const int op[3],
+                               float *y, aps_stream_t stream) {
+    if (!x || !w || !y) return APS_ERR_NULL;
+    int64_t out[5];
+    aps_status st = aps_convtranspose3d_out_shape(in, c_out, k, s, p, d, op, out);
+    if (st != APS_OK) return st;
+    if (!aligned(x, 4) || !aligned(w, 4) || !aligned(y, 4) || (bias && !aligned(bias, 4)))
+        return APS_ERR_ALIGN;
+    if (numel(out, 5) == 0) return APS_OK;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    bool fast = c_out == 16 && in[1] >= 1 && in[1] <= 8;
+    for (int i = 0; i < 3; ++i)
+        fast = fast && k[i] == 3 && s[i] == 2 && p[i] == 1 && d[i] == 1 && op[i] <= 1;
+    if (fast) {
+        st = launch_convt3d_k3s2p1(x, in, w, bias, y, out, cs);
+        if (st != APS_ERR_UNSUPPORTED) return st;
+    }
+    return launch_convt3d_direct(x, in, w, bias, c_out, k, s, p, d, y, out, cs);
+}
+
 // -------------------------------------------------------- convtranspose1d
 aps_status aps_convtranspose1d_out_shape(const int64_t in[3], int64_t c_out, int k, int s,
                                          int p, int d, int op, int64_t out[3]) {

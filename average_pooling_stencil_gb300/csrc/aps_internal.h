@@ -61,6 +61,16 @@ aps_status launch_ct3d_pool_direct(const float *x, const int64_t in[5], const fl
                                    const int d[3], int pool_k, float scale1, float scale2,
                                    float *y, const int64_t out[5], cudaStream_t st);
 
+// ConvTranspose3d, fp32: the k3 s2 p1 d1 kernel (C_out 16, C_in <= 8, TMA
+// staging) and the direct per-output kernel for any geometry.
+aps_status launch_convt3d_k3s2p1(const float *x, const int64_t in[5], const float *w,
+                                 const float *bias, float *y, const int64_t out[5],
+                                 cudaStream_t st);
+aps_status launch_convt3d_direct(const float *x, const int64_t in[5], const float *w,
+                                 const float *bias, int64_t c_out, const int k[3],
+                                 const int s[3], const int p[3], const int d[3], float *y,
+                                 const int64_t out[5], cudaStream_t st);
+
 // ConvTranspose1d, fp32.  The tiled kernel covers the (stride, taps,
 // dilation, padding mod stride) combinations compiled in and C_out % 8 == 0;
 // it returns APS_ERR_UNSUPPORTED otherwise.

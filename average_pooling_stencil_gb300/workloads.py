@@ -11,6 +11,9 @@ Each workload mirrors one task traced on the Kimi-K2.6 pages:
     s1, p0, d3), no bias, on [32,32,131072].
   * ``convt1d_strided``         -- the strided variant (64->64, K4, s2, p1, op1, d2,
     with bias) that exercises per-parity tap selection.
+  * ``convt3d``                 -- the first stage of l2_p50's unfused chain: its
+    ConvTranspose3d(3->16, k3, s2, p1) with conv bias alone, on the fused
+    workload's input, emitting the full [128,16,31,63,63] tensor.
 Initialiser bounds are the usual 1/sqrt(fan) uniform ones: fan = C_out*prod(k)
 for the transposed-conv weights (432 = 16*27, 320 = 64*5, 256 = 64*4).
 """
@@ -28,6 +31,7 @@ STREAM_X, STREAM_W, STREAM_CONV_BIAS, STREAM_BIAS = 0, 1, 2, 3
 class Workload:
     name: str
     op: str                      # "ct3d_scale_pool_bias" | "avgpool3d" | "convtranspose1d"
+                                 # | "convtranspose3d"
     seed: int
     tensors: dict                # name -> (shape, dist, stream)
     params: dict = field(default_factory=dict)
@@ -95,6 +99,16 @@ WORKLOADS = {
             "bias": ((64,), _u(1.0 / 16.0), STREAM_BIAS),
         },
         dict(c_out=64, k=4, stride=2, pad=1, dil=2, out_pad=1, has_bias=True),
+    ),
+    5: Workload(
+        "convt3d", "convtranspose3d", 5,
+        {
+            "x": ((128, 3, 16, 32, 32), ("uniform", -1.0, 1.0), STREAM_X),
+            "w": ((3, 16, 3, 3, 3), _u(1.0 / math.sqrt(432.0)), STREAM_W),
+            "bias": ((16,), _u(1.0 / math.sqrt(432.0)), STREAM_CONV_BIAS),
+        },
+        dict(c_out=16, k=(3, 3, 3), stride=(2, 2, 2), pad=(1, 1, 1), out_pad=(0, 0, 0),
+             dil=(1, 1, 1), has_bias=True),
     ),
 }
 

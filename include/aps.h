@@ -137,6 +137,32 @@ aps_status aps_ct3d_scale_pool_bias(const float *x, const int64_t in_ncdhw[5],
                                     float scale1, float scale2, float *y,
                                     aps_stream_t stream);
 
+/* -------------------------------------------------------- convtranspose3d
+ * The transposed convolution alone, emitting the full-resolution tensor (the
+ * first stage of Kimi-K2.6__l2_p50's unfused chain, "approach 1" there):
+ *   y[n,co,o] = bias[co] + sum_ci sum_k w[ci,co,k] * x[n,ci,(o + p - d*k)/s],
+ * per spatial dim a term existing only where o + p - d*k is a non-negative
+ * multiple of s whose quotient is inside the input; weights are not flipped.
+ *
+ * x: [N, C_in, D, H, W]; w: [C_in, C_out, kD, kH, kW]; bias: [C_out] or NULL
+ * (no bias); y: [N, C_out, Do, Ho, Wo] with O = (I-1)*s - 2p + d*(k-1) + op + 1
+ * (shape from aps_convtranspose3d_out_shape).  Requires k, s, d >= 1,
+ * p >= 0, 0 <= out_pad < max(s, d).
+ * Fast path: k = 3, s = 2, p = 1, d = 1 in all dims (out_pad 0 or 1),
+ * C_out = 16, 1 <= C_in <= 8, W % 4 == 0 and x 16-byte aligned (per-parity
+ * tap sets, TMA-staged input, bulk-copied output runs); every other valid
+ * request runs a direct per-output kernel.
+ */
+aps_status aps_convtranspose3d_out_shape(const int64_t in_ncdhw[5], int64_t c_out,
+                                         const int k[3], const int stride[3],
+                                         const int pad[3], const int dil[3],
+                                         const int out_pad[3], int64_t out_ncdhw[5]);
+
+aps_status aps_convtranspose3d(const float *x, const int64_t in_ncdhw[5], const float *w,
+                               const float *bias, int64_t c_out, const int k[3],
+                               const int stride[3], const int pad[3], const int dil[3],
+                               const int out_pad[3], float *y, aps_stream_t stream);
+
 /* -------------------------------------------------------- convtranspose1d
  * y[n,co,o] = bias[co] + sum_ci sum_k w[ci,co,k] * x[n,ci,(o + p - d*k)/s], each
  * term taken only when o + p - d*k is a multiple of s and the quotient lies in

@@ -59,10 +59,11 @@ def test_printed_sizes_through_shape_queries():
 
 
 def test_workload_output_shapes():
-    """Output shapes of the five workloads (cfg 4 has 131076 outputs: the
-    closed form (65536-1)*2 - 2 + 2*3 + 1 + 1)."""
+    """Output shapes of the six workloads (cfg 4 has 131076 outputs: the
+    closed form (65536-1)*2 - 2 + 2*3 + 1 + 1; cfg 5 is l2_p50's pre-pool
+    tensor, (16-1)*2 - 2 + 3 = 31 and (32-1)*2 - 2 + 3 = 63)."""
     want = {0: (2, 16, 7, 15, 15), 1: (16, 32, 64, 64, 128), 2: (128, 16, 15, 31, 31),
-            3: (32, 64, 131084), 4: (16, 64, 131076)}
+            3: (32, 64, 131084), 4: (16, 64, 131076), 5: (128, 16, 31, 63, 63)}
     for cfg, shape in want.items():
         wl = workloads.get(cfg)
         p = wl.params
@@ -73,6 +74,9 @@ def test_workload_output_shapes():
                                                            p["pool_k"])
         elif wl.op == "avgpool3d":
             st, out = B.aps_avgpool3d_out_shape(xs, p["k"], p["stride"], p["pad"], p["ceil_mode"])
+        elif wl.op == "convtranspose3d":
+            st, out = B.aps_convtranspose3d_out_shape(xs, p["c_out"], p["k"], p["stride"],
+                                                      p["pad"], p["dil"], p["out_pad"])
         else:
             st, out = B.aps_convtranspose1d_out_shape(xs, p["c_out"], p["k"], p["stride"],
                                                       p["pad"], p["dil"], p["out_pad"])
@@ -157,3 +161,23 @@ def test_tensor_api_requires_cuda_tensors():
     import torch
     with pytest.raises(TypeError):
         B.avgpool3d(torch.zeros(1, 1, 4, 4, 4))
+
+
+def test_convtranspose3d_shape_query_matches_closed_form_and_rejects_bad_params():
+    """O = (I-1)*s - 2p + d*(k-1) + op + 1 per dim; out_pad must be < max(s, d)."""
+    cases = [((1, 2, 4, 5, 6), (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (0, 1, 0)),
+             ((2, 1, 3, 3, 3), (2, 3, 4), (1, 2, 3), (0, 1, 2), (2, 1, 1), (1, 1, 2))]
+    for xs, k, s, p, d, op in cases:
+        st, out = B.aps_convtranspose3d_out_shape(xs, 7, k, s, p, d, op)
+        want = tuple((xs[2 + i] - 1) * s[i] - 2 * p[i] + d[i] * (k[i] - 1) + op[i] + 1
+                     for i in range(3))
+        assert st == 0 and out == (xs[0], 7) + want, (st, out, want)
+    st, _ = B.aps_convtranspose3d_out_shape((1, 1, 4, 4, 4), 2, (3, 3, 3), (2, 2, 2),
+                                            (1, 1, 1), (1, 1, 1), (2, 0, 0))
+    assert st == B.APS_ERR_SHAPE
+    st, _ = B.aps_convtranspose3d_out_shape((1, 1, 4, 4, 4), 0, (3, 3, 3), (2, 2, 2),
+                                            (1, 1, 1), (1, 1, 1), (0, 0, 0))
+    assert st == B.APS_ERR_SHAPE
+    st = B.aps_convtranspose3d(0, (1, 1, 4, 4, 4), 0, 0, 2, (3, 3, 3), (2, 2, 2), (1, 1, 1),
+                               (1, 1, 1), (0, 0, 0), 0)
+    assert st == B.APS_ERR_NULL

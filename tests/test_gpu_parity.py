@@ -171,6 +171,46 @@ def test_fused_general_geometry(cout, k, s, p, op, d, q):
     assert_close(fused_gpu(x, w, cb, b, prm), ref, what=f"fused general {k} {s} {p} {op} {d} {q}")
 
 
+# ------------------------------------------------------------ convtranspose3d
+CONVT3D_CASES = [  # (x shape, C_out, k, s, p, d, op, bias)
+    # the k3 s2 p1 d1 kernel: one and two column blocks, C_in 1..8, output padding
+    ((2, 3, 5, 9, 12), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (0, 0, 0), True),
+    ((1, 3, 4, 19, 36), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (0, 0, 0), True),
+    ((2, 8, 3, 17, 8), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (1, 1, 1), False),
+    ((1, 1, 6, 6, 4), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (0, 1, 0), True),
+    ((1, 3, 2, 2, 68), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (1, 0, 1), True),
+    # W % 4 != 0 (no TMA) and other geometries: the direct kernel
+    ((2, 3, 4, 5, 10), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (0, 0, 0), True),
+    ((1, 2, 3, 4, 5), 5, (2, 3, 4), (1, 2, 3), (0, 1, 2), (2, 1, 1), (1, 1, 2), True),
+    ((2, 4, 3, 3, 3), 7, (1, 1, 1), (1, 1, 1), (0, 0, 0), (1, 1, 1), (0, 0, 0), False),
+    ((1, 3, 5, 4, 4), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (2, 2, 2), (1, 1, 1), True),
+]
+
+
+@pytest.mark.parametrize("xs,cout,k,s,p,d,op,has_bias", CONVT3D_CASES)
+def test_convt3d_cases(xs, cout, k, s, p, d, op, has_bias):
+    x, = rng_inputs(31, xs)
+    w, b = rng_inputs(32, (xs[1], cout) + tuple(k), (cout,), lo=-0.3, hi=0.3)
+    b = b if has_bias else None
+    y = B.convtranspose3d(dev(x), dev(w), None if b is None else dev(b), s, p, d, op)
+    assert_close(y.cpu().numpy(), ora.convt(x, w, b, s, p, d, op),
+                 what=f"convt3d {xs} k{k} s{s} p{p} d{d} op{op}")
+
+
+def test_convt3d_full_workload_sampled_planes():
+    wl = workloads.get(5)
+    p = wl.params
+    x, w, b = wl.generate("x"), wl.generate("w"), wl.generate("bias")
+    y = B.convtranspose3d(dev(x), dev(w), dev(b), p["stride"], p["pad"], p["dil"], p["out_pad"])
+    torch.cuda.synchronize()
+    N, C = y.shape[0], y.shape[1]
+    sel = [(0, 0), (N - 1, C - 1), (N // 2, 7), (5, 12)]
+    ref = ora.convt(x, w, b, p["stride"], p["pad"], p["dil"], p["out_pad"], sel=sel)
+    got = np.stack([y[n, c].cpu().numpy() for n, c in sel])
+    assert_close(got, ref, what="convt3d full workload")
+    assert torch.isfinite(y).all()
+
+
 # ------------------------------------------------------------ convtranspose1d
 CONVT_CASES = [  # (s, K, d, p, op, Cin, Cout, L, bias)
     (1, 5, 3, 0, 0, 32, 64, 1000, False),
