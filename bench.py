@@ -15,8 +15,9 @@ also carries:
   * cpu_baseline -- the fp64 oracle on the host cores, on a bounded sample of
     (n, c) planes of the same workload;
   * clocks -- nvidia-smi samples taken during the timed region;
-  * per_config -- the other four workloads (fused op tiny / full size, the two
-    ConvTranspose1d workloads) with outputs/s and their own roofline fraction.
+  * per_config -- the other workloads (fused op tiny / full size, the two
+    ConvTranspose1d workloads in fp32 and tf32, the standalone ConvTranspose3d)
+    with outputs/s and their own roofline fraction.
 
 `--impl reference` times the oracle itself (the only other leg that runs
 oracle code) on the same workload and prints the same line shape.
@@ -174,6 +175,9 @@ def workload_desc(wl):
     if wl.op == "ct3d_scale_pool_bias":
         return (f"convtranspose3d(k3,s2,p1)+x{p['scale1']}+avgpool3d(2)+bias+x{p['scale2']} "
                 f"x[{shp}] fp32")
+    if wl.op == "convtranspose3d":
+        return (f"convtranspose3d k3 s2 p1 d1 op0 x[{shp}] -> C_out {p['c_out']} "
+                f"(the pre-pool tensor) fp32")
     return (f"convtranspose1d K{p['k']} s{p['stride']} p{p['pad']} d{p['dil']} "
             f"op{p['out_pad']} x[{shp}] -> C_out {p['c_out']} fp32")
 
@@ -213,6 +217,15 @@ class GpuCase:
                 p["pool_k"])
             self.flops = 2 * 8 * x.shape[1] * numel(oshape)   # 8 collapsed taps per ci
             self.bound = "hbm+alu"
+        elif wl.op == "convtranspose3d":
+            st, oshape = aps.binding.aps_convtranspose3d_out_shape(
+                x.shape, p["c_out"], p["k"], p["stride"], p["pad"], p["dil"], p["out_pad"])
+            pairs = 1
+            for i in range(3):   # in-range taps, per dim
+                pairs *= convt_pairs(x.shape[2 + i], oshape[2 + i], p["k"][i], p["stride"][i],
+                                     p["pad"][i], p["dil"][i])
+            self.flops = 2 * x.shape[0] * x.shape[1] * p["c_out"] * pairs
+            self.bound = "hbm+alu"
         else:
             st, oshape = aps.binding.aps_convtranspose1d_out_shape(
                 x.shape, p["c_out"], p["k"], p["stride"], p["pad"], p["dil"], p["out_pad"])
@@ -243,6 +256,10 @@ class GpuCase:
                 d["x"].data_ptr(), d["x"].shape, d["w"].data_ptr(), d["conv_bias"].data_ptr(),
                 d["bias"].data_ptr(), p["c_out"], p["k"], p["stride"], p["pad"], p["out_pad"],
                 p["dil"], p["pool_k"], p["scale1"], p["scale2"], self.y.data_ptr(), s)
+        elif self.wl.op == "convtranspose3d":
+            st = B.aps_convtranspose3d(d["x"].data_ptr(), d["x"].shape, d["w"].data_ptr(),
+                                       d["bias"].data_ptr(), p["c_out"], p["k"], p["stride"],
+                                       p["pad"], p["dil"], p["out_pad"], self.y.data_ptr(), s)
         else:
             bias = d["bias"].data_ptr() if "bias" in d else 0
             st = B.aps_convtranspose1d(d["x"].data_ptr(), d["x"].shape, d["w"].data_ptr(), bias,
@@ -504,6 +521,7 @@ def run_native(args):
     roof = roofline_for(case, per_launch, peaks, peak_src, clocks.get("sm_mhz"))
     kernel_of = {"avgpool3d": ("avgpool3d.cu", "avgpool3d_k3s2p1_tma_kernel"),
                  "ct3d_scale_pool_bias": ("ct3d_pool.cu", "ct3d_pool2_fast_kernel"),
+                 "convtranspose3d": ("convt3d.cu", "convt3d_k3s2p1_kernel"),
                  "convtranspose1d": (("convt1d_tc.cu", "convt1d_tf32_kernel") if case.precision
                                      else ("convt1d.cu", "convt1d_tiled_kernel"))}[case.wl.op]
     roof["kernel"] = kernel_of[1]
@@ -534,7 +552,7 @@ def run_native(args):
     if rank == 0 and not args.no_per_config:
         per = {}
         flush = torch.empty(64 * 1024 * 1024, device="cuda")   # 256 MB > L2
-        for cfg, prec in ((0, 0), (2, 0), (3, 0), (4, 0), (3, 1), (4, 1)):
+        for cfg, prec in ((0, 0), (2, 0), (3, 0), (4, 0), (3, 1), (4, 1), (5, 0)):
             c = GpuCase(cfg, torch, aps, precision=prec)
             for _ in range(3):
                 c.launch()
@@ -545,6 +563,9 @@ def run_native(args):
             elif cfg == 2:
                 t = time_launches(torch, c, 30, flush)
                 how = "30 launches, 256 MB L2 flush before each, events per launch"
+            elif cfg == 5:
+                t = time_launches(torch, c, 20)
+                how = "20 back-to-back launches (output 1.0 GB, larger than L2)"
             else:
                 t = time_launches(torch, c, 20)
                 how = "20 back-to-back launches (input larger than L2)"
