@@ -31,6 +31,7 @@ APS_ERR_CUDA = -6
 APS_DEVERR_TIMEOUT = 1
 APS_PREC_FP32 = 0
 APS_PREC_TF32 = 1
+APS_PREC_TF32X3 = 2
 
 # Every symbol include/aps.h declares.
 EXPORTS = [

@@ -352,13 +352,16 @@ aps_status aps_convtranspose1d(const float *x, const int64_t in[3], const float 
     int64_t out[3];
     aps_status st = aps_convtranspose1d_out_shape(in, c_out, k, s, p, d, op, out);
     if (st != APS_OK) return st;
-    if (precision != APS_PREC_FP32 && precision != APS_PREC_TF32) return APS_ERR_SHAPE;
+    if (precision != APS_PREC_FP32 && precision != APS_PREC_TF32 &&
+        precision != APS_PREC_TF32X3)
+        return APS_ERR_SHAPE;
     if (!aligned(x, 4) || !aligned(w, 4) || !aligned(y, 4) || (bias && !aligned(bias, 4)))
         return APS_ERR_ALIGN;
     if (numel(out, 3) == 0) return APS_OK;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    if (precision == APS_PREC_TF32)
-        return launch_convt1d_tf32(x, in, w, bias, c_out, k, s, p, d, y, out[2], cs);
+    if (precision != APS_PREC_FP32)
+        return launch_convt1d_tf32(x, in, w, bias, c_out, k, s, p, d, y, out[2],
+                                   precision == APS_PREC_TF32X3, cs);
     if (in[1] >= 1) {
         st = launch_convt1d_tiled(x, in, w, bias, c_out, k, s, p, d, y, out[2], cs);
         if (st != APS_ERR_UNSUPPORTED) return st;

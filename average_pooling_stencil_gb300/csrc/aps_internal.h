@@ -84,7 +84,7 @@ aps_status launch_convt1d_tiled(const float *x, const int64_t in[3], const float
 // taps; returns APS_ERR_UNSUPPORTED otherwise.
 aps_status launch_convt1d_tf32(const float *x, const int64_t in[3], const float *w,
                                const float *bias, int64_t c_out, int k, int s, int p, int d,
-                               float *y, int64_t l_out, cudaStream_t st);
+                               float *y, int64_t l_out, bool split, cudaStream_t st);
 
 aps_status launch_convt1d_direct(const float *x, const int64_t in[3], const float *w,
                                  const float *bias, int64_t c_out, int k, int s, int p,

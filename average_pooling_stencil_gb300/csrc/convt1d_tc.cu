@@ -48,9 +48,9 @@
 namespace aps {
 namespace tc1 {
 constexpr int BM = 128;           // positions per tile (MMA M)
-constexpr int CK = 32;            // input channels per staged chunk (MMA K per chunk)
+constexpr int CK = 32;            // input channels per staged chunk (at most; MMA K per chunk)
 constexpr int RAW_STAGES = 4;    // at most; the launcher may use fewer to fit smem
-constexpr int XT_STAGES = 3;
+constexpr int XT_STAGES = 3;      // converted-operand stages (at most; the launcher may use 2)
 constexpr int MAX_CLASSES = 4;
 constexpr int MAX_TAPS = 8;       // taps per class
 constexpr int NBUF = 4;           // TMA-store staging slabs in flight (at most; 2 if smem is short)
@@ -144,27 +144,36 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 }
 }  // namespace tc1
 
+// SPLIT: 3xTF32 (operands split into tf32 hi + lo, three MMAs per product).
+template <bool SPLIT>
 __global__ void __launch_bounds__(tc1::THREADS, 1)
     convt1d_tf32_kernel(const __grid_constant__ CUtensorMap xmap,
                         const __grid_constant__ CUtensorMap ymap, const float *__restrict__ w,
                         const float *__restrict__ bias, float *__restrict__ y, int Cin, int Cout,
                         int K, int S, int L_out, int n_mtiles, long long n_units, int win0, int BW,
                         int tmem_cols, int nacc, int RS, int nbuf, int dgroups, int vec_store,
-                        int tma_store,
+                        int tma_store, int CKr, int XTS,
                         const __grid_constant__ tc1::Taps taps, unsigned int *status) {
     using namespace tc1;
+    constexpr bool split = SPLIT;
     extern __shared__ __align__(1024) unsigned char smem[];
-    const int CKr = Cin < CK ? Cin : CK;          // channels per chunk
+    // CKr: channels per chunk; XTS: converted-operand stages.  split: operands
+    // are split as v = hi + lo (both tf32) and each product is accumulated as
+    // lo(x)*hi(w) + hi(x)*lo(w) + hi(x)*hi(w) (3xTF32, fp32-level accuracy);
+    // the lo halves sit XT_LO bytes after a stage's hi half and W_LO bytes
+    // after the hi weights.
     const int nchunks = Cin / CKr;
     const uint32_t LBO_X = (uint32_t)BW * 16 + 16;   // 16-byte pad: conflict-free transposes
     const uint32_t XT_BYTES = (uint32_t)(CKr / 4) * LBO_X;
-    const uint32_t XT_STRIDE = (XT_BYTES + 1023) & ~1023u;
+    const uint32_t XT_LO = split ? ((XT_BYTES + 127u) & ~127u) : 0u;
+    const uint32_t XT_STRIDE = (XT_LO + XT_BYTES + 1023) & ~1023u;
     const uint32_t RAW_BYTES = (uint32_t)CKr * BW * 4;
     const uint32_t RAW_STRIDE = (RAW_BYTES + 1023) & ~1023u;
     unsigned char *xt = smem;
-    unsigned char *raw = xt + XT_STAGES * XT_STRIDE;
-    float *wt = reinterpret_cast<float *>(raw + RS * RAW_STRIDE);   // [K][Cin/4][Cout][4]
-    float *bs = wt + (size_t)K * Cin * Cout;
+    unsigned char *raw = xt + XTS * XT_STRIDE;
+    float *wt = reinterpret_cast<float *>(raw + RS * RAW_STRIDE);   // [K][Cin/4][Cout][4] (x2)
+    const uint32_t W_LO = split ? (uint32_t)K * Cin * Cout * 4u : 0u;
+    float *bs = wt + (size_t)K * Cin * Cout * (split ? 2 : 1);
     const int OROW = BM * S + 4;                   // staged output row (one channel)
     const int SLAB = S == 1 ? 32 : 16;             // channels per TMA-stored slab
     // epilogue staging, 1 KB aligned (offset from the shared array so the
@@ -196,7 +205,7 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
             mbar_init(&raw_full[s], 1);
             mbar_init(&raw_empty[s], CONVERTERS);
         }
-        for (int s = 0; s < XT_STAGES; ++s) {
+        for (int s = 0; s < XTS; ++s) {
             mbar_init(&xt_full[s], CONVERTERS);
             mbar_init(&xt_empty[s], 1);
         }
@@ -228,7 +237,10 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
             const int cb = t % (Cin / 4);
             const int k = t / (Cin / 4);
             const int ci = cb * 4 + j;
-            wtu[e] = to_tf32(__ldg(w + ((size_t)ci * Cout + co) * K + k));
+            const float v = __ldg(w + ((size_t)ci * Cout + co) * K + k);
+            const uint32_t hi = to_tf32(v);
+            wtu[e] = hi;
+            if (split) wtu[total + e] = to_tf32(v - __uint_as_float(hi));
         }
         for (int c = threadIdx.x; c < Cout; c += THREADS) bs[c] = bias ? __ldg(bias + c) : 0.f;
     }
@@ -304,7 +316,10 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
             uint64_t a_stage[XT_STAGES];
             for (int st = 0; st < XT_STAGES; ++st)
                 a_stage[st] = tc1::umma_desc(smem_u32(xt) + st * XT_STRIDE, LBO_X, 128);
-            uint32_t it = 0, tile = 0;
+            // lo halves: the same descriptors with the start address moved
+            const uint32_t a_lo = XT_LO >> 4, b_lo = W_LO >> 4;
+            uint32_t tile = 0;
+            uint32_t xs_i = 0, xs_ph = 0;   // converted stage and its phase parity
             bool issued = false;
             for (long long u = blockIdx.x; u < n_units && !abort_flag; u += gridDim.x, ++tile) {
                 const uint32_t b = tile % (uint32_t)nacc;
@@ -317,9 +332,9 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
                 tc1::tc_fence_after();
                 const uint32_t dbase = tmem_base + b * taps.nclass * (uint32_t)Cout;
                 bool fail = false;
-                for (int ch = 0; ch < nchunks; ++ch, ++it) {
-                    const uint32_t s = it % XT_STAGES;
-                    if (!mbar_wait(&xt_full[s], (it / XT_STAGES) & 1u)) {
+                for (int ch = 0; ch < nchunks; ++ch) {
+                    const uint32_t s = xs_i;
+                    if (!mbar_wait(&xt_full[s], xs_ph)) {
                         record_error(status, APS_DEVERR_TIMEOUT);
                         abort_flag = 1;
                         fail = true;
@@ -328,15 +343,32 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
                     tc1::tc_fence_after();
                     const uint64_t abase = s == 0 ? a_stage[0] : (s == 1 ? a_stage[1] : a_stage[2]);
                     const uint64_t *bt = tab_b + ch * n_ent;
+                    if constexpr (split) {
+#pragma unroll 2
+                        for (int e = 0; e < n_ent; ++e) {
+                            const uint32_t ae = tab_a[e];
+                            const uint32_t acc = (ch != 0 || !(ae >> 31)) ? 1u : 0u;
+                            const uint32_t d = dbase + ((ae >> 16) & 0xFFu) * (uint32_t)Cout;
+                            const uint64_t a = abase + (ae & 0xFFFFu), bw = bt[e];
+                            tc1::umma_tf32(d, a + a_lo, bw, idesc, acc);   // lo(x) hi(w)
+                            tc1::umma_tf32(d, a, bw + b_lo, idesc, 1u);    // hi(x) lo(w)
+                            tc1::umma_tf32(d, a, bw, idesc, 1u);           // hi(x) hi(w)
+                        }
+                    } else {
 #pragma unroll 4
-                    for (int e = 0; e < n_ent; ++e) {
-                        const uint32_t ae = tab_a[e];
-                        const uint32_t acc = (ch != 0 || !(ae >> 31)) ? 1u : 0u;
-                        tc1::umma_tf32(dbase + ((ae >> 16) & 0xFFu) * (uint32_t)Cout,
-                                       abase + (ae & 0xFFFFu), bt[e], idesc, acc);
+                        for (int e = 0; e < n_ent; ++e) {
+                            const uint32_t ae = tab_a[e];
+                            const uint32_t acc = (ch != 0 || !(ae >> 31)) ? 1u : 0u;
+                            tc1::umma_tf32(dbase + ((ae >> 16) & 0xFFu) * (uint32_t)Cout,
+                                           abase + (ae & 0xFFFFu), bt[e], idesc, acc);
+                        }
                     }
                     issued = true;
                     tc1::umma_commit(&xt_empty[s]);
+                    if (++xs_i == (uint32_t)XTS) {
+                        xs_i = 0;
+                        xs_ph ^= 1u;
+                    }
                 }
                 if (fail) break;
                 tc1::umma_commit(&acc_full[b]);
@@ -500,13 +532,13 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
         // converter warp cb owns channels 4cb..4cb+3 of every chunk
         const int cb = converter_id(warp);
         uint32_t it = 0;
+        uint32_t xs_i = 0, xs_ph = 0;   // converted stage and its phase parity
         for (long long u = blockIdx.x; u < n_units && !abort_flag; u += gridDim.x) {
             bool fail = false;
             for (int ch = 0; ch < nchunks; ++ch, ++it) {
-                const uint32_t rs = it % RS, xs = it % XT_STAGES;
+                const uint32_t rs = it % RS, xs = xs_i;
                 if (!mbar_wait(&raw_full[rs], (it / RS) & 1u) ||
-                    (it >= (uint32_t)XT_STAGES &&
-                     !mbar_wait(&xt_empty[xs], ((it / XT_STAGES) & 1u) ^ 1u))) {
+                    (it >= (uint32_t)XTS && !mbar_wait(&xt_empty[xs], xs_ph ^ 1u))) {
                     record_error(status, APS_DEVERR_TIMEOUT);
                     abort_flag = 1;
                     fail = true;
@@ -519,17 +551,36 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
                     // and the 16-byte row writes of a warp are each contiguous, so
                     // neither has bank conflicts
                     uint4 *d0 = reinterpret_cast<uint4 *>(xt + xs * XT_STRIDE + cb * LBO_X);
+                    if constexpr (split) {
+                        uint4 *d1 = reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(d0) + XT_LO);
+                        for (int pos = lane; pos < BW; pos += 32) {
+                            const float v0 = s0[pos], v1 = s0[BW + pos], v2 = s0[2 * BW + pos],
+                                        v3 = s0[3 * BW + pos];
+                            const uint4 h = make_uint4(tc1::to_tf32(v0), tc1::to_tf32(v1),
+                                                       tc1::to_tf32(v2), tc1::to_tf32(v3));
+                            d0[pos] = h;
+                            d1[pos] = make_uint4(tc1::to_tf32(v0 - __uint_as_float(h.x)),
+                                                 tc1::to_tf32(v1 - __uint_as_float(h.y)),
+                                                 tc1::to_tf32(v2 - __uint_as_float(h.z)),
+                                                 tc1::to_tf32(v3 - __uint_as_float(h.w)));
+                        }
+                    } else {
 #pragma unroll 2
-                    for (int pos = lane; pos < BW; pos += 32)
-                        d0[pos] = make_uint4(tc1::to_tf32(s0[pos]), tc1::to_tf32(s0[BW + pos]),
-                                             tc1::to_tf32(s0[2 * BW + pos]),
-                                             tc1::to_tf32(s0[3 * BW + pos]));
+                        for (int pos = lane; pos < BW; pos += 32)
+                            d0[pos] = make_uint4(tc1::to_tf32(s0[pos]), tc1::to_tf32(s0[BW + pos]),
+                                                 tc1::to_tf32(s0[2 * BW + pos]),
+                                                 tc1::to_tf32(s0[3 * BW + pos]));
+                    }
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&raw_empty[rs]);
                     mbar_arrive(&xt_full[xs]);
+                }
+                if (++xs_i == (uint32_t)XTS) {
+                    xs_i = 0;
+                    xs_ph ^= 1u;
                 }
             }
             if (fail) break;
@@ -553,7 +604,7 @@ int floordiv_h(int a, int b) { return (a >= 0) ? a / b : -((-a + b - 1) / b); }
 
 aps_status launch_convt1d_tf32(const float *x, const int64_t in[3], const float *w,
                                const float *bias, int64_t c_out, int k, int s, int p, int d,
-                               float *y, int64_t l_out, cudaStream_t st) {
+                               float *y, int64_t l_out, bool split, cudaStream_t st) {
     using namespace tc1;
     const int64_t N = in[0], Cin = in[1], L = in[2];
     if (Cin % 8 != 0 || (Cin > CK && Cin % CK != 0) || c_out % 32 != 0 || c_out > 256 ||
@@ -610,40 +661,55 @@ aps_status launch_convt1d_tf32(const float *x, const int64_t in[3], const float 
     int cols = 32;
     while (cols < nacc * taps.nclass * (int)c_out) cols *= 2;
 
-    const int CKr = Cin < CK ? (int)Cin : CK;
     const uint32_t LBO_X = (uint32_t)BW * 16 + 16;
-    const uint32_t XT_STRIDE = ((uint32_t)(CKr / 4) * LBO_X + 1023) & ~1023u;
-    const uint32_t RAW_STRIDE = ((uint32_t)CKr * BW * 4 + 1023) & ~1023u;
-    const size_t w_bytes = (size_t)k * Cin * c_out * 4;
-    int n_ent = 0;   // MMAs per chunk; the descriptor table holds them for every chunk
-    for (int c = 0; c < taps.nclass; ++c) n_ent += taps.ntaps[c] * (CKr / 8);
-    if (n_ent * (int)(Cin / CKr) > MAX_MMA_TAB) return APS_ERR_UNSUPPORTED;
+    // split (3xTF32): hi and lo copies of the weights and of each converted stage
+    const size_t w_bytes = (size_t)k * Cin * c_out * 4 * (split ? 2 : 1);
     // the output leaves by TMA store when a tile's outputs form a <= 256-wide box
     // and the output rows are 16-byte strided
     const int tma_store = (s <= 2 && l_out % 4 == 0) ? 1 : 0;
     // 227 KB per CTA, less the 1 KB of static shared memory the kernel declares
     const size_t budget = 227 * 1024 - 1024;
-    // deepest input ring and store staging that fit: 4 staging slabs if the
-    // raw ring can still hold 2 stages, otherwise 2
-    // (for direct stores: two epilogue groups' staging blocks, else one)
-    int RS = RAW_STAGES, nbuf = tma_store ? NBUF : 0, dgroups = tma_store ? 0 : 2;
-    size_t smem = 0;
-    for (;;) {
-        const size_t ost_bytes = tma_store ? (size_t)nbuf * (s == 1 ? 32 : 16) * BM * s * 4
-                                           : (size_t)dgroups * 32 * (BM * s + 4) * 4;
-        const size_t fixed = XT_STAGES * XT_STRIDE + w_bytes + (size_t)c_out * 4 + 1024 +
-                             ost_bytes + (2 * RAW_STAGES + 2 * XT_STAGES + 2 * MAX_ACC + 1) * 8 +
-                             16 + MAX_MMA_TAB * 8 + MAX_MMA_TAB * 4;
-        RS = RAW_STAGES;
-        while (RS > 2 && fixed + RS * RAW_STRIDE > budget) --RS;
-        smem = fixed + RS * RAW_STRIDE;
-        if (smem <= budget) break;
-        if (tma_store && nbuf == 4) {
-            nbuf = 2;
-        } else if (!tma_store && dgroups == 2) {
-            dgroups = 1;
-        } else {
-            break;
+    // Deepest pipeline that fits, trying in order: chunks of 32 channels then
+    // (split only) 16; 3 converted stages then 2; then, as before, 4 staging
+    // slabs if the raw ring can still hold 2 stages, otherwise 2 (for direct
+    // stores: two epilogue groups' staging blocks, else one).
+    int CKr = 0, XTS = 0, RS = 0, nbuf = 0, dgroups = 0;
+    size_t smem = budget + 1;
+    const int ck_try[2] = {Cin < CK ? (int)Cin : CK, (split && Cin >= 16) ? 16 : 0};
+    for (int ci = 0; ci < 2 && smem > budget; ++ci) {
+        const int ck = ck_try[ci];
+        if (ck == 0 || (ci == 1 && ck == ck_try[0]) || Cin % ck != 0) continue;
+        int n_ent = 0;   // MMAs per chunk; the descriptor table holds them for every chunk
+        for (int c = 0; c < taps.nclass; ++c) n_ent += taps.ntaps[c] * (ck / 8);
+        if (n_ent * (int)(Cin / ck) > MAX_MMA_TAB) continue;
+        const uint32_t xt_bytes = (uint32_t)(ck / 4) * LBO_X;
+        const uint32_t xt_lo = split ? ((xt_bytes + 127u) & ~127u) : 0u;
+        const uint32_t XT_STRIDE = (xt_lo + xt_bytes + 1023) & ~1023u;
+        const uint32_t RAW_STRIDE = ((uint32_t)ck * BW * 4 + 1023) & ~1023u;
+        for (int xts = XT_STAGES; xts >= (split ? 2 : XT_STAGES) && smem > budget; --xts) {
+            int rs = RAW_STAGES, nb = tma_store ? NBUF : 0, dg = tma_store ? 0 : 2;
+            for (;;) {
+                const size_t ost_bytes = tma_store ? (size_t)nb * (s == 1 ? 32 : 16) * BM * s * 4
+                                                   : (size_t)dg * 32 * (BM * s + 4) * 4;
+                const size_t fixed = xts * XT_STRIDE + w_bytes + (size_t)c_out * 4 + 1024 +
+                                     ost_bytes +
+                                     (2 * RAW_STAGES + 2 * XT_STAGES + 2 * MAX_ACC + 1) * 8 +
+                                     16 + MAX_MMA_TAB * 8 + MAX_MMA_TAB * 4;
+                rs = RAW_STAGES;
+                while (rs > 2 && fixed + rs * RAW_STRIDE > budget) --rs;
+                const size_t need = fixed + rs * RAW_STRIDE;
+                if (need <= budget) {
+                    CKr = ck, XTS = xts, RS = rs, nbuf = nb, dgroups = dg, smem = need;
+                    break;
+                }
+                if (tma_store && nb == 4) {
+                    nb = 2;
+                } else if (!tma_store && dg == 2) {
+                    dg = 1;
+                } else {
+                    break;
+                }
+            }
         }
     }
     if (smem > budget) return APS_ERR_UNSUPPORTED;
@@ -667,16 +733,17 @@ aps_status launch_convt1d_tf32(const float *x, const int64_t in[3], const float 
     } else {
         ymap = map;   // unused
     }
-    const int per_sm = resident_ctas((const void *)convt1d_tf32_kernel, THREADS, (int)smem);
+    const auto kern = split ? convt1d_tf32_kernel<true> : convt1d_tf32_kernel<false>;
+    const int per_sm = resident_ctas((const void *)kern, THREADS, (int)smem);
     if (per_sm < 1) return APS_ERR_UNSUPPORTED;
     const int64_t M = ceil_div(l_out, s);
     const int n_mtiles = (int)ceil_div(M, BM);
     const long long n_units = (long long)N * n_mtiles;
     const long long grid = std::min<long long>(n_units, (long long)sm_count());
     const int vec = (l_out % 4 == 0) && (reinterpret_cast<uintptr_t>(y) % 16 == 0);
-    convt1d_tf32_kernel<<<(unsigned)grid, THREADS, smem, st>>>(
+    kern<<<(unsigned)grid, THREADS, smem, st>>>(
         map, ymap, w, bias, y, (int)Cin, (int)c_out, k, s, (int)l_out, n_mtiles, n_units, win0,
-        BW, cols, nacc, RS, nbuf, dgroups, vec, tma_store, taps, status_word());
+        BW, cols, nacc, RS, nbuf, dgroups, vec, tma_store, CKr, XTS, taps, status_word());
     return launch_status();
 }
 

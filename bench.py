@@ -59,7 +59,7 @@ def parse_args_from(argv):
     ap.add_argument("--e2e-steps", type=int, default=8, help="0 skips the e2e leg")
     ap.add_argument("--workload", type=int, default=HEADLINE_CFG,
                     help="workload of the headline line (default: the avgpool workload)")
-    ap.add_argument("--precision", choices=["fp32", "tf32"], default="fp32",
+    ap.add_argument("--precision", choices=["fp32", "tf32", "tf32x3"], default="fp32",
                     help="ConvTranspose1d precision of the headline workload")
     ap.add_argument("--x-shape", type=str, default=None,
                     help="override the input shape of the headline workload (profiling "
@@ -476,7 +476,7 @@ def run_native(args):
     # ---- headline: each rank runs its own full workload (weak scaling)
     x_shape = tuple(int(v) for v in args.x_shape.split(",")) if args.x_shape else None
     case = GpuCase(args.workload, torch, aps, with_host=args.e2e_steps > 0, x_shape=x_shape,
-                   precision=1 if args.precision == "tf32" else 0)
+                   precision={"fp32": 0, "tf32": 1, "tf32x3": 2}[args.precision])
     for _ in range(max(3, args.warmup)):
         case.launch()
     barrier()
@@ -552,7 +552,7 @@ def run_native(args):
     if rank == 0 and not args.no_per_config:
         per = {}
         flush = torch.empty(64 * 1024 * 1024, device="cuda")   # 256 MB > L2
-        for cfg, prec in ((0, 0), (2, 0), (3, 0), (4, 0), (3, 1), (4, 1), (5, 0)):
+        for cfg, prec in ((0, 0), (2, 0), (3, 0), (4, 0), (3, 1), (4, 1), (3, 2), (4, 2), (5, 0)):
             c = GpuCase(cfg, torch, aps, precision=prec)
             for _ in range(3):
                 c.launch()
@@ -569,8 +569,9 @@ def run_native(args):
             else:
                 t = time_launches(torch, c, 20)
                 how = "20 back-to-back launches (input larger than L2)"
-            per[c.wl.name + ("_tf32" if prec else "")] = {
-                "workload": workload_desc(c.wl) + (" (tf32 tensor cores)" if prec else ""),
+            per[c.wl.name + ("", "_tf32", "_tf32x3")[prec]] = {
+                "workload": workload_desc(c.wl) + ("", " (tf32 tensor cores)",
+                                                   " (3xTF32 tensor cores, fp32 accuracy)")[prec],
                 "outputs_per_s": c.outputs / t,
                 "us_per_launch": 1e6 * t, "gb_per_s": c.bytes / t / 1e9,
                 "tflop_per_s": c.flops / t / 1e12, "algorithmic_bytes": c.bytes,

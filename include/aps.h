@@ -76,6 +76,9 @@ typedef enum {
 #define APS_PREC_FP32 0   /* fp32 FMA; max |y - exact| <= 1e-5 * (1 + |exact|) */
 #define APS_PREC_TF32 1   /* tcgen05 tensor cores, tf32 operands, fp32 accumulate;
                              ||y - exact||_F <= 5e-3 * ||exact||_F */
+#define APS_PREC_TF32X3 2 /* tensor cores, each operand split v = hi + lo (tf32) and
+                             each product summed as lo*hi + hi*lo + hi*hi (3xTF32);
+                             max |y - exact| <= 1e-5 * (1 + |exact|), as fp32 */
 
 /* Version of this ABI (bumped on any incompatible change). */
 int aps_abi_version(void);
@@ -170,15 +173,18 @@ aps_status aps_convtranspose3d(const float *x, const int64_t in_ncdhw[5], const 
  *
  * x: [N, C_in, L]; w: [C_in, C_out, K]; bias: [C_out] or NULL (no bias);
  * y: [N, C_out, L_out] (shape from aps_convtranspose1d_out_shape).  Requires
- * K, s, d >= 1, p >= 0, 0 <= out_pad < max(s, d).  precision: APS_PREC_FP32 or
- * APS_PREC_TF32 (tolerances above).  APS_PREC_TF32 returns APS_ERR_UNSUPPORTED
+ * K, s, d >= 1, p >= 0, 0 <= out_pad < max(s, d).  precision: APS_PREC_FP32,
+ * APS_PREC_TF32 or APS_PREC_TF32X3 (tolerances above).  The two tensor-core
+ * precisions return APS_ERR_UNSUPPORTED
  * (nothing launched) unless: C_in % 8 == 0 and, above 32, C_in % 32 == 0;
  * C_out % 32 == 0 and (number of output residues mod s that some tap reaches)
  * x C_out <= 256; L % 4 == 0 and x 16-byte aligned; s <= 8, at most 4
  * reached residues with at most 8 taps each; the tap span d*(K-1)/s <= 124;
  * K * C_in <= 2048 (the per-tile MMA descriptor table);
- * and the weights (K*C_in*C_out*4 bytes) plus the staging buffers fit in one
- * CTA's 227 KB of shared memory.  APS_PREC_FP32 accepts every valid shape.
+ * and the weights (K*C_in*C_out*4 bytes, twice that for APS_PREC_TF32X3, which
+ * also holds two copies of each converted stage and may stage 16 channels at a
+ * time) plus the staging buffers fit in one CTA's 227 KB of shared memory.
+ * APS_PREC_FP32 accepts every valid shape.
  */
 aps_status aps_convtranspose1d_out_shape(const int64_t in_ncl[3], int64_t c_out, int k,
                                          int stride, int pad, int dil, int out_pad,

@@ -306,6 +306,55 @@ def test_convt1d_tf32_cases(s, K, d, p, op, cin, cout, L, has_bias):
                      what=f"tf32 s{s} K{K} d{d} p{p} op{op} {cin}->{cout} L{L}")
 
 
+# 3xTF32 (APS_PREC_TF32X3): the fp32 elementwise bound, on the tensor cores
+TF32X3_CASES = [  # (s, K, d, p, op, Cin, Cout, L, bias)
+    (1, 5, 3, 0, 0, 32, 64, 1000, False),
+    (2, 4, 2, 1, 1, 64, 64, 516, True),     # hi+lo weights 128 KB: 16-channel chunks
+    (1, 3, 1, 1, 0, 8, 32, 300, True),
+    (2, 4, 1, 1, 1, 16, 32, 64, True),
+    (3, 2, 1, 1, 2, 8, 32, 32, True),
+    (1, 2, 1, 0, 0, 32, 256, 200, True),
+    (1, 1, 1, 0, 0, 24, 64, 4, True),
+]
+
+
+@pytest.mark.parametrize("s,K,d,p,op,cin,cout,L,has_bias", TF32X3_CASES)
+def test_convt1d_tf32x3_cases_meet_fp32_bound(s, K, d, p, op, cin, cout, L, has_bias):
+    x, = rng_inputs(25, (3, cin, L))
+    w, b = rng_inputs(26, (cin, cout, K), (cout,), lo=-0.3, hi=0.3)
+    b = b if has_bias else None
+    y = B.convtranspose1d(dev(x), dev(w), None if b is None else dev(b), s, p, d, op,
+                          precision=B.APS_PREC_TF32X3)
+    assert_close(y.cpu().numpy(), ora.convt(x, w, b, s, p, d, op),
+                 what=f"tf32x3 s{s} K{K} d{d} p{p} op{op} {cin}->{cout} L{L}")
+
+
+def test_convt1d_tf32x3_rejects_weights_too_large_for_shared_memory():
+    # hi + lo weights of 3 x 64 x 128 taps = 196 KB: no pipeline fits beside them
+    x, = rng_inputs(27, (1, 64, 160))
+    w, = rng_inputs(28, (64, 128, 3))
+    with pytest.raises(B.ApsError) as e:
+        B.convtranspose1d(dev(x), dev(w), None, 1, 1, 2, 0, precision=B.APS_PREC_TF32X3)
+    assert e.value.status == B.APS_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("cfg", [3, 4])
+@pytest.mark.slow
+def test_convt1d_tf32x3_full_workload_sampled_planes(cfg):
+    wl = workloads.get(cfg)
+    p = wl.params
+    x, w = wl.generate("x"), wl.generate("w")
+    b = wl.generate("bias") if p["has_bias"] else None
+    y = B.convtranspose1d(dev(x), dev(w), None if b is None else dev(b), p["stride"], p["pad"],
+                          p["dil"], p["out_pad"], precision=B.APS_PREC_TF32X3)
+    torch.cuda.synchronize()
+    N, C = y.shape[0], y.shape[1]
+    sel = [(0, 0), (N - 1, C - 1), (N // 2, 17), (3, C // 2), (N - 1, 0)]
+    ref = ora.convt(x, w, b, p["stride"], p["pad"], p["dil"], p["out_pad"], sel=sel)
+    got = np.stack([y[n, c].cpu().numpy() for n, c in sel])
+    assert_close(got, ref, what=f"tf32x3 cfg {cfg}")
+
+
 @pytest.mark.parametrize("cin,cout,L", [(12, 32, 64), (32, 48, 64), (32, 64, 66), (40, 64, 64),
                                         (64, 256, 64)])
 def test_convt1d_tf32_unsupported_shapes(cin, cout, L):
