@@ -55,7 +55,9 @@ constexpr int MAX_CLASSES = 4;
 constexpr int MAX_TAPS = 8;       // taps per class
 constexpr int NBUF = 4;           // TMA-store staging slabs in flight (at most; 2 if smem is short)
 constexpr int MAX_ACC = 8;        // accumulator buffers in tensor memory (at most)
-constexpr int PREFETCH = 12;      // input boxes prefetched into L2 ahead of the loads
+constexpr int PREFETCH = 4;       // input boxes prefetched into L2 ahead of the loads
+                                  // (swept 0..24 on the box: 4 is fastest; 12 cost 9 %
+                                  // on the strided workload)
 constexpr int THREADS = 576;      // 18 warps
 constexpr int CONVERTERS = 8;     // converter warps: 2, 3, 12..17
 constexpr int EPI_WARPS = 8;      // two epilogue groups of four warps: 4..7 and 8..11

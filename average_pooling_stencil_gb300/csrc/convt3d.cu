@@ -11,13 +11,14 @@
 // per dim an output o = 2m + r takes, for r = 0, input m with tap 1 and, for
 // r = 1, input m+1 with tap 0 and input m with tap 2 (the page's per-parity
 // analysis).  A thread owns one input position (mh, mw) of a plane and the 2x2
-// outputs (2mh + rh, 2mw + rw) around it for all 16 channels; per input
-// channel it reads the 2x2 inputs (mh+b, mw+c) of each input plane the
-// output plane's parity needs (one for an even od, two for an odd one) and
-// applies each to the outputs it reaches: 9 (kh, kw) products per plane for 4
-// outputs, i.e. 1.5 taps per dim per output and no zero taps.  A CTA of 8 warps
-// owns a unit of 16 output rows x 64 output columns of one (n, od) plane:
-// warp w takes input row mh0 + w, lane l input column mw0 + l.  The unit's
+// outputs (2mh + rh, 2mw + rw) around it; per input channel it reads the
+// inputs (mh+b, mw+c) of each input plane the output plane's parity needs
+// (one for an even od, two for an odd one) and applies each to the outputs it
+// reaches: 9 (kh, kw) products per plane for 4 outputs, i.e. 1.5 taps per dim
+// per output and no zero taps.  A CTA of 8 warps owns a unit of 16 output rows
+// x 64 output columns of one (n, od) plane: warp w takes input rows
+// mh0 + 2*(w%4) + {0, 1} and channels 8*(w/4) .. +7 (each broadcast weight
+// read serves two input rows), lane l input column mw0 + l.  The unit's
 // input -- C_in x 2 planes x 9 rows x 36 columns -- is one 4-D TMA box,
 // double-buffered behind mbarriers with bounded waits; units are dealt to a
 // persistent grid round-robin.  Accumulators are channel pairs updated with
@@ -133,19 +134,24 @@ __global__ void __launch_bounds__(c3::THREADS, 2)
             return;
         }
 
-        // ---- 2x2 outputs x 16 channels per thread
-        float2 acc[COUT / 2][2][2];   // [channel pair][rh][rw]
+        // ---- 2 input rows x 2x2 outputs x 8 channels per thread: warp w takes
+        // input rows mh0 + 2*(w % 4) + {0, 1} and channels 8*(w / 4) .. +7, so
+        // each weight read serves two input rows
+        const int rsel = warp & 3, chalf = warp >> 2;
+        float2 acc[4][2][2][2];   // [channel pair][input row r][rh][rw]
 #pragma unroll
-        for (int c2 = 0; c2 < COUT / 2; ++c2) {
-            const float2 bv = make_float2(bsm[2 * c2], bsm[2 * c2 + 1]);
+        for (int c2 = 0; c2 < 4; ++c2) {
+            const float2 bv = make_float2(bsm[8 * chalf + 2 * c2], bsm[8 * chalf + 2 * c2 + 1]);
 #pragma unroll
-            for (int rh = 0; rh < 2; ++rh)
+            for (int r = 0; r < 2; ++r)
 #pragma unroll
-                for (int rw = 0; rw < 2; ++rw) acc[c2][rh][rw] = bv;
+                for (int rh = 0; rh < 2; ++rh)
+#pragma unroll
+                    for (int rw = 0; rw < 2; ++rw) acc[c2][r][rh][rw] = bv;
         }
         const int pd = cur.od & 1;   // even plane: input plane md with tap 1; odd:
                                      // md+1 with tap 0 and md with tap 2
-        const float *xb = xs + b * stage_stride + warp * XC + lane;
+        const float *xb = xs + b * stage_stride + 2 * rsel * XC + lane;
 #pragma unroll 1
         for (int ci = 0; ci < Cin; ++ci) {
 #pragma unroll 1
@@ -153,28 +159,31 @@ __global__ void __launch_bounds__(c3::THREADS, 2)
                 const int a = pd ? (dt == 0 ? 1 : 0) : 0;            // staged plane
                 const int kd = pd ? (dt == 0 ? 0 : 2) : 1;
                 const float *xp = xb + (ci * 2 + a) * XR * XC;
-                const float v00 = xp[0], v01 = xp[1], v10 = xp[XC], v11 = xp[XC + 1];
-                const float4 *wq = reinterpret_cast<const float4 *>(wsm + (ci * 27 + kd * 9) * COUT);
+                float v[3][2];   // input rows 2*rsel + 0..2, columns lane + 0..1
+#pragma unroll
+                for (int rr = 0; rr < 3; ++rr)
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) v[rr][c] = xp[rr * XC + c];
+                const float4 *wq =
+                    reinterpret_cast<const float4 *>(wsm + (ci * 27 + kd * 9) * COUT + 8 * chalf);
                 // (input row b, column c) reaches output (rh, rw) with tap
                 // kh = rh ? (b ? 0 : 2) : 1 (b = 0 only), likewise kw
 #pragma unroll
                 for (int t = 0; t < 9; ++t) {
-                    const int rh = (t / 3) == 1 ? 0 : 1, bb = (t / 3) == 0 ? 1 : 0;
-                    const int rw = (t % 3) == 1 ? 0 : 1, cc = (t % 3) == 0 ? 1 : 0;
                     // t / 3 = kh, t % 3 = kw; kh 1 -> (rh 0, b 0), kh 2 -> (rh 1, b 0),
                     // kh 0 -> (rh 1, b 1); the same for kw
-                    const float v = bb ? (cc ? v11 : v10) : (cc ? v01 : v00);
-                    const float4 w0 = wq[4 * t], w1 = wq[4 * t + 1], w2 = wq[4 * t + 2],
-                                 w3 = wq[4 * t + 3];
-                    const float2 vv = make_float2(v, v);
-                    acc[0][rh][rw] = __ffma2_rn(vv, make_float2(w0.x, w0.y), acc[0][rh][rw]);
-                    acc[1][rh][rw] = __ffma2_rn(vv, make_float2(w0.z, w0.w), acc[1][rh][rw]);
-                    acc[2][rh][rw] = __ffma2_rn(vv, make_float2(w1.x, w1.y), acc[2][rh][rw]);
-                    acc[3][rh][rw] = __ffma2_rn(vv, make_float2(w1.z, w1.w), acc[3][rh][rw]);
-                    acc[4][rh][rw] = __ffma2_rn(vv, make_float2(w2.x, w2.y), acc[4][rh][rw]);
-                    acc[5][rh][rw] = __ffma2_rn(vv, make_float2(w2.z, w2.w), acc[5][rh][rw]);
-                    acc[6][rh][rw] = __ffma2_rn(vv, make_float2(w3.x, w3.y), acc[6][rh][rw]);
-                    acc[7][rh][rw] = __ffma2_rn(vv, make_float2(w3.z, w3.w), acc[7][rh][rw]);
+                    const int rh = (t / 3) == 1 ? 0 : 1, bb = (t / 3) == 0 ? 1 : 0;
+                    const int rw = (t % 3) == 1 ? 0 : 1, cc = (t % 3) == 0 ? 1 : 0;
+                    const float4 w0 = wq[4 * t], w1 = wq[4 * t + 1];
+                    const float2 wp[4] = {make_float2(w0.x, w0.y), make_float2(w0.z, w0.w),
+                                          make_float2(w1.x, w1.y), make_float2(w1.z, w1.w)};
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const float2 vv = make_float2(v[r + bb][cc], v[r + bb][cc]);
+#pragma unroll
+                        for (int c2 = 0; c2 < 4; ++c2)
+                            acc[c2][r][rh][rw] = __ffma2_rn(vv, wp[c2], acc[c2][r][rh][rw]);
+                    }
                 }
             }
         }
@@ -192,21 +201,23 @@ __global__ void __launch_bounds__(c3::THREADS, 2)
         if (tid == 0) bulk_wait_read<0>();
         __syncthreads();
 #pragma unroll
-        for (int rh = 0; rh < 2; ++rh) {
-            const int row = 2 * warp + rh;
-            if (row >= rows) break;
+        for (int r = 0; r < 2; ++r)
 #pragma unroll
-            for (int rw = 0; rw < 2; ++rw) {
-                const int col = 2 * lane + rw;
-                if (col >= cols) continue;
+            for (int rh = 0; rh < 2; ++rh) {
+                const int row = 2 * (2 * rsel + r) + rh;
+                if (row >= rows) continue;
 #pragma unroll
-                for (int c2 = 0; c2 < COUT / 2; ++c2) {
-                    const int c0 = 2 * c2, c1 = 2 * c2 + 1;
-                    ost[c0 * CH + ((a0 + c0 * ac) & 3u) + row * WB + col] = acc[c2][rh][rw].x;
-                    ost[c1 * CH + ((a0 + c1 * ac) & 3u) + row * WB + col] = acc[c2][rh][rw].y;
+                for (int rw = 0; rw < 2; ++rw) {
+                    const int col = 2 * lane + rw;
+                    if (col >= cols) continue;
+#pragma unroll
+                    for (int c2 = 0; c2 < 4; ++c2) {
+                        const int c0 = 8 * chalf + 2 * c2, c1 = c0 + 1;
+                        ost[c0 * CH + ((a0 + c0 * ac) & 3u) + row * WB + col] = acc[c2][r][rh][rw].x;
+                        ost[c1 * CH + ((a0 + c1 * ac) & 3u) + row * WB + col] = acc[c2][r][rh][rw].y;
+                    }
                 }
             }
-        }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncthreads();
         if (runs) {
