@@ -17,8 +17,8 @@
 // reaches: 9 (kh, kw) products per plane for 4 outputs, i.e. 1.5 taps per dim
 // per output and no zero taps.  A CTA of 8 warps owns a unit of 16 output rows
 // x 64 output columns of one (n, od) plane: warp w takes input rows
-// mh0 + 2*(w%4) + {0, 1} and channels 8*(w/4) .. +7 (each broadcast weight
-// read serves two input rows), lane l input column mw0 + l.  The unit's
+// mh0 + 4*(w%2) + 0..3 and channels 4*(w/2) .. +3 (each broadcast weight
+// read serves four input rows), lane l input column mw0 + l.  The unit's
 // input -- C_in x 2 planes x 9 rows x 36 columns -- is one 4-D TMA box,
 // double-buffered behind mbarriers with bounded waits; units are dealt to a
 // persistent grid round-robin.  Accumulators are channel pairs updated with
@@ -48,6 +48,10 @@ constexpr int XC = MW + 4;             // staged input columns (33 used)
 constexpr int OR = 2 * MH;             // output rows per unit
 constexpr int OC = 2 * MW;             // output columns per unit
 constexpr int SLACK = 64;
+constexpr int R = 4;                   // input rows per thread (4: 251 us, 2: 258, 1: 300 on
+                                       // the [128,3,16,32,32] workload)
+constexpr int CPW = COUT / R;          // output channels per thread
+static_assert(MH % R == 0 && CPW % 4 == 0, "rows per warp and channel groups");
 
 __host__ __device__ inline int stage_stride_of(int Cin) {
     return (Cin * 2 * XR * XC + SLACK + 31) & ~31;
@@ -134,16 +138,17 @@ __global__ void __launch_bounds__(c3::THREADS, 2)
             return;
         }
 
-        // ---- 2 input rows x 2x2 outputs x 8 channels per thread: warp w takes
-        // input rows mh0 + 2*(w % 4) + {0, 1} and channels 8*(w / 4) .. +7, so
-        // each weight read serves two input rows
-        const int rsel = warp & 3, chalf = warp >> 2;
-        float2 acc[4][2][2][2];   // [channel pair][input row r][rh][rw]
+        // ---- R input rows x 2x2 outputs x CPW channels per thread: warp w
+        // takes input rows mh0 + R*(w % (MH/R)) + 0..R-1 and channels
+        // CPW*(w / (MH/R)) .. +CPW-1, so each weight read serves R input rows
+        const int rsel = warp % (MH / R), cgrp = warp / (MH / R);
+        float2 acc[CPW / 2][R][2][2];   // [channel pair][input row r][rh][rw]
 #pragma unroll
-        for (int c2 = 0; c2 < 4; ++c2) {
-            const float2 bv = make_float2(bsm[8 * chalf + 2 * c2], bsm[8 * chalf + 2 * c2 + 1]);
+        for (int c2 = 0; c2 < CPW / 2; ++c2) {
+            const float2 bv =
+                make_float2(bsm[CPW * cgrp + 2 * c2], bsm[CPW * cgrp + 2 * c2 + 1]);
 #pragma unroll
-            for (int r = 0; r < 2; ++r)
+            for (int r = 0; r < R; ++r)
 #pragma unroll
                 for (int rh = 0; rh < 2; ++rh)
 #pragma unroll
@@ -151,7 +156,7 @@ __global__ void __launch_bounds__(c3::THREADS, 2)
         }
         const int pd = cur.od & 1;   // even plane: input plane md with tap 1; odd:
                                      // md+1 with tap 0 and md with tap 2
-        const float *xb = xs + b * stage_stride + 2 * rsel * XC + lane;
+        const float *xb = xs + b * stage_stride + R * rsel * XC + lane;
 #pragma unroll 1
         for (int ci = 0; ci < Cin; ++ci) {
 #pragma unroll 1
@@ -159,13 +164,13 @@ __global__ void __launch_bounds__(c3::THREADS, 2)
                 const int a = pd ? (dt == 0 ? 1 : 0) : 0;            // staged plane
                 const int kd = pd ? (dt == 0 ? 0 : 2) : 1;
                 const float *xp = xb + (ci * 2 + a) * XR * XC;
-                float v[3][2];   // input rows 2*rsel + 0..2, columns lane + 0..1
+                float v[R + 1][2];   // input rows R*rsel + 0..R, columns lane + 0..1
 #pragma unroll
-                for (int rr = 0; rr < 3; ++rr)
+                for (int rr = 0; rr <= R; ++rr)
 #pragma unroll
                     for (int c = 0; c < 2; ++c) v[rr][c] = xp[rr * XC + c];
                 const float4 *wq =
-                    reinterpret_cast<const float4 *>(wsm + (ci * 27 + kd * 9) * COUT + 8 * chalf);
+                    reinterpret_cast<const float4 *>(wsm + (ci * 27 + kd * 9) * COUT + CPW * cgrp);
                 // (input row b, column c) reaches output (rh, rw) with tap
                 // kh = rh ? (b ? 0 : 2) : 1 (b = 0 only), likewise kw
 #pragma unroll
@@ -174,14 +179,18 @@ __global__ void __launch_bounds__(c3::THREADS, 2)
                     // kh 0 -> (rh 1, b 1); the same for kw
                     const int rh = (t / 3) == 1 ? 0 : 1, bb = (t / 3) == 0 ? 1 : 0;
                     const int rw = (t % 3) == 1 ? 0 : 1, cc = (t % 3) == 0 ? 1 : 0;
-                    const float4 w0 = wq[4 * t], w1 = wq[4 * t + 1];
-                    const float2 wp[4] = {make_float2(w0.x, w0.y), make_float2(w0.z, w0.w),
-                                          make_float2(w1.x, w1.y), make_float2(w1.z, w1.w)};
+                    float2 wp[CPW / 2];
 #pragma unroll
-                    for (int r = 0; r < 2; ++r) {
+                    for (int q = 0; q < CPW / 4; ++q) {
+                        const float4 w4 = wq[(COUT / 4) * t + q];
+                        wp[2 * q] = make_float2(w4.x, w4.y);
+                        wp[2 * q + 1] = make_float2(w4.z, w4.w);
+                    }
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
                         const float2 vv = make_float2(v[r + bb][cc], v[r + bb][cc]);
 #pragma unroll
-                        for (int c2 = 0; c2 < 4; ++c2)
+                        for (int c2 = 0; c2 < CPW / 2; ++c2)
                             acc[c2][r][rh][rw] = __ffma2_rn(vv, wp[c2], acc[c2][r][rh][rw]);
                     }
                 }
@@ -201,18 +210,18 @@ __global__ void __launch_bounds__(c3::THREADS, 2)
         if (tid == 0) bulk_wait_read<0>();
         __syncthreads();
 #pragma unroll
-        for (int r = 0; r < 2; ++r)
+        for (int r = 0; r < R; ++r)
 #pragma unroll
             for (int rh = 0; rh < 2; ++rh) {
-                const int row = 2 * (2 * rsel + r) + rh;
+                const int row = 2 * (R * rsel + r) + rh;
                 if (row >= rows) continue;
 #pragma unroll
                 for (int rw = 0; rw < 2; ++rw) {
                     const int col = 2 * lane + rw;
                     if (col >= cols) continue;
 #pragma unroll
-                    for (int c2 = 0; c2 < 4; ++c2) {
-                        const int c0 = 8 * chalf + 2 * c2, c1 = c0 + 1;
+                    for (int c2 = 0; c2 < CPW / 2; ++c2) {
+                        const int c0 = CPW * cgrp + 2 * c2, c1 = c0 + 1;
                         ost[c0 * CH + ((a0 + c0 * ac) & 3u) + row * WB + col] = acc[c2][r][rh][rw].x;
                         ost[c1 * CH + ((a0 + c1 * ac) & 3u) + row * WB + col] = acc[c2][r][rh][rw].y;
                     }
