@@ -219,13 +219,17 @@ aps_status aps_avgpool3d_out_shape(const int64_t in[5], const int k[3], const in
     return APS_OK;
 }
 
+// A data pointer may be NULL exactly when its array has no elements (nothing
+// is read from or written to it).
+static bool present(const void *ptr, int64_t elems) { return elems == 0 || ptr != nullptr; }
+
 aps_status aps_avgpool3d(const float *x, const int64_t in[5], const int k[3], const int s[3],
                          const int p[3], int count_include_pad, int ceil_mode, float *y,
                          aps_stream_t stream) {
-    if (!x || !y) return APS_ERR_NULL;
     int64_t out[5];
     aps_status st = aps_avgpool3d_out_shape(in, k, s, p, ceil_mode, out);
     if (st != APS_OK) return st;
+    if (!present(x, numel(in, 5)) || !present(y, numel(out, 5))) return APS_ERR_NULL;
     if (!aligned(x, 4) || !aligned(y, 4)) return APS_ERR_ALIGN;
     if (numel(out, 5) == 0) return APS_OK;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
@@ -267,10 +271,12 @@ aps_status aps_ct3d_scale_pool_bias(const float *x, const int64_t in[5], const f
                                     const int k[3], const int s[3], const int p[3],
                                     const int op[3], const int d[3], int pool_k, float scale1,
                                     float scale2, float *y, aps_stream_t stream) {
-    if (!x || !w || !bias || !y) return APS_ERR_NULL;
     int64_t out[5];
     aps_status st = aps_ct3d_scale_pool_bias_out_shape(in, c_out, k, s, p, op, d, pool_k, out);
     if (st != APS_OK) return st;
+    if (!present(x, numel(in, 5)) || !present(w, in[1]) || !present(y, numel(out, 5)) ||
+        !present(bias, numel(out, 5)))
+        return APS_ERR_NULL;
     if (!aligned(x, 4) || !aligned(w, 4) || !aligned(bias, 4) || !aligned(y, 4) ||
         (conv_bias && !aligned(conv_bias, 4)))
         return APS_ERR_ALIGN;
@@ -310,10 +316,11 @@ aps_status aps_convtranspose3d(const float *x, const int64_t in[5], const float 
                                const float *bias, int64_t c_out, const int k[3],
                                const int s[3], const int p[3], const int d[3], const int op[3],
                                float *y, aps_stream_t stream) {
-    if (!x || !w || !y) return APS_ERR_NULL;
     int64_t out[5];
     aps_status st = aps_convtranspose3d_out_shape(in, c_out, k, s, p, d, op, out);
     if (st != APS_OK) return st;
+    if (!present(x, numel(in, 5)) || !present(w, in[1]) || !present(y, numel(out, 5)))
+        return APS_ERR_NULL;
     if (!aligned(x, 4) || !aligned(w, 4) || !aligned(y, 4) || (bias && !aligned(bias, 4)))
         return APS_ERR_ALIGN;
     if (numel(out, 5) == 0) return APS_OK;
@@ -348,10 +355,11 @@ aps_status aps_convtranspose1d_out_shape(const int64_t in[3], int64_t c_out, int
 aps_status aps_convtranspose1d(const float *x, const int64_t in[3], const float *w,
                                const float *bias, int64_t c_out, int k, int s, int p, int d,
                                int op, int precision, float *y, aps_stream_t stream) {
-    if (!x || !w || !y) return APS_ERR_NULL;
     int64_t out[3];
     aps_status st = aps_convtranspose1d_out_shape(in, c_out, k, s, p, d, op, out);
     if (st != APS_OK) return st;
+    if (!present(x, numel(in, 3)) || !present(w, in[1]) || !present(y, numel(out, 3)))
+        return APS_ERR_NULL;
     if (precision != APS_PREC_FP32 && precision != APS_PREC_TF32 &&
         precision != APS_PREC_TF32X3)
         return APS_ERR_SHAPE;
@@ -359,6 +367,8 @@ aps_status aps_convtranspose1d(const float *x, const int64_t in[3], const float 
         return APS_ERR_ALIGN;
     if (numel(out, 3) == 0) return APS_OK;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    // no input channels: every output is its bias (exact at any precision)
+    if (in[1] == 0) return launch_convt1d_direct(x, in, w, bias, c_out, k, s, p, d, y, out[2], cs);
     if (precision != APS_PREC_FP32)
         return launch_convt1d_tf32(x, in, w, bias, c_out, k, s, p, d, y, out[2],
                                    precision == APS_PREC_TF32X3, cs);

@@ -60,7 +60,9 @@ typedef struct CUstream_st *aps_stream_t;
 
 typedef enum {
     APS_OK = 0,
-    APS_ERR_NULL = -1,        /* a required pointer or shape array is NULL */
+    APS_ERR_NULL = -1,        /* a shape array, or the data pointer of an array
+                                 with elements, is NULL (a pointer to an array of
+                                 zero elements may be NULL: nothing touches it) */
     APS_ERR_SHAPE = -2,       /* a dimension or parameter is out of range, or
                                  the output would be empty in a spatial dim */
     APS_ERR_UNSUPPORTED = -3, /* a valid request no kernel here implements */

@@ -399,3 +399,65 @@ def test_kernel_smem_limit_survives_smaller_launches():
         w, = rng_inputs(33, (cin, cout, 5), lo=-0.3, hi=0.3)
         y = B.convtranspose1d(dev(x), dev(w), None, 1, 0, 3, 0, precision=B.APS_PREC_TF32)
         assert_frobenius(y.cpu().numpy(), ora.convt(x, w, None, 1, 0, 3, 0), what="tf32 order")
+
+
+# ------------------------------------------------------------ degenerate inputs
+def test_empty_batch_every_op():
+    """N = 0: a zero-element output, no launch, no error (the data pointers of
+    empty tensors may be NULL)."""
+    y = B.avgpool3d(torch.empty((0, 3, 8, 8, 8), device="cuda"), 3, 2, 1)
+    assert tuple(y.shape) == (0, 3, 4, 4, 4)
+    w3, cb, b = (dev(a) for a in rng_inputs(41, (3, 16, 3, 3, 3), (16,), (16,)))
+    y = B.ct3d_scale_pool_bias(torch.empty((0, 3, 8, 8, 8), device="cuda"), w3, cb, b)
+    assert tuple(y.shape) == (0, 16, 7, 7, 7)
+    y = B.convtranspose3d(torch.empty((0, 3, 4, 4, 4), device="cuda"), w3, b, 2, 1, 1, 0)
+    assert tuple(y.shape) == (0, 16, 7, 7, 7)
+    w1, b1 = (dev(a) for a in rng_inputs(42, (32, 64, 5), (64,)))
+    for prec in (B.APS_PREC_FP32, B.APS_PREC_TF32, B.APS_PREC_TF32X3):
+        y = B.convtranspose1d(torch.empty((0, 32, 100), device="cuda"), w1, b1, 1, 0, 3, 0,
+                              precision=prec)
+        assert tuple(y.shape) == (0, 64, 112)
+
+
+def test_zero_input_channels_give_the_bias():
+    """C_in = 0: every output is the (folded) bias, at every precision."""
+    b1, = rng_inputs(43, (8,))
+    x1, w1 = np.zeros((2, 0, 9), np.float32), np.zeros((0, 8, 3), np.float32)
+    want = ora.convt(x1, w1, b1, 2, 1, 1, 0)
+    for prec in (B.APS_PREC_FP32, B.APS_PREC_TF32, B.APS_PREC_TF32X3):
+        y = B.convtranspose1d(torch.empty((2, 0, 9), device="cuda"),
+                              torch.empty((0, 8, 3), device="cuda"), dev(b1), 2, 1, 1, 0,
+                              precision=prec)
+        assert_close(y.cpu().numpy(), want, what=f"convt1d C_in 0 prec {prec}")
+    b3, cb = rng_inputs(44, (16,), (16,))
+    x3, w3 = np.zeros((1, 0, 3, 4, 4), np.float32), np.zeros((0, 16, 3, 3, 3), np.float32)
+    y = B.convtranspose3d(torch.empty((1, 0, 3, 4, 4), device="cuda"),
+                          torch.empty((0, 16, 3, 3, 3), device="cuda"), dev(b3), 2, 1, 1, 0)
+    assert_close(y.cpu().numpy(), ora.convt(x3, w3, b3, 2, 1, 1, 0), what="convt3d C_in 0")
+    y = B.ct3d_scale_pool_bias(torch.empty((1, 0, 3, 4, 4), device="cuda"),
+                               torch.empty((0, 16, 3, 3, 3), device="cuda"), dev(cb), dev(b3),
+                               scale1=0.5, scale2=2.0)
+    assert_close(y.cpu().numpy(), ora.ct3d_scale_pool_bias(x3, w3, cb, b3, 2, 1, 0, 1, 2, 0.5,
+                                                           2.0), what="fused C_in 0")
+
+
+def test_launches_on_a_side_stream_are_ordered_on_it():
+    wl = workloads.get(3).with_input_shape((2, 32, 700))
+    p = wl.params
+    x, w = wl.generate("x"), wl.generate("w")
+    s = torch.cuda.Stream()
+    xd, wd = dev(x), dev(w)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        y = B.convtranspose1d(xd, wd, None, p["stride"], p["pad"], p["dil"], p["out_pad"],
+                              precision=B.APS_PREC_TF32X3, stream=s)
+    s.synchronize()
+    assert_close(y.cpu().numpy(), ora.convt(x, w, None, p["stride"], p["pad"], p["dil"],
+                                            p["out_pad"]), what="side stream")
+
+
+def test_no_kernel_recorded_a_timeout():
+    """Every bounded wait in every launch so far completed in time."""
+    torch.cuda.synchronize()
+    st, bits = B.aps_device_status(clear=False)
+    assert st == B.APS_OK and bits == 0, (st, bits)
