@@ -1,5 +1,6 @@
 // convt1d_tc.cu -- ConvTranspose1d as a TF32 implicit GEMM on the tcgen05
-// tensor cores (APS_PREC_TF32).
+// tensor cores (APS_PREC_TF32), and its 3xTF32 form at fp32 accuracy
+// (APS_PREC_TF32X3: the SPLIT instantiation, described at the end).
 //
 // Operation (Kimi-K2.6__l1_p74, its gather formula): y[n,co,o] = bias[co] +
 // sum_ci sum_k w[ci,co,k] * x[n,ci,(o + p - d*k)/s], where a term exists only
@@ -11,11 +12,12 @@
 // an im2col buffer and without inserting zeros).
 //
 // Kernel structure (one persistent CTA per SM, warp-specialised):
-//  * warp 0, lane 0  -- TMA producer: for each (n, 128-position tile, 32-channel
-//    chunk) one 3-D box x[n, ci0:ci0+32, a0:a0+BW] (BW = 128 + tap span, start
-//    rounded down to 16 bytes; out-of-range cells arrive as zeros) into a
-//    ring of up to 4 stages, and an L2 prefetch of the box 12 steps ahead (one
-//    CTA per SM holds few stages; the prefetch keeps enough bytes in flight).
+//  * warp 0, lane 0  -- TMA producer: for each (n, 128-position tile, chunk
+//    of 32 (or, split, 16) channels) one 3-D box x[n, ci0:ci0+CKr, a0:a0+BW]
+//    (BW = 128 + tap span, start rounded down to 16 bytes; out-of-range cells
+//    arrive as zeros) into a ring of up to 4 stages, and an L2 prefetch of the
+//    box 4 steps ahead (one CTA per SM holds few stages; the prefetch keeps
+//    bytes in flight; 4 measured fastest of 0..24).
 //    Warp 0 also owns the tensor-memory allocation.
 //  * warps 2, 3, 12..17 -- converters (one per 4 channels): transpose each raw
 //    box into the K-major,
@@ -25,7 +27,7 @@
 //    tap k is the same buffer with its start moved by 16 bytes per row of tap
 //    offset: one transposed copy serves every tap of every class.
 //  * warp 1, lane 0  -- MMA issuer: walks a per-CTA table of descriptors and,
-//    per chunk and (class, tap), issues CK/8 tcgen05.mma
+//    per chunk and (class, tap), issues CKr/8 tcgen05.mma
 //    kind::tf32 of 128 x C_out x 8 into the class's accumulator in tensor memory
 //    (a ring of up to 8 tiles' accumulators, as many as 512 columns hold, so the
 //    epilogue's latency never stalls the MMAs), then tcgen05.commit to release the
@@ -40,6 +42,11 @@
 // K-major layout, one [C_in/4][C_out][4] block per tap.  Every wait is bounded;
 // a wait that times out records APS_DEVERR_TIMEOUT, the CTA drains what it has
 // in flight and frees its tensor memory before returning.
+// 3xTF32 (SPLIT): weights and every converted stage are held twice, hi =
+// tf32(v) and lo = tf32(v - hi); each table entry issues lo(x)hi(w),
+// hi(x)lo(w), hi(x)hi(w) into the same accumulator (the dropped lo*lo term is
+// ~2^-22 of each product).  The launcher picks the deepest pipeline that fits
+// 227 KB: 32- then 16-channel chunks, 3 then 2 converted stages.
 #include <algorithm>
 
 #include "aps_dev.cuh"

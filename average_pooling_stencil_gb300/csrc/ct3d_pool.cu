@@ -17,20 +17,25 @@
 // chain in exact arithmetic; in fp32 it differs by rounding only (the page
 // argues the reassociation is far inside an fp32 tolerance).
 //
-// Design (GB300): one CTA of 4 warps per unit = (batch row, output plane,
-// block of 16 output rows, block of 32 output columns).  The unit's input --
-// C_in channels x 2 planes x 17 rows x (32 or 36) columns -- arrives by one
-// 4-D TMA box (zero-filled outside the tensor), or by 4-byte cp.async when the
-// rows are not 16-byte strided.  While it is in flight the CTA collapses the
-// weights itself (C_in*16*27 loads) into shared memory, so the op is one
-// kernel with no scratch buffer and no host access to the weights.  Lane l
-// owns output column l and warp w output rows 4w..4w+3 of the block, all 16
-// channels: per input channel a thread reads its 2 x 5 x 2 input window once
-// (32 consecutive words per warp load: no bank conflicts) and applies each of
-// the 8 taps to its 4 rows with broadcast float4 weight reads.  Accumulators
-// are channel pairs updated with the packed fp32x2 FMA (two exactly rounded
-// fp32 FMAs per instruction).  Each store instruction of a warp writes one
-// output row segment of 32 consecutive floats.
+// Design (GB300): a persistent grid of 8-warp CTAs (2 per SM).  Each CTA
+// collapses the weights once (C_in*16*27 loads) into shared memory, so the op
+// is one kernel with no scratch buffer and no host access to the weights.  A
+// unit is up to 32 output rows x 32 output columns of one (n, od) plane; units
+// are dealt to the CTAs round-robin, so at any time the grid works on a narrow
+// window of the output.  A unit's input -- C_in channels x 2 planes x 33 rows
+// x (32 or 36) columns -- arrives by one 4-D TMA box (zero-filled outside the
+// tensor), double-buffered behind mbarriers with bounded waits, or by 4-byte
+// cp.async when the rows are not 16-byte strided.  Lane l owns output column
+// l and warp w output rows 4w..4w+3 of the unit, all 16 channels: per input
+// channel a thread reads its 2 x 5 x 2 input window once (32 consecutive
+// words per warp load: no bank conflicts) and applies each of the 8 taps to
+// its 4 rows with broadcast float4 weight reads.  Accumulators are channel
+// pairs updated with the packed fp32x2 FMA (two exactly rounded fp32 FMAs per
+// instruction).  Outputs are staged per channel in shared memory at their
+// destination's float offset mod 4; when the unit spans whole output rows a
+// channel's outputs are one contiguous run of y, whose 16-byte-aligned middle
+// leaves by one cp.async.bulk copy (head and tail floats by plain stores), so
+// the stores overlap the next unit's math.
 //
 // General path: one thread per pooled output evaluates the literal chain with
 // the gather form of the transposed convolution, tap k taken where
