@@ -39,6 +39,7 @@ EXPORTS = [
     "aps_ct3d_scale_pool_bias_out_shape", "aps_ct3d_scale_pool_bias",
     "aps_convtranspose3d_out_shape", "aps_convtranspose3d",
     "aps_convtranspose1d_out_shape", "aps_convtranspose1d", "aps_device_status",
+    "aps_fp32_fma_probe",
 ]
 
 _lib = None
@@ -81,6 +82,7 @@ def lib():
         L.aps_convtranspose1d.argtypes = [_VP, _VP, _VP, _VP, ctypes.c_int64] + \
             [ctypes.c_int] * 6 + [_VP, _VP]
         L.aps_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), ctypes.c_int]
+        L.aps_fp32_fma_probe.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _VP, _VP]
         for name in EXPORTS:
             if name != "aps_status_string" and name != "aps_abi_version":
                 getattr(L, name).restype = ctypes.c_int
@@ -171,6 +173,14 @@ def aps_device_status(clear: bool = False):
 
 
 # --------------------------------------------------------- torch-level calls
+APS_PROBE_THREADS = 256
+
+
+def aps_fp32_fma_probe(packed, blocks, iters, sink_ptr, stream=0) -> int:
+    return lib().aps_fp32_fma_probe(int(bool(packed)), int(blocks), int(iters), _VP(sink_ptr),
+                                    _VP(stream))
+
+
 def _stream(stream):
     import torch
     if stream is None:

@@ -323,6 +323,29 @@ def time_graph(torch, case, per_graph=100, reps=20):
     return e0.elapsed_time(e1) / 1e3 / (reps * per_graph)
 
 
+def measure_fma_ceilings(torch, aps, sms, iters=4096, reps=5):
+    """FP32 FMA rate this GPU sustains (TFLOP/s), scalar and packed fp32x2,
+    from the library's register-only probe at 64 warps per SM."""
+    B = aps.binding
+    sink = torch.zeros(1, device="cuda")
+    st = torch.cuda.current_stream()
+    blocks = sms * 8
+    out = {}
+    for packed in (0, 1):
+        for _ in range(2):
+            assert B.aps_fp32_fma_probe(packed, blocks, iters, sink.data_ptr(), st.cuda_stream) == 0
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(reps):
+            B.aps_fp32_fma_probe(packed, blocks, iters, sink.data_ptr(), st.cuda_stream)
+        e1.record(st)
+        e1.synchronize()
+        t = e0.elapsed_time(e1) / 1e3
+        flops = 64.0 * iters * blocks * B.APS_PROBE_THREADS * reps
+        out["packed" if packed else "scalar"] = flops / t / 1e12
+    return out
+
+
 def roofline_for(case, t, peaks, src, clock_mhz):
     hbm = float(peaks["hbm_gbs"])
     gbs = case.bytes / t / 1e9
@@ -332,10 +355,18 @@ def roofline_for(case, t, peaks, src, clock_mhz):
         return {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                 "peak_source": src}
     if case.bound == "alu":
-        return {"bound": "alu", "achieved": tfl, "peak": fp32, "unit": "TFLOP/s",
-                "frac": tfl / fp32,
-                "peak_source": "152 SMs x 128 FP32 lanes x 2 FLOP x max SM clock "
-                               f"{peaks.get('sm_max_mhz', 2070.0)} MHz"}
+        r = {"bound": "alu", "achieved": tfl, "peak": fp32, "unit": "TFLOP/s",
+             "frac": tfl / fp32,
+             "peak_source": "152 SMs x 128 FP32 lanes x 2 FLOP x max SM clock "
+                            f"{peaks.get('sm_max_mhz', 2070.0)} MHz"}
+        fma = peaks.get("fma_measured")
+        if fma:
+            r["measured_ceiling"] = fma["packed"]
+            r["frac_of_measured_ceiling"] = tfl / fma["packed"]
+            r["measured_ceiling_source"] = (
+                "packed fp32x2 FMA probe (aps_fp32_fma_probe, 64 warps/SM) timed in this run; "
+                f"scalar FMA {fma['scalar']:.1f} TFLOP/s")
+        return r
     floor = max(case.bytes / (hbm * 1e9), case.flops / (fp32 * 1e12))
     return {"bound": "hbm" if case.bytes / (hbm * 1e9) >= case.flops / (fp32 * 1e12) else "alu",
             "achieved": gbs, "unit": "GB/s", "peak": hbm, "frac": floor / t,
@@ -410,6 +441,10 @@ def whole_job_rate(world_size, units_per_rank_step, steps, t_max):
     return world_size * units_per_rank_step * steps / t_max
 
 
+def sm_count_of(torch):
+    return torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -466,6 +501,9 @@ def run_native(args):
         torch.cuda.set_device(0)
     aps_build.build()
     peaks, peak_src = load_peaks()
+    # measured FP32 FMA ceilings (outside every timed region), for the FMA-bound lines
+    peaks = dict(peaks)
+    peaks["fma_measured"] = measure_fma_ceilings(torch, aps, sm_count_of(torch))
     dev_index = local if ws > 1 else 0
 
     def barrier():
@@ -539,10 +577,11 @@ def run_native(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": workload_desc(case.wl), "seed": case.wl.seed,
-                   "l2": ("inputs larger than L2 (8.59 GB input per step), no flush"
+                   "l2": (f"data larger than L2 ({case.bytes / 1e9:.2f} GB moved per step), no flush"
                           if case.bytes > 2 * 129e6 else "input may stay in L2 (small case)"),
                    "parallelism": f"replicas{ws}" if ws > 1 else "single GPU"},
         "roofline": roof, "e2e": e2e, "gpu_launches": args.steps, "clocks": clocks,
+        "fma_ceilings_tflops": peaks["fma_measured"],
     }
     xhost = case.host["x"].numpy() if args.workload == HEADLINE_CFG and x_shape is None else None
     del case

@@ -204,6 +204,18 @@ aps_status aps_convtranspose1d(const float *x, const int64_t in_ncl[3], const fl
  */
 aps_status aps_device_status(unsigned int *bits, int clear);
 
+/* FP32 FMA-rate probe (not part of any op): launches `blocks` CTAs of
+ * APS_PROBE_THREADS threads, each thread running `iters` rounds of 32
+ * independent fp32 multiply-adds on registers -- scalar FMA, or (packed != 0)
+ * the packed fp32x2 FMA in 16 pairs.  FLOPs per launch =
+ * 64 * iters * blocks * APS_PROBE_THREADS.  The caller times the launch on
+ * `stream`; sink (one device float) is written only under a condition that
+ * never holds.  Returns APS_ERR_NULL without sink, APS_ERR_SHAPE for
+ * blocks < 1 or iters < 1.  Asynchronous, allocates nothing. */
+#define APS_PROBE_THREADS 256
+aps_status aps_fp32_fma_probe(int packed, int blocks, int iters, float *sink,
+                              aps_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -461,3 +461,13 @@ def test_no_kernel_recorded_a_timeout():
     torch.cuda.synchronize()
     st, bits = B.aps_device_status(clear=False)
     assert st == B.APS_OK and bits == 0, (st, bits)
+
+
+def test_fp32_fma_probe_reports_a_sane_rate():
+    """The FMA-rate probe behind the roofline of the FMA-bound kernels: its
+    packed form beats its scalar form and both lie below the unit-count peak
+    (152 SMs x 128 lanes x 2 FLOP x 2.07 GHz = 80.5 TFLOP/s)."""
+    import bench
+    r = bench.measure_fma_ceilings(torch, __import__("average_pooling_stencil_gb300"),
+                                   bench.sm_count_of(torch), iters=1024, reps=3)
+    assert 10.0 < r["scalar"] < r["packed"] < 82.0, r
