@@ -346,14 +346,46 @@ def measure_fma_ceilings(torch, aps, sms, iters=4096, reps=5):
     return out
 
 
+def measure_tf32_ceiling(torch, n=8192, reps=5):
+    """Dense TF32 tensor-core rate (TFLOP/s) of the vendor GEMM (cuBLAS through
+    torch.matmul with TF32 allowed) on n x n x n: a ceiling for the tensor work
+    of the TF32 paths, measured only, never on an op's path."""
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    try:
+        a = torch.randn(n, n, device="cuda")
+        b = torch.randn(n, n, device="cuda")
+        for _ in range(2):
+            c = a @ b
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            c = a @ b
+        e1.record()
+        e1.synchronize()
+        del a, b, c
+        return 2.0 * n ** 3 * reps / (e0.elapsed_time(e1) / 1e3) / 1e12
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+
+
 def roofline_for(case, t, peaks, src, clock_mhz):
     hbm = float(peaks["hbm_gbs"])
     gbs = case.bytes / t / 1e9
     tfl = case.flops / t / 1e12
     fp32 = fp32_peak_tflops(float(peaks.get("sm_max_mhz", 2070.0)))
     if case.bound == "hbm":
-        return {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
-                "peak_source": src}
+        r = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+             "peak_source": src}
+        tc = peaks.get("tf32_measured")
+        if getattr(case, "precision", 0) and tc:
+            # tensor work: one MMA product per FLOP pair, three for 3xTF32
+            work = case.flops * (3 if case.precision == 2 else 1) / t / 1e12
+            r["tensor_tflops"] = work
+            r["tensor_ceiling"] = tc
+            r["tensor_frac_of_ceiling"] = work / tc
+            r["tensor_ceiling_source"] = "cuBLAS TF32 GEMM 8192^3 timed in this run"
+        return r
     if case.bound == "alu":
         r = {"bound": "alu", "achieved": tfl, "peak": fp32, "unit": "TFLOP/s",
              "frac": tfl / fp32,
@@ -504,6 +536,7 @@ def run_native(args):
     # measured FP32 FMA ceilings (outside every timed region), for the FMA-bound lines
     peaks = dict(peaks)
     peaks["fma_measured"] = measure_fma_ceilings(torch, aps, sm_count_of(torch))
+    peaks["tf32_measured"] = measure_tf32_ceiling(torch)
     dev_index = local if ws > 1 else 0
 
     def barrier():
@@ -582,6 +615,7 @@ def run_native(args):
                    "parallelism": f"replicas{ws}" if ws > 1 else "single GPU"},
         "roofline": roof, "e2e": e2e, "gpu_launches": args.steps, "clocks": clocks,
         "fma_ceilings_tflops": peaks["fma_measured"],
+        "tf32_gemm_ceiling_tflops": peaks["tf32_measured"],
     }
     xhost = case.host["x"].numpy() if args.workload == HEADLINE_CFG and x_shape is None else None
     del case
