@@ -46,7 +46,9 @@
 // tf32(v) and lo = tf32(v - hi); each table entry issues lo(x)hi(w),
 // hi(x)lo(w), hi(x)hi(w) into the same accumulator (the dropped lo*lo term is
 // ~2^-22 of each product).  The launcher picks the deepest pipeline that fits
-// 227 KB: 32- then 16-channel chunks, 3 then 2 converted stages.
+// 227 KB: 32- then 16-channel chunks, 3 then 2 converted stages.  Only two
+// converter warps convert in this form, each taking every second 4-channel
+// block (its hi + lo stores from eight warps at once slowed the MMAs by 4 %).
 #include <algorithm>
 
 #include "aps_dev.cuh"
@@ -538,8 +540,12 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
         if (tma_store && gtid == 0) bulk_wait<0>();
     } else {
         // ------------------------------------------------------ converters
-        // converter warp cb owns channels 4cb..4cb+3 of every chunk
+        // converter warp cb owns channels 4cbx..4cbx+3 of every chunk, cbx = cb,
+        // cb + ACTIVE, ...  The split form writes twice the bytes per channel, and
+        // its shared-memory stores then slow the tensor core's operand reads: two
+        // busy converters (the rest only arrive) leave the MMA more of the port.
         const int cb = converter_id(warp);
+        constexpr int ACTIVE = split ? 2 : tc1::CONVERTERS;
         uint32_t it = 0;
         uint32_t xs_i = 0, xs_ph = 0;   // converted stage and its phase parity
         for (long long u = blockIdx.x; u < n_units && !abort_flag; u += gridDim.x) {
@@ -553,13 +559,13 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
                     fail = true;
                     break;
                 }
-                if (cb < CKr / 4) {
+                for (int cbx = cb; cb < ACTIVE && cbx < CKr / 4; cbx += ACTIVE) {
                     const float *s0 = reinterpret_cast<const float *>(raw + rs * RAW_STRIDE) +
-                                      (size_t)(4 * cb) * BW;
+                                      (size_t)(4 * cbx) * BW;
                     // lane -> positions lane, lane+32, ...: the four channel reads
                     // and the 16-byte row writes of a warp are each contiguous, so
                     // neither has bank conflicts
-                    uint4 *d0 = reinterpret_cast<uint4 *>(xt + xs * XT_STRIDE + cb * LBO_X);
+                    uint4 *d0 = reinterpret_cast<uint4 *>(xt + xs * XT_STRIDE + cbx * LBO_X);
                     if constexpr (split) {
                         uint4 *d1 = reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(d0) + XT_LO);
                         for (int pos = lane; pos < BW; pos += 32) {
