@@ -55,6 +55,13 @@ aps_status launch_ct3d_pool2_fast(const float *x, const int64_t in[5], const flo
                                   float scale2, float *y, const int64_t out[5],
                                   cudaStream_t st);
 
+// The same fused op on the tensor cores (3xTF32: fp32 accuracy), for
+// C_in <= 3 and input rows of a multiple of 16 bytes; APS_ERR_UNSUPPORTED
+// otherwise (the caller then uses launch_ct3d_pool2_fast).
+aps_status launch_ct3d_pool2_tc(const float *x, const int64_t in[5], const float *w,
+                                const float *conv_bias, const float *bias, float scale1,
+                                float scale2, float *y, const int64_t out[5], cudaStream_t st);
+
 aps_status launch_ct3d_pool_direct(const float *x, const int64_t in[5], const float *w,
                                    const float *conv_bias, const float *bias, int64_t c_out,
                                    const int k[3], const int s[3], const int p[3],

@@ -1,0 +1,372 @@
+// ct3d_pool_tc.cu -- the fused ConvTranspose3d(k3, s2, p1) -> x scale1 ->
+// AvgPool3d(2) -> + bias -> x scale2 of Kimi-K2.6__l2_p50 on the tensor cores.
+//
+// The chain collapses (the page's per-parity grouping of the 27 taps; see
+// ct3d_pool.cu) to a 2x2x2 valid correlation with collapsed weights:
+//     y[n,co,d,h,w] = beff[co] + sum_{ci,a,b,c} x[n,ci,d+a,h+b,w+c] * Weff[ci,co,a,b,c].
+// Per output position that is a dot product of length K = 8*C_in for each of
+// the 16 output channels: a (positions x K) x (K x 16) matrix product whose
+// A row is the position's 2x2x2 x C_in input neighbourhood.  On the FP32 pipe
+// it costs 24 FMAs per output plus the loads and moves around them, and the
+// instruction issue, not HBM, bounds it.  Here the tensor core does the
+// product and the SM only gathers A and stores y.
+//
+// Precision (3xTF32): every operand v is split as hi = v with the low 13 bits
+// of its fp32 pattern cleared (exactly a tf32) and lo = v - hi (exact in fp32;
+// the tensor core reads its leading tf32 bits), and each product is
+// accumulated as lo(x)hi(w) + hi(x)lo(w) + hi(x)hi(w) in fp32.  The terms
+// left out are below 2^-21 of each product.
+//
+// Design (GB300): one persistent CTA per SM holding all 512 tensor-memory
+// columns, 16 warps in 4 groups of 4.  A unit is up to 32 output rows x 32
+// output columns of one (n, od) plane; units are dealt round-robin.  Thread 0
+// keeps a 4-stage ring of units in flight, one 4-D TMA box each (C_in
+// channels x 2 input planes x 33 rows x 32/36 columns, zero-filled outside
+// the tensor) behind full/empty mbarriers, and writes each unit's coordinates
+// into its stage's slot.  An M-tile is 4 output rows x 32 columns = 128
+// positions; group g takes tiles g and g+4 of each unit, warp q of the group
+// row q of a tile (tensor-memory lanes 32q..32q+31, the lanes a warp may
+// address), lane l column l.  Per tile each thread reads its 8*C_in inputs
+// from shared memory (32 consecutive words per warp load), splits them and
+// writes its hi and lo A row into its lane with tcgen05.st.  After both tiles
+// one group barrier hands them to the group's MMA thread, which issues the
+// 2 x 3*C_in MMAs (M 128, N 16, K 8, A from tensor memory, B = the collapsed
+// weights in shared memory) and one commit.  The warps then release the stage,
+// wait for the commit, load both accumulator rows (two tcgen05.ld in flight,
+// one wait), add the folded bias and write each channel's row with one
+// whole-warp store.  Every wait is bounded; the group barrier also carries
+// each warp's "go on" vote, so that a group whose wait ran out leaves
+// together, drains what it issued and frees the tensor memory.
+#include <algorithm>
+#include <cstring>
+
+#include "aps_dev.cuh"
+#include "aps_internal.h"
+#include "aps_tc.cuh"
+
+namespace aps {
+namespace ctc {
+constexpr int COUT = 16;
+constexpr int CIN_MAX = 3;                 // K = 8*C_in <= 24: A hi + lo fit 48 columns
+constexpr int GROUPS = 4;
+constexpr int WARPS = 4 * GROUPS;
+constexpr int THREADS = 32 * WARPS;        // 512
+constexpr int TILE_ROWS = 4;               // 4 rows x 32 columns = MMA M 128
+constexpr int UNIT_ROWS = 32;
+constexpr int UNIT_COLS = 32;
+constexpr int TILES_PER_GROUP = UNIT_ROWS / TILE_ROWS / GROUPS;   // 2
+constexpr int STAGES = 4;                  // input ring: units in flight ahead of the math
+constexpr int TMEM_COLS = 512;
+constexpr int GROUP_COLS = TMEM_COLS / GROUPS;                    // 128: two tile buffers
+constexpr int BUF_COLS = GROUP_COLS / TILES_PER_GROUP;            // 64: A hi, A lo, D
+constexpr int D_COL = 48;                                         // accumulator, 16 columns
+constexpr int SLACK = 64;                  // floats after a stage: lanes past the last column read on
+// Fixed head of the dynamic shared memory (bytes); the stages follow.
+constexpr int OFF_FULL = 0;                // uint64 [STAGES]
+constexpr int OFF_EMPTY = 32;              // uint64 [STAGES]
+constexpr int OFF_DFULL = 64;              // uint64 [GROUPS]: the group's MMAs of a unit are done
+constexpr int OFF_TMEM = 96;               // uint32: tensor-memory base
+constexpr int OFF_ABORT = 100;             // int
+constexpr int OFF_SLOT = 128;              // UnitSlot [STAGES]
+constexpr int OFF_BIAS = 256;              // float [16]
+constexpr int OFF_B = 384;                 // B operand, hi then lo: [C_in][2][16][4] words each
+constexpr int B_CI_BYTES = 2 * COUT * 16;  // one input channel's K-step of 8: 512 bytes
+constexpr int HEAD_BYTES = OFF_B + 2 * CIN_MAX * B_CI_BYTES;      // 3456, a multiple of 128
+static_assert(HEAD_BYTES % 128 == 0, "stages start 128-byte aligned");
+static_assert(D_COL + COUT <= BUF_COLS && 16 * CIN_MAX <= D_COL, "tile buffer layout");
+
+struct UnitSlot {
+    long long n;
+    int od, oh0, ow0, rows, cols, pad;
+};
+static_assert(sizeof(UnitSlot) * STAGES <= OFF_BIAS - OFF_SLOT, "slots fit");
+
+// Floats one stage occupies: the staged window plus the rows the last tile
+// may still read (up to row UNIT_ROWS), plus slack.
+__host__ __device__ inline int stage_stride_of(int Cin, int XR, int BW) {
+    return (Cin * 2 * XR * BW + (UNIT_ROWS + 1 - XR) * BW + SLACK + 31) & ~31;
+}
+}  // namespace ctc
+
+// CIN: input channels (1..3); BW_T: staged row length fixed at compile time
+// (0: run time).
+template <int CIN, int BW_T>
+__global__ void __launch_bounds__(ctc::THREADS, 1)
+    ct3d_pool2_tc_kernel(const __grid_constant__ CUtensorMap xmap, const float *__restrict__ w,
+                         const float *__restrict__ conv_bias, const float *__restrict__ bias,
+                         float scale1, float scale2, float *__restrict__ y, int D, int H, int W,
+                         int BW_rt, int XR, int RB, int WB, int n_ohb, int n_owb,
+                         long long n_units, unsigned int *status) {
+    using namespace ctc;
+    const int BW = BW_T ? BW_T : BW_rt;
+    const int Do = D - 1, Ho = H - 1, Wo = W - 1;
+    extern __shared__ __align__(128) unsigned char smraw[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smraw + OFF_FULL);
+    uint64_t *empty = reinterpret_cast<uint64_t *>(smraw + OFF_EMPTY);
+    uint64_t *dfull = reinterpret_cast<uint64_t *>(smraw + OFF_DFULL);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smraw + OFF_TMEM);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smraw + OFF_ABORT);
+    UnitSlot *slot = reinterpret_cast<UnitSlot *>(smraw + OFF_SLOT);
+    float *bsm = reinterpret_cast<float *>(smraw + OFF_BIAS);
+    uint32_t *bop = reinterpret_cast<uint32_t *>(smraw + OFF_B);
+    float *xs = reinterpret_cast<float *>(smraw + HEAD_BYTES);   // [STAGES][C_in][2][XR][BW]
+    const int stage_floats = CIN * 2 * XR * BW;
+    const int stage_stride = stage_stride_of(CIN, XR, BW);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int grp = warp >> 2, q = warp & 3;
+
+    // decode unit u into the slot of stage b and load its input window
+    auto fill = [&](long long u, int b) {
+        const int owb = (int)(u % n_owb);
+        long long t = u / n_owb;
+        const int ohb = (int)(t % n_ohb);
+        t /= n_ohb;
+        const int od = (int)(t % Do);
+        const long long n = t / Do;
+        const int oh0 = ohb * RB, ow0 = owb * WB;
+        UnitSlot &g = slot[b];
+        g.n = n;
+        g.od = od;
+        g.oh0 = oh0;
+        g.ow0 = ow0;
+        g.rows = Ho - oh0 < RB ? Ho - oh0 : RB;
+        g.cols = Wo - ow0 < WB ? Wo - ow0 : WB;
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive_expect_tx(&full[b], (uint32_t)stage_floats * 4u);
+        tma_load_4d(xs + b * stage_stride, &xmap, &full[b], ow0, oh0, od, (int)(n * CIN));
+    };
+
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], WARPS);
+        }
+        for (int g = 0; g < GROUPS; ++g) mbar_init(&dfull[g], 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 0) tc::tmem_alloc(tmem_slot, TMEM_COLS);
+    __syncthreads();
+    uint32_t issued = 0;   // units thread 0 has filled
+    if (tid == 0) {
+        tma_prefetch_desc(&xmap);
+        for (; issued < STAGES - 1 && (long long)blockIdx.x + (long long)issued * gridDim.x < n_units;
+             ++issued)
+            fill(blockIdx.x + (long long)issued * gridDim.x, (int)issued);
+    }
+
+    // ---- B = collapsed weights, split hi / lo, K-major: word (ci, kc, co, e)
+    // holds Weff[ci][co][tap 4*kc+e] (tap = a*4 + b*2 + c), so that input
+    // channel ci is one K-step of 8 and its core matrices (8 co x 4 taps) lie
+    // 128 bytes apart along N and 256 bytes apart along K
+    const float wscale = scale1 * scale2 * 0.125f;
+    for (int i = tid; i < CIN * 8 * COUT; i += THREADS) {
+        const int co = i % COUT, t = (i / COUT) % 8, ci = i / (8 * COUT);
+        const int a = t >> 2, b = (t >> 1) & 1, c = t & 1;
+        const float *wp = w + (size_t)(ci * COUT + co) * 27;
+        float acc = 0.f;
+        for (int kd = a ? 0 : 1; kd <= (a ? 0 : 2); ++kd)
+            for (int kh = b ? 0 : 1; kh <= (b ? 0 : 2); ++kh)
+                for (int kw = c ? 0 : 1; kw <= (c ? 0 : 2); ++kw)
+                    acc += __ldg(wp + kd * 9 + kh * 3 + kw);
+        const float v = acc * wscale;
+        const uint32_t hi = __float_as_uint(v) & 0xFFFFE000u;
+        const int word = ((ci * 2 + (t >> 2)) * COUT + co) * 4 + (t & 3);
+        bop[word] = hi;
+        bop[CIN * 8 * COUT + word] = __float_as_uint(v - __uint_as_float(hi));
+    }
+    if (tid < COUT) {
+        const float cb = conv_bias ? __ldg(conv_bias + tid) : 0.f;
+        bsm[tid] = fmaf(cb, scale1, __ldg(bias + tid)) * scale2;
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // B is read by the tensor core
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const long long plane = (long long)Ho * Wo;
+    const int cs = (int)(Do * plane);                    // between output channels (< 2^27)
+    constexpr uint32_t IDESC = tc::idesc_tf32(128, COUT);
+    const uint32_t b_hi = smem_u32(bop), b_lo = b_hi + CIN * B_CI_BYTES;
+    const uint32_t lane_q = (uint32_t)(32 * q) << 16;   // this warp's tensor-memory lanes
+    const uint32_t gcol = (uint32_t)(grp * GROUP_COLS); // the group's two tile buffers
+    const int gbar = 1 + grp;                            // the group's barrier (0 is __syncthreads)
+    float bias_r[COUT];
+#pragma unroll
+    for (int co = 0; co < COUT; ++co) bias_r[co] = bsm[co];
+    uint32_t k = 0;                                      // units this CTA has taken
+    bool fail = false;
+    for (long long u = blockIdx.x; u < n_units; u += gridDim.x, ++k) {
+        const int b = (int)(k % STAGES);
+        // thread 0 keeps STAGES-1 units in flight ahead of this one: unit
+        // k+STAGES-1 goes into the stage that held unit k-1, once every warp is
+        // done with it
+        const long long ahead = u + (long long)(STAGES - 1) * gridDim.x;
+        if (tid == 0 && !*abort_flag && ahead < n_units) {
+            const int nb = (int)((k + STAGES - 1) % STAGES);
+            if (k >= 1 && !mbar_wait(&empty[nb], ((k - 1) / STAGES) & 1u)) {
+                record_error(status, APS_DEVERR_TIMEOUT);
+                *abort_flag = 1;
+            } else {
+                fill(ahead, nb);
+                ++issued;
+            }
+        }
+        bool ok = !fail && !*abort_flag;
+        if (ok && !mbar_wait(&full[b], (k / STAGES) & 1u)) {
+            record_error(status, APS_DEVERR_TIMEOUT);
+            *abort_flag = 1;
+            ok = false;
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        const int grows = ok ? slot[b].rows : 0;
+
+        // ---- A rows of the group's two tiles into tensor memory
+        if (ok) {
+            const float *xb = xs + b * stage_stride;
+#pragma unroll 1
+            for (int j = 0; j < TILES_PER_GROUP; ++j) {
+                const int tile = grp + GROUPS * j;   // rows 4*tile .. 4*tile+3 of the unit
+                if (TILE_ROWS * tile >= grows) continue;   // uniform over the group
+                const int h = TILE_ROWS * tile + q;
+                uint32_t av[16 * CIN];   // hi[0 .. 8*CIN), then lo
+#pragma unroll
+                for (int ci = 0; ci < CIN; ++ci)
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        const int a = t >> 2, bb = (t >> 1) & 1, c = t & 1;
+                        const float v = xb[((ci * 2 + a) * XR + h + bb) * BW + lane + c];
+                        const uint32_t hi = __float_as_uint(v) & 0xFFFFE000u;
+                        av[ci * 8 + t] = hi;
+                        av[8 * CIN + ci * 8 + t] = __float_as_uint(v - __uint_as_float(hi));
+                    }
+                const uint32_t col = gcol + (uint32_t)(j * BUF_COLS);
+#pragma unroll
+                for (int s = 0; s < CIN; ++s) tc::tmem_st16(tmem + lane_q + col + 16 * s, av + 16 * s);
+            }
+            tc::tmem_st_wait();
+        }
+        tc::tc_fence_before();
+        __syncwarp();
+        // hand both tiles to the group's MMA thread; the group decides together
+        // whether to go on, so that no warp is left at a group barrier
+        if (tc::named_bar_or(gbar, 128, !ok)) break;
+        if (q == 0 && lane == 0) {
+            tc::tc_fence_after();
+#pragma unroll 1
+            for (int j = 0; j < TILES_PER_GROUP; ++j) {
+                if (TILE_ROWS * (grp + GROUPS * j) >= grows) continue;
+                const uint32_t col = gcol + (uint32_t)(j * BUF_COLS);
+                const uint32_t d = tmem + col + D_COL;
+#pragma unroll
+                for (int ci = 0; ci < CIN; ++ci) {
+                    const uint32_t ahi = tmem + col + 8 * ci, alo = ahi + 8 * CIN;
+                    const uint64_t bh = tc::umma_desc(b_hi + ci * B_CI_BYTES, 256, 128);
+                    const uint64_t bl = tc::umma_desc(b_lo + ci * B_CI_BYTES, 256, 128);
+                    tc::umma_tf32_ts(d, alo, bh, IDESC, ci > 0 ? 1u : 0u);   // lo(x) hi(w)
+                    tc::umma_tf32_ts(d, ahi, bl, IDESC, 1u);                 // hi(x) lo(w)
+                    tc::umma_tf32_ts(d, ahi, bh, IDESC, 1u);                 // hi(x) hi(w)
+                }
+            }
+            tc::umma_commit(&dfull[grp]);   // once per unit, tiles or not
+        }
+        __syncwarp();
+
+        // where the outputs go, read before the stage and its slot are released
+        const long long gn = slot[b].n;
+        const int god = slot[b].od, goh0 = slot[b].oh0, gow0 = slot[b].ow0, gcols = slot[b].cols;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[b]);
+
+        // ---- epilogue: both accumulator rows -> + bias -> whole-warp row stores
+        if (!mbar_wait(&dfull[grp], k & 1u)) {
+            record_error(status, APS_DEVERR_TIMEOUT);
+            *abort_flag = 1;
+            fail = true;
+        }
+        fail = __any_sync(0xffffffffu, fail);
+        if (fail) continue;   // the next unit's decision ends the loop
+        tc::tc_fence_after();
+        uint32_t d0[COUT], d1[COUT];
+        tc::tmem_ld16_async(tmem + lane_q + gcol + D_COL, d0);
+        tc::tmem_ld16_async(tmem + lane_q + gcol + BUF_COLS + D_COL, d1);
+        tc::tmem_ld_wait(d0, d1);
+        if (lane < gcols) {
+            float *yb = y + ((gn * COUT) * Do + god) * plane + (long long)goh0 * Wo + gow0 + lane;
+            const int h0 = TILE_ROWS * grp + q, h1 = h0 + TILE_ROWS * GROUPS;
+            if (h0 < grows) {
+                float *yr = yb + h0 * Wo;
+#pragma unroll
+                for (int co = 0; co < COUT; ++co) yr[co * cs] = __uint_as_float(d0[co]) + bias_r[co];
+            }
+            if (h1 < grows) {
+                float *yr = yb + h1 * Wo;
+#pragma unroll
+                for (int co = 0; co < COUT; ++co) yr[co * cs] = __uint_as_float(d1[co]) + bias_r[co];
+            }
+        }
+    }
+
+    // ---- leave nothing in flight: the group's last MMAs (their wait may
+    // have run out), the fills no warp consumed; then free the tensor memory
+    if (q == 0 && lane == 0 && k > 0) mbar_wait(&dfull[grp], (k - 1) & 1u);
+    if (tid == 0)
+        for (uint32_t j = k; j < issued; ++j) mbar_wait(&full[j % STAGES], (j / STAGES) & 1u);
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+aps_status launch_ct3d_pool2_tc(const float *x, const int64_t in[5], const float *w,
+                                const float *conv_bias, const float *bias, float scale1,
+                                float scale2, float *y, const int64_t out[5], cudaStream_t st) {
+    using namespace ctc;
+    const int64_t N = in[0], Cin = in[1], D = in[2], H = in[3], W = in[4];
+    // the TMA box needs 16-byte rows; C_in > 3 does not fit the tile buffers
+    if (Cin < 1 || Cin > CIN_MAX || D < 2 || H < 2 || W < 2 || W % 4 != 0 ||
+        reinterpret_cast<uintptr_t>(x) % 16 != 0 || D >= (1 << 30) || H >= (1 << 30) ||
+        W >= (1 << 30) || N * Cin >= (1ll << 31))
+        return APS_ERR_UNSUPPORTED;
+    const int64_t Do = out[2], Ho = out[3], Wo = out[4];
+    if (Do * Ho * Wo >= (1ll << 27)) return APS_ERR_UNSUPPORTED;   // channel offsets in 32 bits
+    const int RB = (int)std::min<int64_t>(Ho, UNIT_ROWS), WB = (int)std::min<int64_t>(Wo, UNIT_COLS);
+    const int64_t n_ohb = ceil_div(Ho, RB), n_owb = ceil_div(Wo, WB);
+    const long long n_units = N * Do * n_ohb * n_owb;
+    const int XR = RB + 1;                  // staged rows
+    const int BW = (WB + 1 + 3) & ~3;       // staged columns, a multiple of 4
+    CUtensorMap map;
+    const cuuint64_t dims[4] = {(cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)D, (cuuint64_t)(N * Cin)};
+    const cuuint64_t strides[3] = {(cuuint64_t)(W * 4), (cuuint64_t)(H * W * 4),
+                                   (cuuint64_t)(D * H * W * 4)};
+    const cuuint32_t box[4] = {(cuuint32_t)BW, (cuuint32_t)XR, 2, (cuuint32_t)Cin};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    if (!encode_tiled(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(x), dims,
+                      strides, box, estr))
+        return APS_ERR_UNSUPPORTED;
+    const size_t smem = (size_t)HEAD_BYTES + (size_t)STAGES * stage_stride_of((int)Cin, XR, BW) * 4;
+    using Kern = void (*)(CUtensorMap, const float *, const float *, const float *, float, float,
+                          float *, int, int, int, int, int, int, int, int, int, long long,
+                          unsigned int *);
+    Kern kern;
+    if (BW == 32)
+        kern = Cin == 1 ? ct3d_pool2_tc_kernel<1, 32>
+             : Cin == 2 ? ct3d_pool2_tc_kernel<2, 32>
+                        : ct3d_pool2_tc_kernel<3, 32>;
+    else
+        kern = Cin == 1 ? ct3d_pool2_tc_kernel<1, 0>
+             : Cin == 2 ? ct3d_pool2_tc_kernel<2, 0>
+                        : ct3d_pool2_tc_kernel<3, 0>;
+    // one CTA per SM: each holds all 512 tensor-memory columns
+    if (resident_ctas((const void *)kern, THREADS, (int)smem) < 1) return APS_ERR_UNSUPPORTED;
+    const long long grid = std::min<long long>(sm_count(), n_units);
+    kern<<<(unsigned)grid, THREADS, smem, st>>>(map, w, conv_bias, bias, scale1, scale2, y,
+                                                 (int)D, (int)H, (int)W, BW, XR, RB, WB,
+                                                 (int)n_ohb, (int)n_owb, n_units, status_word());
+    return launch_status();
+}
+
+}  // namespace aps

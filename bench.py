@@ -216,7 +216,11 @@ class GpuCase:
                 x.shape, p["c_out"], p["k"], p["stride"], p["pad"], p["out_pad"], p["dil"],
                 p["pool_k"])
             self.flops = 2 * 8 * x.shape[1] * numel(oshape)   # 8 collapsed taps per ci
-            self.bound = "hbm+alu"
+            # C_in <= 3 with 16-byte input rows runs on the tensor cores (3xTF32,
+            # three MMA passes), bound by HBM; otherwise on the FP32 pipe
+            self.tc = x.shape[1] <= 3 and x.shape[4] % 4 == 0
+            self.tensor_passes = 3 if self.tc else 0
+            self.bound = "hbm" if self.tc else "hbm+alu"
         elif wl.op == "convtranspose3d":
             st, oshape = aps.binding.aps_convtranspose3d_out_shape(
                 x.shape, p["c_out"], p["k"], p["stride"], p["pad"], p["dil"], p["out_pad"])
@@ -233,6 +237,7 @@ class GpuCase:
             self.flops = 2 * x.shape[0] * x.shape[1] * p["c_out"] * pairs
             # fp32 FMA path is bound by the FP32 pipe; the tf32 tensor path by HBM
             self.bound = "alu" if precision == 0 else "hbm"
+            self.tensor_passes = {0: 0, 1: 1, 2: 3}[precision]
         assert st == 0
         self.oshape = oshape
         self.y = torch.empty(oshape, device=dev, dtype=torch.float32)
@@ -378,9 +383,10 @@ def roofline_for(case, t, peaks, src, clock_mhz):
         r = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
              "peak_source": src}
         tc = peaks.get("tf32_measured")
-        if getattr(case, "precision", 0) and tc:
+        passes = getattr(case, "tensor_passes", 0)
+        if passes and tc:
             # tensor work: one MMA product per FLOP pair, three for 3xTF32
-            work = case.flops * (3 if case.precision == 2 else 1) / t / 1e12
+            work = case.flops * passes / t / 1e12
             r["tensor_tflops"] = work
             r["tensor_ceiling"] = tc
             r["tensor_frac_of_ceiling"] = work / tc
@@ -591,7 +597,9 @@ def run_native(args):
     clocks = sampler.summary(t_wall0, t_wall1)
     roof = roofline_for(case, per_launch, peaks, peak_src, clocks.get("sm_mhz"))
     kernel_of = {"avgpool3d": ("avgpool3d.cu", "avgpool3d_k3s2p1_tma_kernel"),
-                 "ct3d_scale_pool_bias": ("ct3d_pool.cu", "ct3d_pool2_fast_kernel"),
+                 "ct3d_scale_pool_bias": (("ct3d_pool_tc.cu", "ct3d_pool2_tc_kernel")
+                                          if getattr(case, "tc", False)
+                                          else ("ct3d_pool.cu", "ct3d_pool2_fast_kernel")),
                  "convtranspose3d": ("convt3d.cu", "convt3d_k3s2p1_kernel"),
                  "convtranspose1d": (("convt1d_tc.cu", "convt1d_tf32_kernel") if case.precision
                                      else ("convt1d.cu", "convt1d_tiled_kernel"))}[case.wl.op]

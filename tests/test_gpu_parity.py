@@ -136,9 +136,13 @@ def test_fused_workloads_all_outputs(cfg):
                  what=f"fused cfg {cfg}")
 
 
+# C_in <= 3 with W % 4 == 0 runs on the tensor cores (C_in 1, 2, 3; staged rows of 32
+# columns or a run-time width; Ho = 32 exactly; several row and column blocks); the rest on
+# the FP32 pipe (C_in 4..8, rows that are not 16-byte strided)
 @pytest.mark.parametrize("shape", [(1, 3, 5, 7, 9), (2, 1, 2, 2, 2), (3, 8, 4, 6, 33),
                                    (1, 2, 3, 40, 40), (2, 3, 4, 8, 32), (1, 5, 2, 3, 1030),
-                                   (1, 3, 3, 70, 20)])
+                                   (1, 3, 3, 70, 20), (2, 1, 3, 9, 12), (1, 2, 5, 33, 8),
+                                   (1, 1, 2, 2, 4), (3, 3, 2, 17, 68)])
 def test_fused_fast_path_shapes(shape):
     base = workloads.get(0)
     wl = workloads.Workload(base.name, base.op, 5, dict(base.tensors), dict(base.params))
@@ -147,6 +151,21 @@ def test_fused_fast_path_shapes(shape):
     x, w, cb, b = (wl.generate(n) for n in ("x", "w", "conv_bias", "bias"))
     assert_close(fused_gpu(x, w, cb, b, wl.params), fused_ref(wl, x, w, cb, b),
                  what=f"fused {shape}")
+
+
+def test_fused_unaligned_input_takes_the_fp32_kernel():
+    """An input that is not 16-byte aligned cannot be a TMA source: the op then runs the
+    FP32-pipe kernel with element copies, on the same shape the tensor cores take."""
+    base = workloads.get(0)
+    x, = rng_inputs(41, (2, 3, 4, 8, 32))
+    w, cb, b = (base.generate(n) for n in ("w", "conv_bias", "bias"))
+    store = torch.empty(x.size + 1, device="cuda", dtype=torch.float32)
+    xd = store[1:].view(x.shape)
+    xd.copy_(dev(x))
+    assert xd.data_ptr() % 16 != 0
+    y = B.ct3d_scale_pool_bias(xd, dev(w), dev(cb), dev(b), scale1=base.params["scale1"],
+                               scale2=base.params["scale2"])
+    assert_close(y.cpu().numpy(), fused_ref(base, x, w, cb, b), what="fused unaligned x")
 
 
 def test_fused_without_conv_bias_and_other_scales():
