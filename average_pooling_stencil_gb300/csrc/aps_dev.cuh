@@ -152,6 +152,30 @@ __device__ __forceinline__ void bulk_wait() {
     asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// ---------------------------------- k3 s2 p1 + pool 2: the collapsed taps
+// Collapsed tap g = a*4 + b*2 + c of the weights wp[kd*9 + kh*3 + kw] of one
+// (ci, co): the sum over kd in T(a), kh in T(b), kw in T(c), where input
+// offset 0 takes taps {1, 2} and offset 1 tap {0} (the page's grouping of the
+// 27 terms), in ascending (kd, kh, kw).  The loads are unrolled and
+// predicated, so that they are all in flight at once.
+__device__ __forceinline__ float collapse_tap_ldg(const float *__restrict__ wp, int g) {
+    const int a = g >> 2, b = (g >> 1) & 1, c = g & 1;
+    float v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        // e-th term of a 2x2x2 enumeration; terms outside the tap sets are 0
+        const int od = e >> 2, oh = (e >> 1) & 1, ow = e & 1;
+        const int kd = a ? 0 : 1 + od, kh = b ? 0 : 1 + oh, kw = c ? 0 : 1 + ow;
+        const bool in = !(a && od) && !(b && oh) && !(c && ow);
+        v[e] = in ? __ldg(wp + kd * 9 + kh * 3 + kw) : 0.f;
+    }
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        if (!(a && (e >> 2)) && !(b && ((e >> 1) & 1)) && !(c && (e & 1))) acc += v[e];
+    return acc;
+}
+
 // ------------------------------------------------------------- cp.async
 __device__ __forceinline__ void cp_async_4(void *dst, const void *src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
@@ -167,12 +191,6 @@ __device__ __forceinline__ void cp_async_commit() {
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-// one arrival on `bar` once every cp.async this thread issued so far has
-// landed; .noinc: the arrival counts against the barrier's expected count
-__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
 }
 
 }  // namespace aps

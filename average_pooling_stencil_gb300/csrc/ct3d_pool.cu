@@ -157,15 +157,10 @@ __global__ void __launch_bounds__(ct3::THREADS, BW_T ? 2 : 1)
     // ---- collapsed weights [ci][a*4+b*2+c][co] and folded bias, once per CTA
     const float wscale = scale1 * scale2 * 0.125f;
     for (int i = tid; i < Cin * 8 * COUT; i += THREADS) {
+        // one collapsed tap of one (ci, co): its (up to 8) weights by
+        // independent loads, summed in ascending (kd, kh, kw)
         const int co = i % COUT, g = (i / COUT) % 8, ci = i / (8 * COUT);
-        const int a = g >> 2, b = (g >> 1) & 1, c = g & 1;
-        const float *wp = w + (size_t)(ci * COUT + co) * 27;
-        float acc = 0.f;
-        for (int kd = a ? 0 : 1; kd <= (a ? 0 : 2); ++kd)
-            for (int kh = b ? 0 : 1; kh <= (b ? 0 : 2); ++kh)
-                for (int kw = c ? 0 : 1; kw <= (c ? 0 : 2); ++kw)
-                    acc += __ldg(wp + kd * 9 + kh * 3 + kw);
-        wsm[i] = acc * wscale;
+        wsm[i] = collapse_tap_ldg(w + (size_t)(ci * COUT + co) * 27, g) * wscale;
     }
     if (tid < COUT) {
         const float cb = conv_bias ? __ldg(conv_bias + tid) : 0.f;

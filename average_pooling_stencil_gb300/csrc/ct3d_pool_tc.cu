@@ -161,15 +161,10 @@ __global__ void __launch_bounds__(ctc::THREADS, 1)
     // 128 bytes apart along N and 256 bytes apart along K
     const float wscale = scale1 * scale2 * 0.125f;
     for (int i = tid; i < CIN * 8 * COUT; i += THREADS) {
+        // one collapsed tap of one (ci, co): its (up to 8) weights by
+        // independent loads, summed in ascending (kd, kh, kw)
         const int co = i % COUT, t = (i / COUT) % 8, ci = i / (8 * COUT);
-        const int a = t >> 2, b = (t >> 1) & 1, c = t & 1;
-        const float *wp = w + (size_t)(ci * COUT + co) * 27;
-        float acc = 0.f;
-        for (int kd = a ? 0 : 1; kd <= (a ? 0 : 2); ++kd)
-            for (int kh = b ? 0 : 1; kh <= (b ? 0 : 2); ++kh)
-                for (int kw = c ? 0 : 1; kw <= (c ? 0 : 2); ++kw)
-                    acc += __ldg(wp + kd * 9 + kh * 3 + kw);
-        const float v = acc * wscale;
+        const float v = collapse_tap_ldg(w + (size_t)(ci * COUT + co) * 27, t) * wscale;
         const uint32_t hi = __float_as_uint(v) & 0xFFFFE000u;
         const int word = ((ci * 2 + (t >> 2)) * COUT + co) * 4 + (t & 3);
         bop[word] = hi;
