@@ -125,7 +125,11 @@ aps_status aps_avgpool3d(const float *x, const int64_t in_ncdhw[5], const int k[
  * 1 <= C_in <= 8: the pooled output then equals a 2x2x2 valid correlation of x
  * with 8 collapsed weights per (ci, co) plus a folded bias (the page's
  * grouping of the 27 taps by input neighbour), computed in one kernel whose
- * CTAs collapse the weights themselves.  Every other valid geometry runs a
+ * CTAs collapse the weights themselves.  With C_in <= 3, W % 4 == 0 and x
+ * 16-byte aligned that kernel runs the correlation on the tensor cores as
+ * 3xTF32 (each operand split v = hi + lo, each product summed as lo*hi + hi*lo
+ * + hi*hi in fp32); otherwise on the FP32 pipe.  Both meet
+ * max |y - exact| <= 1e-5 * (1 + |exact|).  Every other valid geometry runs a
  * direct per-output kernel.
  */
 aps_status aps_ct3d_scale_pool_bias_out_shape(const int64_t in_ncdhw[5], int64_t c_out,
