@@ -17,6 +17,10 @@
 // chain in exact arithmetic; in fp32 it differs by rounding only (the page
 // argues the reassociation is far inside an fp32 tolerance).
 //
+// Which kernel runs: C_in <= 3 with 16-byte input rows takes the tensor-core
+// kernel (ct3d_pool_tc.cu); this FP32-pipe kernel serves the rest of the fast
+// path (C_in 4..8, inputs a TMA box cannot read).
+//
 // Design (GB300): a persistent grid of 8-warp CTAs (2 per SM).  Each CTA
 // collapses the weights once (C_in*16*27 loads) into shared memory, so the op
 // is one kernel with no scratch buffer and no host access to the weights.  A
