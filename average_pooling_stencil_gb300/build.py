@@ -17,7 +17,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libaps.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 SOURCES = ["aps_api.cu", "avgpool3d.cu", "ct3d_pool.cu", "ct3d_pool_tc.cu", "convt3d.cu",
-           "convt1d.cu", "convt1d_tc.cu", "fma_probe.cu"]
+           "convt3d_tc.cu", "convt1d.cu", "convt1d_tc.cu", "fma_probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-I", INCLUDE]

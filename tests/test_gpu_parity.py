@@ -198,6 +198,11 @@ CONVT3D_CASES = [  # (x shape, C_out, k, s, p, d, op, bias)
     ((2, 8, 3, 17, 8), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (1, 1, 1), False),
     ((1, 1, 6, 6, 4), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (0, 1, 0), True),
     ((1, 3, 2, 2, 68), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (1, 0, 1), True),
+    # C_in <= 3, W <= 32: the tensor-core kernel (output padding in every dim, H not a
+    # multiple of 4, a single input plane, no bias)
+    ((3, 2, 3, 9, 16), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (1, 1, 1), True),
+    ((1, 3, 1, 7, 32), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (0, 0, 0), False),
+    ((2, 1, 4, 4, 28), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (1, 0, 1), True),
     # W % 4 != 0 (no TMA) and other geometries: the direct kernel
     ((2, 3, 4, 5, 10), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (0, 0, 0), True),
     ((1, 2, 3, 4, 5), 5, (2, 3, 4), (1, 2, 3), (0, 1, 2), (2, 1, 1), (1, 1, 2), True),
@@ -214,6 +219,21 @@ def test_convt3d_cases(xs, cout, k, s, p, d, op, has_bias):
     y = B.convtranspose3d(dev(x), dev(w), None if b is None else dev(b), s, p, d, op)
     assert_close(y.cpu().numpy(), ora.convt(x, w, b, s, p, d, op),
                  what=f"convt3d {xs} k{k} s{s} p{p} d{d} op{op}")
+
+
+def test_convt3d_unaligned_input_takes_the_direct_kernel():
+    """An input that is not 16-byte aligned cannot be a TMA source: the op then runs
+    the direct kernel, on a shape the tensor cores take when aligned."""
+    xs = (2, 3, 3, 8, 16)
+    x, = rng_inputs(43, xs)
+    w, b = rng_inputs(44, (3, 16, 3, 3, 3), (16,), lo=-0.3, hi=0.3)
+    store = torch.empty(x.size + 1, device="cuda", dtype=torch.float32)
+    xd = store[1:].view(x.shape)
+    xd.copy_(dev(x))
+    assert xd.data_ptr() % 16 != 0
+    y = B.convtranspose3d(xd, dev(w), dev(b), (2, 2, 2), (1, 1, 1), (1, 1, 1), (0, 0, 0))
+    assert_close(y.cpu().numpy(), ora.convt(x, w, b, (2, 2, 2), (1, 1, 1), (1, 1, 1), (0, 0, 0)),
+                 what="convt3d unaligned x")
 
 
 def test_convt3d_full_workload_sampled_planes():
