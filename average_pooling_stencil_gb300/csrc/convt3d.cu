@@ -7,6 +7,10 @@
 // per spatial dim, a term existing only where o + p - d*k is a non-negative
 // multiple of s whose quotient is inside the input.
 //
+// Which kernel runs: C_in <= 3 with W <= 32 and 16-byte input rows takes the
+// tensor-core kernel (convt3d_tc.cu); this FP32-pipe kernel serves the rest of
+// the fast path (C_in 4..8, W > 32).
+//
 // Fast kernel (k3, s2, p1, d1, output_padding 0 or 1, C_out = 16, C_in <= 8):
 // per dim an output o = 2m + r takes, for r = 0, input m with tap 1 and, for
 // r = 1, input m+1 with tap 0 and input m with tap 2 (the page's per-parity
