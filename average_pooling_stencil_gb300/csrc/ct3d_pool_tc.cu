@@ -29,9 +29,9 @@
 // address), lane l column l.  Per tile each thread reads its 8*C_in inputs
 // from shared memory (32 consecutive words per warp load), splits them and
 // writes its hi and lo A row into its lane with tcgen05.st.  After both tiles
-// one group barrier hands them to the group's MMA thread, which issues the
-// 2 x 3*C_in MMAs (M 128, N 16, K 8, A from tensor memory, B = the collapsed
-// weights in shared memory) and one commit.  The warps then release the stage,
+// one group barrier hands them to two MMA threads (lane 0 of the group's
+// first two warps), each issuing one tile's 3*C_in MMAs (M 128, N 16, K 8, A
+// from tensor memory, B = the collapsed weights in shared memory) and a commit.  The warps then release the stage,
 // wait for the commit, load both accumulator rows (two tcgen05.ld in flight,
 // one wait), add the folded bias and write each channel's row with one
 // whole-warp store.  Every wait is bounded; the group barrier also carries
@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(ctc::THREADS, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], WARPS);
         }
-        for (int g = 0; g < GROUPS; ++g) mbar_init(&dfull[g], 1);
+        for (int g = 0; g < GROUPS; ++g) mbar_init(&dfull[g], TILES_PER_GROUP);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -247,11 +247,13 @@ __global__ void __launch_bounds__(ctc::THREADS, 1)
         // hand both tiles to the group's MMA thread; the group decides together
         // whether to go on, so that no warp is left at a group barrier
         if (tc::named_bar_or(gbar, 128, !ok)) break;
-        if (q == 0 && lane == 0) {
+        // tile j's MMA chain is issued by lane 0 of the group's warp j, so that
+        // the two chains go out in parallel; each commits to the group's
+        // barrier (two arrivals a unit, tiles or not)
+        if (q < TILES_PER_GROUP && lane == 0) {
+            const int j = q;
             tc::tc_fence_after();
-#pragma unroll 1
-            for (int j = 0; j < TILES_PER_GROUP; ++j) {
-                if (TILE_ROWS * (grp + GROUPS * j) >= grows) continue;
+            if (TILE_ROWS * (grp + GROUPS * j) < grows) {
                 const uint32_t col = gcol + (uint32_t)(j * BUF_COLS);
                 const uint32_t d = tmem + col + D_COL;
 #pragma unroll
@@ -264,7 +266,7 @@ __global__ void __launch_bounds__(ctc::THREADS, 1)
                     tc::umma_tf32_ts(d, ahi, bh, IDESC, 1u);                 // hi(x) hi(w)
                 }
             }
-            tc::umma_commit(&dfull[grp]);   // once per unit, tiles or not
+            tc::umma_commit(&dfull[grp]);
         }
         __syncwarp();
 
