@@ -616,8 +616,9 @@ aps_status launch_convt1d_tf32(const float *x, const int64_t in[3], const float 
     // split (3xTF32): hi and lo copies of the weights and of each converted stage
     const size_t w_bytes = (size_t)k * Cin * c_out * 4 * (split ? 2 : 1);
     // the output leaves by TMA store when a tile's outputs form a <= 256-wide box
-    // and the output rows are 16-byte strided
-    const int tma_store = (s <= 2 && l_out % 4 == 0) ? 1 : 0;
+    // and y and its rows are 16-byte aligned; otherwise by the direct stores
+    const int tma_store =
+        (s <= 2 && l_out % 4 == 0 && reinterpret_cast<uintptr_t>(y) % 16 == 0) ? 1 : 0;
     // 227 KB per CTA, less the 1 KB of static shared memory the kernel declares
     const size_t budget = 227 * 1024 - 1024;
     // Deepest pipeline that fits, trying in order: chunks of 32 channels then

@@ -510,3 +510,83 @@ def test_fp32_fma_probe_reports_a_sane_rate():
     r = bench.measure_fma_ceilings(torch, __import__("average_pooling_stencil_gb300"),
                                    bench.sm_count_of(torch), iters=1024, reps=3)
     assert 10.0 < r["scalar"] < r["packed"] < 82.0, r
+
+
+# ------------------------------------------------------------ guard canaries
+# Every op writes into a view in the middle of a larger buffer whose other words hold a
+# sentinel no kernel writes (a NaN bit pattern): the words around the view must survive, at a
+# 256-byte-aligned start and at a start one float off (which sends the paths that need an
+# aligned output to their fallbacks and gives the bulk-copy runs every head/tail split).
+GUARD = 64
+SENTINEL = 0x7FA5A5A5
+
+
+def _canary_cases():
+    base0, base3, base4, base5 = (workloads.get(i) for i in (0, 3, 4, 5))
+    cases = {}
+
+    def pool(shape, k, s, p):
+        x, = rng_inputs(51, shape)
+        want = ora.avgpool3d(x, k, s, p, 1, 0)
+        return want, lambda out: B.avgpool3d(dev(x), k, s, p, out=out), 1e-5
+    cases["avgpool_tma"] = lambda: pool((2, 3, 9, 20, 68), (3, 3, 3), (2, 2, 2), (1, 1, 1))
+    cases["avgpool_direct"] = lambda: pool((1, 2, 5, 7, 9), (2, 3, 2), (1, 2, 2), (1, 1, 0))
+
+    def fused(shape, k=(3, 3, 3), s=(2, 2, 2), p=(1, 1, 1)):
+        x, = rng_inputs(52, shape)
+        w, cb, b = rng_inputs(53, (shape[1], 16) + k, (16,), (16,), lo=-0.3, hi=0.3)
+        want = ora.ct3d_scale_pool_bias(x, w, cb, b, s, p, (0, 0, 0), (1, 1, 1), 2, 0.5, 1.25)
+        return want, lambda out: B.ct3d_scale_pool_bias(
+            dev(x), dev(w), dev(cb), dev(b), s, p, 0, 1, 2, 0.5, 1.25, out=out), 1e-5
+    cases["fused_tc"] = lambda: fused((2, 3, 4, 8, 32))
+    cases["fused_fp32"] = lambda: fused((1, 5, 3, 6, 20))
+    cases["fused_direct"] = lambda: fused((1, 2, 3, 5, 6), k=(2, 2, 2), s=(2, 2, 2), p=(0, 0, 0))
+
+    def convt1d(wl, shape, prec, tol):
+        x, = rng_inputs(54, shape)
+        w, = rng_inputs(55, (shape[1], 64, wl.params["k"]), lo=-0.1, hi=0.1)
+        b, = rng_inputs(56, (64,))
+        p = wl.params
+        want = ora.convt(x, w, b, p["stride"], p["pad"], p["dil"], p["out_pad"])
+        return want, lambda out: B.convtranspose1d(
+            dev(x), dev(w), dev(b), p["stride"], p["pad"], p["dil"], p["out_pad"],
+            precision=prec, out=out), tol
+    cases["convt1d_fp32"] = lambda: convt1d(base4, (2, 64, 300), B.APS_PREC_FP32, 1e-5)
+    cases["convt1d_tf32"] = lambda: convt1d(base3, (2, 32, 400), B.APS_PREC_TF32, None)
+    cases["convt1d_tf32x3"] = lambda: convt1d(base3, (2, 32, 400), B.APS_PREC_TF32X3, 1e-5)
+
+    def convt3d(shape, k=(3, 3, 3), s=(2, 2, 2), p=(1, 1, 1), op=(0, 0, 0)):
+        x, = rng_inputs(57, shape)
+        w, b = rng_inputs(58, (shape[1], 16) + k, (16,), lo=-0.3, hi=0.3)
+        want = ora.convt(x, w, b, s, p, (1, 1, 1), op)
+        return want, lambda out: B.convtranspose3d(dev(x), dev(w), dev(b), s, p, (1, 1, 1), op,
+                                                   out=out), 1e-5
+    cases["convt3d_tc"] = lambda: convt3d((2, 3, 5, 9, 12), op=(1, 0, 1))
+    cases["convt3d_fp32"] = lambda: convt3d((1, 8, 3, 7, 36))
+    cases["convt3d_direct"] = lambda: convt3d((1, 2, 3, 4, 5), k=(2, 3, 2), s=(1, 2, 3),
+                                              p=(0, 1, 1))
+    del base0, base5
+    return cases
+
+
+CANARY = _canary_cases()
+
+
+@pytest.mark.parametrize("offset", [GUARD, GUARD + 1])
+@pytest.mark.parametrize("name", sorted(CANARY))
+def test_outputs_stay_inside_their_buffer(name, offset):
+    want, run, tol = CANARY[name]()
+    n = want.size
+    buf = torch.empty(n + 2 * GUARD, device="cuda", dtype=torch.float32)
+    buf.view(torch.int32).fill_(SENTINEL)
+    out = buf[offset:offset + n].view(want.shape)
+    run(out)
+    torch.cuda.synchronize()
+    raw = buf.view(torch.int32).cpu().numpy()
+    outside = np.concatenate([raw[:offset], raw[offset + n:]])
+    assert (outside == SENTINEL).all(), f"{name}: {int((outside != SENTINEL).sum())} guard words written"
+    got = out.cpu().numpy()
+    if tol is None:
+        assert_frobenius(got, want, what=name)
+    else:
+        assert_close(got, want, tol=tol, what=name)
