@@ -39,7 +39,7 @@ EXPORTS = [
     "aps_ct3d_scale_pool_bias_out_shape", "aps_ct3d_scale_pool_bias",
     "aps_convtranspose3d_out_shape", "aps_convtranspose3d",
     "aps_convtranspose1d_out_shape", "aps_convtranspose1d", "aps_device_status",
-    "aps_fp32_fma_probe",
+    "aps_fp32_fma_probe", "aps_debug_fail_launches",
 ]
 
 _lib = None
@@ -83,8 +83,10 @@ def lib():
             [ctypes.c_int] * 6 + [_VP, _VP]
         L.aps_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), ctypes.c_int]
         L.aps_fp32_fma_probe.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _VP, _VP]
+        L.aps_debug_fail_launches.argtypes = [ctypes.c_int]
+        L.aps_debug_fail_launches.restype = None
         for name in EXPORTS:
-            if name != "aps_status_string" and name != "aps_abi_version":
+            if name not in ("aps_status_string", "aps_abi_version", "aps_debug_fail_launches"):
                 getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -174,6 +176,11 @@ def aps_device_status(clear: bool = False):
 
 # --------------------------------------------------------- torch-level calls
 APS_PROBE_THREADS = 256
+
+
+def aps_debug_fail_launches(n: int) -> None:
+    """Test hook: the next n launches report APS_ERR_LAUNCH (the kernels still run)."""
+    lib().aps_debug_fail_launches(int(n))
 
 
 def aps_fp32_fma_probe(packed, blocks, iters, sink_ptr, stream=0) -> int:

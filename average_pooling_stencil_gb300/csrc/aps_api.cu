@@ -1,6 +1,7 @@
 // aps_api.cu -- the C ABI declared in include/aps.h: argument validation,
 // output shapes, kernel selection and the per-device status word.  Every
 // accepted request runs on the GPU; nothing here computes on the host.
+#include <atomic>
 #include <mutex>
 
 #include "aps_internal.h"
@@ -126,8 +127,15 @@ bool encode_tiled(CUtensorMap *map, CUtensorMapDataType type, uint32_t rank, voi
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Launches still to report as rejected (aps_debug_fail_launches).
+static std::atomic<int> g_fail_launches{0};
+
 aps_status launch_status() {
-    return cudaGetLastError() == cudaSuccess ? APS_OK : APS_ERR_LAUNCH;
+    const bool ok = cudaGetLastError() == cudaSuccess;
+    if (g_fail_launches.load(std::memory_order_relaxed) > 0 &&
+        g_fail_launches.fetch_sub(1, std::memory_order_relaxed) > 0)
+        return APS_ERR_LAUNCH;
+    return ok ? APS_OK : APS_ERR_LAUNCH;
 }
 
 }  // namespace aps
@@ -399,3 +407,7 @@ aps_status aps_device_status(unsigned int *bits, int clear) {
 }
 
 }  // extern "C"
+
+extern "C" void aps_debug_fail_launches(int n) {
+    aps::g_fail_launches.store(n > 0 ? n : 0, std::memory_order_relaxed);
+}

@@ -223,6 +223,13 @@ aps_status aps_device_status(unsigned int *bits, int clear);
 aps_status aps_fp32_fma_probe(int packed, int blocks, int iters, float *sink,
                               aps_stream_t stream);
 
+/* Test hook for the error path (not part of any op): the next n kernel
+ * launches of this process report APS_ERR_LAUNCH, as if the CUDA runtime had
+ * rejected them, although the kernels still run; n <= 0 clears it.  Lets a
+ * test check that every entry point returns the launch status and that
+ * callers see it.  Host-only, thread-safe. */
+void aps_debug_fail_launches(int n);
+
 #ifdef __cplusplus
 }
 #endif

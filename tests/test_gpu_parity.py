@@ -590,3 +590,22 @@ def test_outputs_stay_inside_their_buffer(name, offset):
         assert_frobenius(got, want, what=name)
     else:
         assert_close(got, want, tol=tol, what=name)
+
+
+# ------------------------------------------------------------ error propagation
+@pytest.mark.parametrize("name", ["avgpool_tma", "fused_tc", "fused_fp32", "convt1d_fp32",
+                                  "convt1d_tf32x3", "convt3d_tc", "convt3d_direct"])
+def test_a_rejected_launch_reaches_the_caller(name):
+    """With the test hook set, the next launch reports APS_ERR_LAUNCH: the op returns it
+    and the binding raises it; the following call runs normally."""
+    want, run, tol = CANARY[name]()
+    out = torch.empty(want.shape, device="cuda", dtype=torch.float32)
+    B.aps_debug_fail_launches(1)
+    try:
+        with pytest.raises(B.ApsError) as e:
+            run(out)
+        assert e.value.status == B.APS_ERR_LAUNCH
+    finally:
+        B.aps_debug_fail_launches(0)
+    run(out)
+    assert_close(out.cpu().numpy(), want, tol=tol, what=name)
