@@ -22,8 +22,9 @@
 //  * warps 2, 3, 12..17 -- converters (one per 4 channels): transpose each raw
 //    box into the K-major,
 //    no-swizzle operand layout (8-row x 16-byte core matrices; rows = window
-//    positions, 4 channels per 16 bytes, one block of rows per 4 channels) and
-//    round to tf32 (cvt.rna).  Because rows are 16 bytes apart, the operand of
+//    positions, 4 channels per 16 bytes, one block of rows per 4 channels); for
+//    tf32 the words go in as they are (the MMA reads their leading 19 bits), for
+//    3xTF32 split into hi and lo.  Because rows are 16 bytes apart, the operand of
 //    tap k is the same buffer with its start moved by 16 bytes per row of tap
 //    offset: one transposed copy serves every tap of every class.
 //  * warp 1, lane 0  -- MMA issuer: walks a per-CTA table of descriptors and,
@@ -516,11 +517,13 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
                                                  tc1::to_tf32(v3 - __uint_as_float(h.w)));
                         }
                     } else {
+                        // plain tf32: the MMA reads the leading 19 bits of each fp32
+                        // word, so the values go in unrounded (truncated to tf32)
 #pragma unroll 2
                         for (int pos = lane; pos < BW; pos += 32)
-                            d0[pos] = make_uint4(tc1::to_tf32(s0[pos]), tc1::to_tf32(s0[BW + pos]),
-                                                 tc1::to_tf32(s0[2 * BW + pos]),
-                                                 tc1::to_tf32(s0[3 * BW + pos]));
+                            d0[pos] = make_uint4(__float_as_uint(s0[pos]), __float_as_uint(s0[BW + pos]),
+                                                 __float_as_uint(s0[2 * BW + pos]),
+                                                 __float_as_uint(s0[3 * BW + pos]));
                     }
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
