@@ -28,6 +28,19 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // in milliseconds; a wait this long means a copy never landed.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
+// ------------------------------------------------------------ launch overlap
+// The convolution kernels are launched as programmatic dependents of the
+// kernel before them on the stream; the AvgPool3d kernels are not.
+// pdl_trigger lets the next launch begin once every CTA of this grid has
+// started (its CTAs take SMs as this grid's CTAs leave them); pdl_wait holds
+// the calling thread until the grids before this one have completed and their
+// writes are visible.  Each thread calls pdl_wait before its first
+// global-memory access, so the overlap covers only launch and on-chip set-up.
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------ mbarriers
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -34,6 +34,26 @@ aps_status launch_status();
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Launches `kern` on `st` as a programmatic dependent of the kernel before it
+// on the stream (the kernel calls pdl_wait before touching global memory), so
+// that its launch and on-chip setup overlap the previous kernel's tail.  The
+// launch error, if any, is left for launch_status.
+template <typename... P, typename... A>
+inline void launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       A &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, kern, static_cast<P>(args)...);
+}
+
 // ------------------------------------------------------------ launchers
 // Each launcher assumes validated arguments and a non-empty output.
 

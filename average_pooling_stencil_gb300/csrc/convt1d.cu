@@ -102,6 +102,8 @@ __global__ void __launch_bounds__(ct1::THREADS, 2)
                          const float *__restrict__ bias, float *__restrict__ y, int Cin,
                          int Cout, int L, int L_out, int ph, int n_mtiles, long long n_units,
                          int vec_store) {
+    pdl_trigger();
+    pdl_wait();
     using namespace ct1;
     using T = Taps<S, K, DIL, PL>;
     constexpr int XW = T::XW, XP = T::XP, XS = T::XS, WC = T::WC;
@@ -287,9 +289,9 @@ static aps_status launch_tiled(const float *x, const int64_t in[3], const float 
     if (per_sm < 1) return APS_ERR_CUDA;
     const long long slots = std::max<long long>(1, (long long)per_sm * sm_count() / gy);
     const long long gx = std::min<long long>(n_units, slots);
-    kern<<<dim3((unsigned)gx, (unsigned)gy, 1), THREADS, (size_t)smem, st>>>(
-        x, w, bias, y, (int)in[1], (int)c_out, (int)in[2], (int)l_out, (p - PL) / S,
-        (int)n_mtiles, n_units, vec);
+    launch_pdl(kern, dim3((unsigned)gx, (unsigned)gy, 1), dim3(THREADS), (size_t)smem, st, x, w,
+               bias, y, (int)in[1], (int)c_out, (int)in[2], (int)l_out, (p - PL) / S, (int)n_mtiles,
+               n_units, vec);
     return launch_status();
 }
 
@@ -315,6 +317,8 @@ __global__ void convt1d_direct_kernel(const float *__restrict__ x, const float *
                                       const float *__restrict__ bias, float *__restrict__ y,
                                       long long total, int Cin, int Cout, int L, int L_out, int K,
                                       int s, int p, int d) {
+    pdl_trigger();
+    pdl_wait();
     for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
          idx += (long long)gridDim.x * blockDim.x) {
         const int o = (int)(idx % L_out);
@@ -346,8 +350,8 @@ aps_status launch_convt1d_direct(const float *x, const int64_t in[3], const floa
     const int threads = 256;
     const long long blocks =
         std::min<long long>(ceil_div(total, threads), (long long)sm_count() * 16);
-    convt1d_direct_kernel<<<(unsigned)blocks, threads, 0, st>>>(
-        x, w, bias, y, total, (int)in[1], (int)c_out, (int)in[2], (int)l_out, k, s, p, d);
+    launch_pdl(convt1d_direct_kernel, dim3((unsigned)blocks), dim3(threads), 0, st, x, w, bias, y,
+               total, (int)in[1], (int)c_out, (int)in[2], (int)l_out, k, s, p, d);
     return launch_status();
 }
 

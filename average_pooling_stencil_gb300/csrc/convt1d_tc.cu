@@ -102,6 +102,8 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
                         int tmem_cols, int nacc, int RS, int nbuf, int dgroups, int vec_store,
                         int tma_store, int CKr, int XTS,
                         const __grid_constant__ tc1::Taps taps, unsigned int *status) {
+    pdl_trigger();
+    pdl_wait();
     using namespace tc1;
     constexpr bool split = SPLIT;
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -696,9 +698,9 @@ aps_status launch_convt1d_tf32(const float *x, const int64_t in[3], const float 
     const long long n_units = (long long)N * n_mtiles;
     const long long grid = std::min<long long>(n_units, (long long)sm_count());
     const int vec = (l_out % 4 == 0) && (reinterpret_cast<uintptr_t>(y) % 16 == 0);
-    kern<<<(unsigned)grid, THREADS, smem, st>>>(
-        map, ymap, w, bias, y, (int)Cin, (int)c_out, k, s, (int)l_out, n_mtiles, n_units, win0,
-        BW, cols, nacc, RS, nbuf, dgroups, vec, tma_store, CKr, XTS, taps, status_word());
+    launch_pdl(kern, dim3((unsigned)grid), dim3(THREADS), smem, st, map, ymap, w, bias, y, (int)Cin,
+               (int)c_out, k, s, (int)l_out, n_mtiles, n_units, win0, BW, cols, nacc, RS, nbuf,
+               dgroups, vec, tma_store, CKr, XTS, taps, status_word());
     return launch_status();
 }
 

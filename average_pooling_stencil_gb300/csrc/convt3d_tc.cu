@@ -105,6 +105,8 @@ __global__ void __launch_bounds__(c3t::THREADS, 1)
                       const float *__restrict__ bias, float *__restrict__ y, int D, int H, int W,
                       int BW, int Do, int Ho, int Wo, int n_mhb, long long n_units,
                       unsigned int *status) {
+    pdl_trigger();
+    pdl_wait();
     using namespace c3t;
     extern __shared__ __align__(128) unsigned char smraw[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smraw + OFF_FULL);
@@ -393,9 +395,8 @@ aps_status launch_convt3d_tc(const float *x, const int64_t in[5], const float *w
     // one CTA per SM: each holds all 512 tensor-memory columns
     if (resident_ctas((const void *)kern, THREADS, (int)smem) < 1) return APS_ERR_UNSUPPORTED;
     const long long grid = std::min<long long>(sm_count(), n_units);
-    kern<<<(unsigned)grid, THREADS, smem, st>>>(map, w, bias, y, (int)D, (int)H, (int)W, BW,
-                                                 (int)Do, (int)Ho, (int)Wo, (int)n_mhb, n_units,
-                                                 status_word());
+    launch_pdl(kern, dim3((unsigned)grid), dim3(THREADS), smem, st, map, w, bias, y, (int)D, (int)H,
+               (int)W, BW, (int)Do, (int)Ho, (int)Wo, (int)n_mhb, n_units, status_word());
     return launch_status();
 }
 

@@ -84,6 +84,8 @@ __global__ void __launch_bounds__(ct3::THREADS, BW_T ? 2 : 1)
                            float scale1, float scale2, float *__restrict__ y, int Cin, int D,
                            int H, int W, int BW_rt, int XR, int RB, int WB, int n_ohb,
                            int n_owb, long long n_units, unsigned int *status) {
+    pdl_trigger();
+    pdl_wait();
     using namespace ct3;
     const int BW = BW_T ? BW_T : BW_rt;
     const int Do = D - 1, Ho = H - 1, Wo = W - 1;
@@ -351,10 +353,9 @@ aps_status launch_ct3d_pool2_fast(const float *x, const int64_t in[5], const flo
     const int per_sm = resident_ctas((const void *)kern, THREADS, (int)smem);
     if (per_sm < 1) return APS_ERR_UNSUPPORTED;
     const long long grid = std::min<long long>((long long)per_sm * sm_count(), n_units);
-    kern<<<(unsigned)grid, THREADS, smem, st>>>(map, use_tma, x, w, conv_bias, bias, scale1,
-                                                 scale2, y, (int)Cin, (int)D, (int)H, (int)W, BW,
-                                                 XR, RB, WB, (int)n_ohb, (int)n_owb, n_units,
-                                                 status_word());
+    launch_pdl(kern, dim3((unsigned)grid), dim3(THREADS), smem, st, map, use_tma, x, w, conv_bias,
+               bias, scale1, scale2, y, (int)Cin, (int)D, (int)H, (int)W, BW, XR, RB, WB,
+               (int)n_ohb, (int)n_owb, n_units, status_word());
     return launch_status();
 }
 
@@ -366,6 +367,8 @@ __global__ void ct3d_pool_direct_kernel(const float *__restrict__ x, const float
                                         int Cin, int Cout, int D, int H, int W, int Do, int Ho,
                                         int Wo, int kd, int kh, int kw, int sd, int sh, int sw,
                                         int pd, int ph, int pw, int dd, int dh, int dw, int q) {
+    pdl_trigger();
+    pdl_wait();
     for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
          idx += (long long)gridDim.x * blockDim.x) {
         const int pw_ = (int)(idx % Wo);
@@ -425,10 +428,10 @@ aps_status launch_ct3d_pool_direct(const float *x, const int64_t in[5], const fl
     const int threads = 256;
     const long long blocks =
         std::min<long long>(ceil_div(total, threads), (long long)sm_count() * 16);
-    ct3d_pool_direct_kernel<<<(unsigned)blocks, threads, 0, st>>>(
-        x, w, conv_bias, bias, scale1, scale2, y, total, (int)in[1], (int)c_out, (int)in[2],
-        (int)in[3], (int)in[4], (int)out[2], (int)out[3], (int)out[4], k[0], k[1], k[2], s[0],
-        s[1], s[2], p[0], p[1], p[2], d[0], d[1], d[2], pool_k);
+    launch_pdl(ct3d_pool_direct_kernel, dim3((unsigned)blocks), dim3(threads), 0, st, x, w,
+               conv_bias, bias, scale1, scale2, y, total, (int)in[1], (int)c_out, (int)in[2],
+               (int)in[3], (int)in[4], (int)out[2], (int)out[3], (int)out[4], k[0], k[1], k[2],
+               s[0], s[1], s[2], p[0], p[1], p[2], d[0], d[1], d[2], pool_k);
     return launch_status();
 }
 

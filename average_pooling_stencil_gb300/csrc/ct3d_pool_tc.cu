@@ -24,19 +24,25 @@
 // channels x 2 input planes x 33 rows x 32/36 columns, zero-filled outside
 // the tensor) behind full/empty mbarriers, and writes each unit's coordinates
 // into its stage's slot.  An M-tile is 4 output rows x 32 columns = 128
-// positions; group g takes tiles g and g+4 of each unit, warp q of the group
-// row q of a tile (tensor-memory lanes 32q..32q+31, the lanes a warp may
-// address), lane l column l.  Per tile each thread reads its 8*C_in inputs
-// from shared memory (32 consecutive words per warp load), splits them and
-// writes its hi and lo A row into its lane with tcgen05.st.  After both tiles
-// one group barrier hands them to two MMA threads (lane 0 of the group's
-// first two warps), each issuing one tile's 3*C_in MMAs (M 128, N 16, K 8, A
-// from tensor memory, B = the collapsed weights in shared memory) and a commit.  The warps then release the stage,
-// wait for the commit, load both accumulator rows (two tcgen05.ld in flight,
-// one wait), add the folded bias and write each channel's row with one
-// whole-warp store.  Every wait is bounded; the group barrier also carries
-// each warp's "go on" vote, so that a group whose wait ran out leaves
-// together, drains what it issued and frees the tensor memory.
+// positions; group g takes tiles g and g+4 of each unit (its tile 0 and tile
+// 1, through tile buffers 0 and 1), warp q of the group row q of a tile
+// (tensor-memory lanes 32q..32q+31, the lanes a warp may address), lane l
+// column l.  Per tile each thread reads its 8*C_in inputs from shared memory
+// (32 consecutive words per warp load), splits them and writes its hi and lo
+// A row into its lane with tcgen05.st; a group barrier then hands the tile to
+// its MMA thread (lane 0 of the group's warp 0 for tile 0, warp 1 for tile 1),
+// which issues the tile's 3*C_in MMAs (M 128, N 16, K 8, A from tensor
+// memory, B = the collapsed weights in shared memory) and commits to the
+// buffer's barrier.  The epilogue of a buffer -- wait for the commit, load the
+// accumulator row, add the folded bias, one whole-warp store per channel row
+// -- runs one step behind: per unit a group gathers tile 0, issues it, stores
+// the previous unit's tile 1, gathers tile 1, releases the stage, issues
+// tile 1 and stores tile 0, so that each MMA chain runs while the group
+// works on the other buffer.  Every wait is bounded; each group barrier also
+// carries each warp's "go on" vote, so that a group whose wait ran out leaves
+// together, drains what it issued and frees the tensor memory.  The kernel is
+// launched as a programmatic dependent of the one before it on the stream:
+// barrier set-up and the tensor-memory allocation overlap that kernel's tail.
 #include <algorithm>
 #include <cstring>
 
@@ -64,11 +70,11 @@ constexpr int SLACK = 64;                  // floats after a stage: lanes past t
 // Fixed head of the dynamic shared memory (bytes); the stages follow.
 constexpr int OFF_FULL = 0;                // uint64 [STAGES]
 constexpr int OFF_EMPTY = 32;              // uint64 [STAGES]
-constexpr int OFF_DFULL = 64;              // uint64 [GROUPS]: the group's MMAs of a unit are done
-constexpr int OFF_TMEM = 96;               // uint32: tensor-memory base
-constexpr int OFF_ABORT = 100;             // int
-constexpr int OFF_SLOT = 128;              // UnitSlot [STAGES]
-constexpr int OFF_BIAS = 256;              // float [16]
+constexpr int OFF_DFULL = 64;              // uint64 [GROUPS][2]: a tile buffer's MMAs are done
+constexpr int OFF_TMEM = 128;              // uint32: tensor-memory base
+constexpr int OFF_ABORT = 132;             // int
+constexpr int OFF_SLOT = 144;              // UnitSlot [STAGES]
+constexpr int OFF_BIAS = 320;              // float [16]
 constexpr int OFF_B = 384;                 // B operand, hi then lo: [C_in][2][16][4] words each
 constexpr int B_CI_BYTES = 2 * COUT * 16;  // one input channel's K-step of 8: 512 bytes
 constexpr int HEAD_BYTES = OFF_B + 2 * CIN_MAX * B_CI_BYTES;      // 3456, a multiple of 128
@@ -141,12 +147,16 @@ __global__ void __launch_bounds__(ctc::THREADS, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], WARPS);
         }
-        for (int g = 0; g < GROUPS; ++g) mbar_init(&dfull[g], TILES_PER_GROUP);
+        for (int g = 0; g < 2 * GROUPS; ++g) mbar_init(&dfull[g], 1);
         *abort_flag = 0;
         mbar_fence_init();
     }
+    // barrier set-up and the tensor-memory allocation overlap the kernel
+    // before this one on the stream; global memory waits for it
+    pdl_trigger();
     if (warp == 0) tc::tmem_alloc(tmem_slot, TMEM_COLS);
     __syncthreads();
+    pdl_wait();
     uint32_t issued = 0;   // units thread 0 has filled
     if (tid == 0) {
         tma_prefetch_desc(&xmap);
@@ -192,11 +202,73 @@ __global__ void __launch_bounds__(ctc::THREADS, 1)
     for (int co = 0; co < COUT; ++co) bias_r[co] = bsm[co];
     uint32_t k = 0;                                      // units this CTA has taken
     bool fail = false;
+    uint64_t *dfb = dfull + 2 * grp;                     // the group's two tile buffers
+    // tile j of a unit goes through buffer j; buffer 1's epilogue runs one
+    // step later, so that each MMA chain runs under the other buffer's
+    // epilogue and gather
+    auto gather = [&](const float *xb, int j) {
+        const int h = TILE_ROWS * (grp + GROUPS * j) + q;
+        uint32_t av[16 * CIN];   // hi[0 .. 8*CIN), then lo
+#pragma unroll
+        for (int ci = 0; ci < CIN; ++ci)
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const int a = t >> 2, bb = (t >> 1) & 1, c = t & 1;
+                const float v = xb[((ci * 2 + a) * XR + h + bb) * BW + lane + c];
+                const uint32_t hi = __float_as_uint(v) & 0xFFFFE000u;
+                av[ci * 8 + t] = hi;
+                av[8 * CIN + ci * 8 + t] = __float_as_uint(v - __uint_as_float(hi));
+            }
+        const uint32_t col = gcol + (uint32_t)(j * BUF_COLS);
+#pragma unroll
+        for (int s = 0; s < CIN; ++s) tc::tmem_st16(tmem + lane_q + col + 16 * s, av + 16 * s);
+        tc::tmem_st_wait();
+    };
+    auto issue = [&](int j, int rows) {
+        if (q == j && lane == 0) {
+            tc::tc_fence_after();
+            if (TILE_ROWS * (grp + GROUPS * j) < rows) {
+                const uint32_t col = gcol + (uint32_t)(j * BUF_COLS);
+                const uint32_t d = tmem + col + D_COL;
+#pragma unroll
+                for (int ci = 0; ci < CIN; ++ci) {
+                    const uint32_t ahi = tmem + col + 8 * ci, alo = ahi + 8 * CIN;
+                    const uint64_t bh = tc::umma_desc(b_hi + ci * B_CI_BYTES, 256, 128);
+                    const uint64_t bl = tc::umma_desc(b_lo + ci * B_CI_BYTES, 256, 128);
+                    tc::umma_tf32_ts(d, alo, bh, IDESC, ci > 0 ? 1u : 0u);   // lo(x) hi(w)
+                    tc::umma_tf32_ts(d, ahi, bl, IDESC, 1u);                 // hi(x) lo(w)
+                    tc::umma_tf32_ts(d, ahi, bh, IDESC, 1u);                 // hi(x) hi(w)
+                }
+            }
+            tc::umma_commit(&dfb[j]);
+        }
+        __syncwarp();
+    };
+    // wait for buffer j's MMAs of the unit taken k-th; then its accumulator
+    // row + bias -> 16 whole-warp row stores
+    auto epilogue = [&](int j, uint32_t kk, float *yb, int rows) {
+        if (!mbar_wait(&dfb[j], kk & 1u)) {
+            record_error(status, APS_DEVERR_TIMEOUT);
+            *abort_flag = 1;
+            fail = true;
+        }
+        fail = __any_sync(0xffffffffu, fail);
+        if (fail) return;
+        tc::tc_fence_after();
+        uint32_t d[COUT];
+        tc::tmem_ld16(tmem + lane_q + gcol + (uint32_t)(j * BUF_COLS) + D_COL, d);
+        const int h = TILE_ROWS * (grp + GROUPS * j) + q;
+        if (h < rows && yb) {
+            float *yr = yb + h * Wo;
+#pragma unroll
+            for (int co = 0; co < COUT; ++co) yr[co * cs] = __uint_as_float(d[co]) + bias_r[co];
+        }
+    };
+    float *prev_y = nullptr;   // the previous unit's output corner (this lane's column)
+    int prev_rows = 0;
+    uint32_t c0 = 0, c1 = 0;         // commits to each buffer's barrier
     for (long long u = blockIdx.x; u < n_units; u += gridDim.x, ++k) {
         const int b = (int)(k % STAGES);
-        // thread 0 keeps STAGES-1 units in flight ahead of this one: unit
-        // k+STAGES-1 goes into the stage that held unit k-1, once every warp is
-        // done with it
         const long long ahead = u + (long long)(STAGES - 1) * gridDim.x;
         if (tid == 0 && !*abort_flag && ahead < n_units) {
             const int nb = (int)((k + STAGES - 1) % STAGES);
@@ -216,98 +288,40 @@ __global__ void __launch_bounds__(ctc::THREADS, 1)
         }
         ok = __all_sync(0xffffffffu, ok);
         const int grows = ok ? slot[b].rows : 0;
-
-        // ---- A rows of the group's two tiles into tensor memory
-        if (ok) {
-            const float *xb = xs + b * stage_stride;
-#pragma unroll 1
-            for (int j = 0; j < TILES_PER_GROUP; ++j) {
-                const int tile = grp + GROUPS * j;   // rows 4*tile .. 4*tile+3 of the unit
-                if (TILE_ROWS * tile >= grows) continue;   // uniform over the group
-                const int h = TILE_ROWS * tile + q;
-                uint32_t av[16 * CIN];   // hi[0 .. 8*CIN), then lo
-#pragma unroll
-                for (int ci = 0; ci < CIN; ++ci)
-#pragma unroll
-                    for (int t = 0; t < 8; ++t) {
-                        const int a = t >> 2, bb = (t >> 1) & 1, c = t & 1;
-                        const float v = xb[((ci * 2 + a) * XR + h + bb) * BW + lane + c];
-                        const uint32_t hi = __float_as_uint(v) & 0xFFFFE000u;
-                        av[ci * 8 + t] = hi;
-                        av[8 * CIN + ci * 8 + t] = __float_as_uint(v - __uint_as_float(hi));
-                    }
-                const uint32_t col = gcol + (uint32_t)(j * BUF_COLS);
-#pragma unroll
-                for (int s = 0; s < CIN; ++s) tc::tmem_st16(tmem + lane_q + col + 16 * s, av + 16 * s);
-            }
-            tc::tmem_st_wait();
-        }
+        const float *xb = xs + b * stage_stride;
+        if (ok && TILE_ROWS * grp < grows) gather(xb, 0);
         tc::tc_fence_before();
         __syncwarp();
-        // hand both tiles to the group's MMA thread; the group decides together
-        // whether to go on, so that no warp is left at a group barrier
         if (tc::named_bar_or(gbar, 128, !ok)) break;
-        // tile j's MMA chain is issued by lane 0 of the group's warp j, so that
-        // the two chains go out in parallel; each commits to the group's
-        // barrier (two arrivals a unit, tiles or not)
-        if (q < TILES_PER_GROUP && lane == 0) {
-            const int j = q;
-            tc::tc_fence_after();
-            if (TILE_ROWS * (grp + GROUPS * j) < grows) {
-                const uint32_t col = gcol + (uint32_t)(j * BUF_COLS);
-                const uint32_t d = tmem + col + D_COL;
-#pragma unroll
-                for (int ci = 0; ci < CIN; ++ci) {
-                    const uint32_t ahi = tmem + col + 8 * ci, alo = ahi + 8 * CIN;
-                    const uint64_t bh = tc::umma_desc(b_hi + ci * B_CI_BYTES, 256, 128);
-                    const uint64_t bl = tc::umma_desc(b_lo + ci * B_CI_BYTES, 256, 128);
-                    tc::umma_tf32_ts(d, alo, bh, IDESC, ci > 0 ? 1u : 0u);   // lo(x) hi(w)
-                    tc::umma_tf32_ts(d, ahi, bl, IDESC, 1u);                 // hi(x) lo(w)
-                    tc::umma_tf32_ts(d, ahi, bh, IDESC, 1u);                 // hi(x) hi(w)
-                }
-            }
-            tc::umma_commit(&dfull[grp]);
-        }
-        __syncwarp();
-
-        // where the outputs go, read before the stage and its slot are released
+        issue(0, grows);
+        ++c0;
+        if (k > 0) epilogue(1, k - 1, prev_y, prev_rows);
+        if (!fail && TILE_ROWS * (grp + GROUPS) < grows) gather(xb, 1);
         const long long gn = slot[b].n;
         const int god = slot[b].od, goh0 = slot[b].oh0, gow0 = slot[b].ow0, gcols = slot[b].cols;
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[b]);
-
-        // ---- epilogue: both accumulator rows -> + bias -> whole-warp row stores
-        if (!mbar_wait(&dfull[grp], k & 1u)) {
-            record_error(status, APS_DEVERR_TIMEOUT);
-            *abort_flag = 1;
-            fail = true;
-        }
-        fail = __any_sync(0xffffffffu, fail);
-        if (fail) continue;   // the next unit's decision ends the loop
-        tc::tc_fence_after();
-        uint32_t d0[COUT], d1[COUT];
-        tc::tmem_ld16_async(tmem + lane_q + gcol + D_COL, d0);
-        tc::tmem_ld16_async(tmem + lane_q + gcol + BUF_COLS + D_COL, d1);
-        tc::tmem_ld_wait(d0, d1);
-        if (lane < gcols) {
-            float *yb = y + ((gn * COUT) * Do + god) * plane + (long long)goh0 * Wo + gow0 + lane;
-            const int h0 = TILE_ROWS * grp + q, h1 = h0 + TILE_ROWS * GROUPS;
-            if (h0 < grows) {
-                float *yr = yb + h0 * Wo;
-#pragma unroll
-                for (int co = 0; co < COUT; ++co) yr[co * cs] = __uint_as_float(d0[co]) + bias_r[co];
-            }
-            if (h1 < grows) {
-                float *yr = yb + h1 * Wo;
-#pragma unroll
-                for (int co = 0; co < COUT; ++co) yr[co * cs] = __uint_as_float(d1[co]) + bias_r[co];
-            }
-        }
+        tc::tc_fence_before();
+        __syncwarp();
+        if (tc::named_bar_or(gbar, 128, fail)) break;
+        issue(1, grows);
+        ++c1;
+        float *ycur = lane < gcols
+            ? y + ((gn * COUT) * Do + god) * plane + (long long)goh0 * Wo + gow0 + lane : nullptr;
+        epilogue(0, k, ycur, grows);
+        prev_y = ycur;
+        prev_rows = grows;
     }
+    // the last unit's buffer-1 tiles
+    if (__all_sync(0xffffffffu, c1 > 0 && c1 == k && !fail && !*abort_flag))
+        epilogue(1, c1 - 1, prev_y, prev_rows);
 
-    // ---- leave nothing in flight: the group's last MMAs (their wait may
+    // ---- leave nothing in flight: each buffer's last MMAs (their wait may
     // have run out), the fills no warp consumed; then free the tensor memory
-    if (q == 0 && lane == 0 && k > 0) mbar_wait(&dfull[grp], (k - 1) & 1u);
+    if (q < 2 && lane == 0) {
+        const uint32_t c = q ? c1 : c0;
+        if (c > 0) mbar_wait(&dfb[q], (c - 1) & 1u);
+    }
     if (tid == 0)
         for (uint32_t j = k; j < issued; ++j) mbar_wait(&full[j % STAGES], (j / STAGES) & 1u);
     tc::tc_fence_before();
@@ -360,9 +374,9 @@ aps_status launch_ct3d_pool2_tc(const float *x, const int64_t in[5], const float
     // one CTA per SM: each holds all 512 tensor-memory columns
     if (resident_ctas((const void *)kern, THREADS, (int)smem) < 1) return APS_ERR_UNSUPPORTED;
     const long long grid = std::min<long long>(sm_count(), n_units);
-    kern<<<(unsigned)grid, THREADS, smem, st>>>(map, w, conv_bias, bias, scale1, scale2, y,
-                                                 (int)D, (int)H, (int)W, BW, XR, RB, WB,
-                                                 (int)n_ohb, (int)n_owb, n_units, status_word());
+    launch_pdl(kern, dim3((unsigned)grid), dim3(THREADS), smem, st, map, w, conv_bias, bias,
+               scale1, scale2, y, (int)D, (int)H, (int)W, BW, XR, RB, WB, (int)n_ohb,
+               (int)n_owb, n_units, status_word());
     return launch_status();
 }
 

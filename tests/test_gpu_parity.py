@@ -168,6 +168,20 @@ def test_fused_unaligned_input_takes_the_fp32_kernel():
     assert_close(y.cpu().numpy(), fused_ref(base, x, w, cb, b), what="fused unaligned x")
 
 
+# many small units: every CTA of the FP32-pipe kernel's persistent grid takes several, so
+# its double-buffered input ring goes round (and its barrier phases flip) many times; W = 4
+# stages the input by TMA, W = 5 by element copies
+@pytest.mark.parametrize("shape", [(80, 5, 33, 3, 4), (80, 4, 33, 3, 5)])
+def test_fused_fp32_kernel_many_units_per_cta(shape):
+    x, = rng_inputs(45, shape)
+    w, cb, b = rng_inputs(46, (shape[1], 16, 3, 3, 3), (16,), (16,), lo=-0.2, hi=0.2)
+    prm = dict(stride=(2, 2, 2), pad=(1, 1, 1), out_pad=(0, 0, 0), dil=(1, 1, 1), pool_k=2,
+               scale1=0.5, scale2=1.0)
+    ref = ora.ct3d_scale_pool_bias(x, w, cb, b, (2, 2, 2), (1, 1, 1), (0, 0, 0), (1, 1, 1), 2,
+                                   0.5, 1.0)
+    assert_close(fused_gpu(x, w, cb, b, prm), ref, what=f"fused fp32 many units {shape}")
+
+
 def test_fused_without_conv_bias_and_other_scales():
     wl = workloads.get(0)
     x, w, b = (wl.generate(n) for n in ("x", "w", "bias"))
@@ -221,6 +235,17 @@ def test_convt3d_cases(xs, cout, k, s, p, d, op, has_bias):
                  what=f"convt3d {xs} k{k} s{s} p{p} d{d} op{op}")
 
 
+# C_in 8 (and C_in 3 at W 36): the FP32-pipe kernel, with ~1500 units, several per CTA of
+# its persistent grid, so its double-buffered ring wraps many times
+@pytest.mark.parametrize("xs", [(48, 8, 16, 3, 4), (24, 3, 16, 3, 36)])
+def test_convt3d_fp32_kernel_many_units_per_cta(xs):
+    x, = rng_inputs(47, xs)
+    w, b = rng_inputs(48, (xs[1], 16, 3, 3, 3), (16,), lo=-0.3, hi=0.3)
+    args = ((2, 2, 2), (1, 1, 1), (1, 1, 1), (0, 0, 0))
+    y = B.convtranspose3d(dev(x), dev(w), dev(b), *args)
+    assert_close(y.cpu().numpy(), ora.convt(x, w, b, *args), what=f"convt3d many units {xs}")
+
+
 def test_convt3d_unaligned_input_takes_the_direct_kernel():
     """An input that is not 16-byte aligned cannot be a TMA source: the op then runs
     the direct kernel, on a shape the tensor cores take when aligned."""
@@ -248,6 +273,40 @@ def test_convt3d_full_workload_sampled_planes():
     got = np.stack([y[n, c].cpu().numpy() for n, c in sel])
     assert_close(got, ref, what="convt3d full workload")
     assert torch.isfinite(y).all()
+
+
+# ------------------------------------------------------------ back-to-back ops
+def test_an_op_sees_what_the_kernel_before_it_wrote():
+    """The convolution kernels are launched as programmatic dependents of the
+    kernel before them on the stream.  A direct ConvTranspose3d writes x1 and the
+    fused tensor-core kernel reads it at once, with no synchronisation between."""
+    x0, = rng_inputs(51, (4, 3, 9, 33, 64))
+    w0, = rng_inputs(52, (3, 3, 1, 1, 1), lo=-0.8, hi=0.8)
+    w, cb, b = rng_inputs(53, (3, 16, 3, 3, 3), (16,), (16,), lo=-0.2, hi=0.2)
+    one, zero = (1, 1, 1), (0, 0, 0)
+    x1 = B.convtranspose3d(dev(x0), dev(w0), None, one, zero, one, zero)
+    y = B.ct3d_scale_pool_bias(x1, dev(w), dev(cb), dev(b), scale1=0.5, scale2=1.0)
+    torch.cuda.synchronize()
+    x1h = x1.cpu().numpy()
+    assert_close(x1h, ora.convt(x0, w0, None, one, zero, one, zero), what="producer")
+    ref = ora.ct3d_scale_pool_bias(x1h, w, cb, b, (2, 2, 2), (1, 1, 1), zero, one, 2, 0.5, 1.0)
+    assert_close(y.cpu().numpy(), ref, what="consumer of the previous kernel's output")
+
+
+def test_an_op_does_not_overwrite_what_the_kernel_before_it_reads():
+    """A ConvTranspose1d reads x; the next op on the stream writes its output over
+    x.  The first must still see the original x everywhere."""
+    x, = rng_inputs(54, (4, 32, 65536))
+    w, = rng_inputs(55, (32, 64, 5), lo=-0.06, hi=0.06)
+    z, w2 = rng_inputs(56, (4, 64, 65532), (64, 32, 5), lo=-0.5, hi=0.5)
+    xd, zd, w2d = dev(x), dev(z), dev(w2)
+    torch.cuda.synchronize()
+    y = B.convtranspose1d(xd, dev(w), None, 1, 0, 3, 0)
+    B.convtranspose1d(zd, w2d, None, 1, 0, 1, 0, out=xd)      # overwrites x
+    torch.cuda.synchronize()
+    sel = [(0, 0), (1, 40), (2, 63), (3, 5)]
+    got = np.stack([y[n, c].cpu().numpy() for n, c in sel])
+    assert_close(got, ora.convt(x, w, None, 1, 0, 3, 0, sel=sel), what="reader of the overwritten x")
 
 
 # ------------------------------------------------------------ convtranspose1d
