@@ -184,9 +184,6 @@ aps_status launch_avgpool3d_k3s2p1_tma(const float *x, const int64_t in[5], floa
                                      SMEM_BYTES);
     if (per_sm < 1) return APS_ERR_CUDA;
     const long long grid = std::min<long long>(n_units, (long long)sm_count() * per_sm);
-    // a plain launch: as a programmatic dependent this streaming kernel ran
-    // 5 % slower back to back with the trigger at its start, and no faster
-    // with the trigger at its end
     avgpool3d_k3s2p1_tma_kernel<<<(unsigned)grid, THREADS, SMEM_BYTES, st>>>(
         map, y, Do, Ho, Wo, n_ht, n_wt, n_units, status_word());
     return launch_status();
