@@ -39,6 +39,10 @@
  *    was launched, except APS_ERR_LAUNCH, which reports the error the CUDA
  *    runtime gave for the launch itself.  A tensor with zero elements (N or C
  *    equal to 0) is valid: the call returns APS_OK and launches nothing.
+ *    The convolution ops launch their kernel as a programmatic dependent of
+ *    the work before it on `stream` (its launch and on-chip set-up overlap
+ *    that work's tail; it touches no global memory until that work has
+ *    completed), so stream order holds exactly as for a plain launch.
  *  - Shape queries are pure host functions; they need no GPU and no CUDA
  *    context.
  *  - Kernels contain no unbounded waits.  A pipeline wait that exceeds its
