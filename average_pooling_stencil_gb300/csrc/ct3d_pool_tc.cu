@@ -79,6 +79,9 @@ constexpr int OFF_B = 384;                 // B operand, hi then lo: [C_in][2][1
 constexpr int B_CI_BYTES = 2 * COUT * 16;  // one input channel's K-step of 8: 512 bytes
 constexpr int HEAD_BYTES = OFF_B + 2 * CIN_MAX * B_CI_BYTES;      // 3456, a multiple of 128
 static_assert(HEAD_BYTES % 128 == 0, "stages start 128-byte aligned");
+static_assert(OFF_EMPTY - OFF_FULL >= 8 * STAGES && OFF_DFULL - OFF_EMPTY >= 8 * STAGES &&
+                  OFF_TMEM - OFF_DFULL >= 16 * GROUPS,
+              "barrier arrays fit");
 static_assert(D_COL + COUT <= BUF_COLS && 16 * CIN_MAX <= D_COL, "tile buffer layout");
 
 struct UnitSlot {

@@ -309,6 +309,55 @@ def test_an_op_does_not_overwrite_what_the_kernel_before_it_reads():
     assert_close(got, ora.convt(x, w, None, 1, 0, 3, 0, sel=sel), what="reader of the overwritten x")
 
 
+def test_dependent_ops_in_a_cuda_graph_and_across_streams():
+    """The same producer -> consumer pair (a direct ConvTranspose3d writing x1, the
+    fused tensor-core op reading it) captured in a CUDA graph and replayed, and run on
+    two streams joined by an event: both give the result of the plain sequence."""
+    x0, = rng_inputs(57, (2, 3, 5, 17, 32))
+    w0, = rng_inputs(58, (3, 3, 1, 1, 1), lo=-0.8, hi=0.8)
+    w, cb, b = rng_inputs(59, (3, 16, 3, 3, 3), (16,), (16,), lo=-0.2, hi=0.2)
+    one, zero = (1, 1, 1), (0, 0, 0)
+    xd, w0d, wd, cbd, bd = dev(x0), dev(w0), dev(w), dev(cb), dev(b)
+    x1h = ora.convt(x0, w0, None, one, zero, one, zero).astype(np.float32)
+    ref = ora.ct3d_scale_pool_bias(x1h, w, cb, b, (2, 2, 2), (1, 1, 1), zero, one, 2, 0.5, 1.0)
+
+    x1 = B.convtranspose3d(xd, w0d, None, one, zero, one, zero)
+    y = B.ct3d_scale_pool_bias(x1, wd, cbd, bd, scale1=0.5, scale2=1.0)
+    torch.cuda.synchronize()
+    plain = y.cpu().numpy()
+    assert_close(plain, ref, what="plain sequence")
+
+    # CUDA graph: capture both calls on a side stream, replay twice with fresh input
+    x1.zero_(); y.zero_()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            B.convtranspose3d(xd, w0d, None, one, zero, one, zero, out=x1)
+            B.ct3d_scale_pool_bias(x1, wd, cbd, bd, scale1=0.5, scale2=1.0, out=y)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        y.zero_()
+        g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(y.cpu().numpy(), plain), "graph replay differs from the plain sequence"
+
+    # two streams: the producer on s1, the consumer on s2 after an event
+    x1.zero_(); y.zero_()
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    with torch.cuda.stream(s1):
+        B.convtranspose3d(xd, w0d, None, one, zero, one, zero, out=x1)
+        ev = torch.cuda.Event()
+        ev.record(s1)
+    s2.wait_event(ev)
+    with torch.cuda.stream(s2):
+        B.ct3d_scale_pool_bias(x1, wd, cbd, bd, scale1=0.5, scale2=1.0, out=y)
+    torch.cuda.synchronize()
+    assert np.array_equal(y.cpu().numpy(), plain), "two-stream run differs from the plain sequence"
+
+
 # ------------------------------------------------------------ convtranspose1d
 CONVT_CASES = [  # (s, K, d, p, op, Cin, Cout, L, bias)
     (1, 5, 3, 0, 0, 32, 64, 1000, False),
