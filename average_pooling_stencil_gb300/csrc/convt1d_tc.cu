@@ -90,6 +90,44 @@ __device__ __forceinline__ int converter_id(int warp) {
 }
 
 using namespace tc;   // named_bar, to_tf32, umma_*, tc_fence_*, tmem_ld*
+
+// One chunk's MMAs.  Table entry e: A offset (16-byte units) | class << 16 | bit 31 on the
+// class's first entry; its B descriptor.  NE > 0: exactly NE entries, UNROLL per turn of
+// the loop, so that the table loads go ahead of the MMAs and the MMAs issue back to back;
+// the issuing thread's loads and address arithmetic, not the tensor core, set the pace of
+// a loop of 2 or 4 entries per turn.  Measured on the two ConvTranspose1d workloads: 20
+// entries fully unrolled 318 / 566 us (TF32 / 3xTF32) against 348 / 675; 16 entries in
+// turns of 8 for 3xTF32 276 against 302 us (TF32 stays at 4: full unrolling was 1.5 %
+// slower there).  NE == 0: any count, 4 (TF32) or 2 (3xTF32) per turn.
+template <int NE, int UNROLL, bool SPLIT>
+__device__ __forceinline__ void issue_chunk(const uint32_t *tab_a, const uint64_t *bt, int n_ent,
+                                            uint64_t abase, uint32_t dbase, uint32_t cout,
+                                            uint32_t idesc, bool first_chunk, uint32_t a_lo,
+                                            uint32_t b_lo) {
+    auto one = [&](int e) {
+        const uint32_t ae = tab_a[e];
+        const uint32_t acc = (!first_chunk || !(ae >> 31)) ? 1u : 0u;
+        const uint32_t d = dbase + ((ae >> 16) & 0xFFu) * cout;
+        const uint64_t a = abase + (ae & 0xFFFFu), bw = bt[e];
+        if (SPLIT) {
+            umma_tf32(d, a + a_lo, bw, idesc, acc);   // lo(x) hi(w)
+            umma_tf32(d, a, bw + b_lo, idesc, 1u);    // hi(x) lo(w)
+            umma_tf32(d, a, bw, idesc, 1u);           // hi(x) hi(w)
+        } else {
+            umma_tf32(d, a, bw, idesc, acc);
+        }
+    };
+    if constexpr (NE > 0) {
+#pragma unroll UNROLL
+        for (int e = 0; e < NE; ++e) one(e);
+    } else if constexpr (SPLIT) {
+#pragma unroll 2
+        for (int e = 0; e < n_ent; ++e) one(e);
+    } else {
+#pragma unroll 4
+        for (int e = 0; e < n_ent; ++e) one(e);
+    }
+}
 }  // namespace tc1
 
 // SPLIT: 3xTF32 (operands split into tf32 hi + lo, three MMAs per product).
@@ -293,26 +331,18 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
                     tc1::tc_fence_after();
                     const uint64_t abase = s == 0 ? a_stage[0] : (s == 1 ? a_stage[1] : a_stage[2]);
                     const uint64_t *bt = tab_b + ch * n_ent;
-                    if constexpr (split) {
-#pragma unroll 2
-                        for (int e = 0; e < n_ent; ++e) {
-                            const uint32_t ae = tab_a[e];
-                            const uint32_t acc = (ch != 0 || !(ae >> 31)) ? 1u : 0u;
-                            const uint32_t d = dbase + ((ae >> 16) & 0xFFu) * (uint32_t)Cout;
-                            const uint64_t a = abase + (ae & 0xFFFFu), bw = bt[e];
-                            tc1::umma_tf32(d, a + a_lo, bw, idesc, acc);   // lo(x) hi(w)
-                            tc1::umma_tf32(d, a, bw + b_lo, idesc, 1u);    // hi(x) lo(w)
-                            tc1::umma_tf32(d, a, bw, idesc, 1u);           // hi(x) hi(w)
-                        }
-                    } else {
-#pragma unroll 4
-                        for (int e = 0; e < n_ent; ++e) {
-                            const uint32_t ae = tab_a[e];
-                            const uint32_t acc = (ch != 0 || !(ae >> 31)) ? 1u : 0u;
-                            tc1::umma_tf32(dbase + ((ae >> 16) & 0xFFu) * (uint32_t)Cout,
-                                           abase + (ae & 0xFFFFu), bt[e], idesc, acc);
-                        }
-                    }
+                    // 20 and 16 entries: the stride-1 K5 and stride-2 K4 geometries at
+                    // 32-channel chunks
+                    if (n_ent == 20)
+                        tc1::issue_chunk<20, 20, split>(tab_a, bt, n_ent, abase, dbase,
+                                                        (uint32_t)Cout, idesc, ch == 0, a_lo,
+                                                        b_lo);
+                    else if (split && n_ent == 16)
+                        tc1::issue_chunk<16, 8, split>(tab_a, bt, n_ent, abase, dbase,
+                                                       (uint32_t)Cout, idesc, ch == 0, a_lo, b_lo);
+                    else
+                        tc1::issue_chunk<0, 1, split>(tab_a, bt, n_ent, abase, dbase,
+                                                      (uint32_t)Cout, idesc, ch == 0, a_lo, b_lo);
                     issued = true;
                     tc1::umma_commit(&xt_empty[s]);
                     if (++xs_i == (uint32_t)XTS) {
