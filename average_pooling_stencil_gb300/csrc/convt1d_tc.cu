@@ -95,10 +95,11 @@ using namespace tc;   // named_bar, to_tf32, umma_*, tc_fence_*, tmem_ld*
 // class's first entry; its B descriptor.  NE > 0: exactly NE entries, UNROLL per turn of
 // the loop, so that the table loads go ahead of the MMAs and the MMAs issue back to back;
 // the issuing thread's loads and address arithmetic, not the tensor core, set the pace of
-// a loop of 2 or 4 entries per turn.  Measured on the two ConvTranspose1d workloads: 20
-// entries fully unrolled 318 / 566 us (TF32 / 3xTF32) against 348 / 675; 16 entries in
-// turns of 8 for 3xTF32 276 against 302 us (TF32 stays at 4: full unrolling was 1.5 %
-// slower there).  NE == 0: any count, 4 (TF32) or 2 (3xTF32) per turn.
+// a loop of 2 or 4 entries per turn.  Measured on the stride-1 K5 workload (20 entries):
+// fully unrolled 318 / 566 us (TF32 / 3xTF32) against 348 / 675.  The strided K4 workload
+// (16 entries) keeps the loop: fully unrolled it was 1.5 % (TF32) and 2 % (3xTF32)
+// slower, and 8 per turn for 3xTF32 was 276 against 302 us in one comparison but 312 in
+// the bench.  NE == 0: any count, 4 (TF32) or 2 (3xTF32) per turn.
 template <int NE, int UNROLL, bool SPLIT>
 __device__ __forceinline__ void issue_chunk(const uint32_t *tab_a, const uint64_t *bt, int n_ent,
                                             uint64_t abase, uint32_t dbase, uint32_t cout,
@@ -331,15 +332,11 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
                     tc1::tc_fence_after();
                     const uint64_t abase = s == 0 ? a_stage[0] : (s == 1 ? a_stage[1] : a_stage[2]);
                     const uint64_t *bt = tab_b + ch * n_ent;
-                    // 20 and 16 entries: the stride-1 K5 and stride-2 K4 geometries at
-                    // 32-channel chunks
+                    // 20 entries: the stride-1 K5 geometry at 32-channel chunks
                     if (n_ent == 20)
                         tc1::issue_chunk<20, 20, split>(tab_a, bt, n_ent, abase, dbase,
                                                         (uint32_t)Cout, idesc, ch == 0, a_lo,
                                                         b_lo);
-                    else if (split && n_ent == 16)
-                        tc1::issue_chunk<16, 8, split>(tab_a, bt, n_ent, abase, dbase,
-                                                       (uint32_t)Cout, idesc, ch == 0, a_lo, b_lo);
                     else
                         tc1::issue_chunk<0, 1, split>(tab_a, bt, n_ent, abase, dbase,
                                                       (uint32_t)Cout, idesc, ch == 0, a_lo, b_lo);
