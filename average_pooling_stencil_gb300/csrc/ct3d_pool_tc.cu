@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(ctc::THREADS, 1)
     for (int co = 0; co < COUT; ++co) bias_r[co] = bsm[co];
     uint32_t k = 0;                                      // units this CTA has taken
     bool fail = false;
-    uint64_t *dfb = dfull + 2 * grp;                     // the group's two tile buffers
+    uint64_t *dfb = dfull + 2 * grp;                     // its two buffers' MMA-done barriers
     // tile j of a unit goes through buffer j; buffer 1's epilogue runs one
     // step later, so that each MMA chain runs under the other buffer's
     // epilogue and gather
