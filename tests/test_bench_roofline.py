@@ -64,3 +64,22 @@ def test_mixed_bound_takes_the_larger_floor():
     assert fp32_floor > hbm_floor
     assert r["bound"] == "alu"
     assert r["frac"] == pytest.approx(fp32_floor / t)
+
+
+def test_profile_traffic_is_used_only_for_the_profiled_source(tmp_path, monkeypatch):
+    """bench.py quotes a kernel's DRAM traffic from its profile summary only while the
+    kernel's source still has the hash recorded beside it."""
+    import hashlib
+    csrc = tmp_path / "average_pooling_stencil_gb300" / "csrc"
+    prof = tmp_path / "profiles"
+    csrc.mkdir(parents=True)
+    prof.mkdir()
+    src = csrc / "k.cu"
+    src.write_text("__global__ void k() {}\n")
+    sha = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    (prof / "k.md").write_text(f"source_sha256_16: {sha}\ntraffic_bytes_per_launch: 1.25e+09\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.traffic_from_profile("k.cu", "k.md") == pytest.approx(1.25e9)
+    src.write_text("__global__ void k() { }\n")            # the kernel changed
+    assert bench.traffic_from_profile("k.cu", "k.md") is None
+    assert bench.traffic_from_profile("k.cu", "missing.md") is None
