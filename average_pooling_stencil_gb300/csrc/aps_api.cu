@@ -10,6 +10,14 @@ namespace aps {
 
 // ------------------------------------------------------------ status word
 static __device__ unsigned int g_status_word;
+// aps_device_status's copy of the word, taken and (optionally) cleared in one
+// atomic step on the GPU, so that a bit set meanwhile by a kernel on another
+// stream is either in this read or left for the next one.
+static __device__ unsigned int g_status_snapshot;
+
+__global__ void status_exchange_kernel(int clear) {
+    g_status_snapshot = clear ? atomicExch(&g_status_word, 0u) : atomicOr(&g_status_word, 0u);
+}
 
 namespace {
 constexpr int kMaxDevices = 64;
@@ -130,12 +138,15 @@ bool encode_tiled(CUtensorMap *map, CUtensorMapDataType type, uint32_t rank, voi
 // Launches still to report as rejected (aps_debug_fail_launches).
 static std::atomic<int> g_fail_launches{0};
 
-aps_status launch_status() {
-    const bool ok = cudaGetLastError() == cudaSuccess;
+aps_status launch_status(cudaError_t launch_result) {
+    if (launch_result != cudaSuccess) {
+        cudaGetLastError();   // the launch's own error; the caller sees it as our status
+        return APS_ERR_LAUNCH;
+    }
     if (g_fail_launches.load(std::memory_order_relaxed) > 0 &&
         g_fail_launches.fetch_sub(1, std::memory_order_relaxed) > 0)
         return APS_ERR_LAUNCH;
-    return ok ? APS_OK : APS_ERR_LAUNCH;
+    return APS_OK;
 }
 
 }  // namespace aps
@@ -170,6 +181,20 @@ bool dims_ok(const int64_t *d, int n) {
         if (d[i] && prod > kMaxElems / d[i]) return false;
         prod *= d[i] ? d[i] : 1;
     }
+    return true;
+}
+
+// Extents the general kernels address with 32-bit positions: every channel
+// count and every spatial size of input and output below 2^30 (and, for the
+// fused op, each pre-pool size pool_k * out).  Larger requests are
+// APS_ERR_UNSUPPORTED, decided here on the host before any CUDA call.
+constexpr int64_t kMaxExtent = (int64_t)1 << 30;
+
+bool extents_ok(const int64_t *in, const int64_t *out, int n, int64_t pool_k = 1) {
+    if (in[1] >= kMaxExtent || out[1] >= kMaxExtent) return false;
+    for (int i = 2; i < n; ++i)
+        if (in[i] >= kMaxExtent || out[i] >= kMaxExtent || out[i] * pool_k >= kMaxExtent)
+            return false;
     return true;
 }
 
@@ -240,12 +265,14 @@ aps_status aps_avgpool3d(const float *x, const int64_t in[5], const int k[3], co
     if (!present(x, numel(in, 5)) || !present(y, numel(out, 5))) return APS_ERR_NULL;
     if (!aligned(x, 4) || !aligned(y, 4)) return APS_ERR_ALIGN;
     if (numel(out, 5) == 0) return APS_OK;
+    // the general kernel also numbers an output plane's cells in 32 bits
+    if (!extents_ok(in, out, 5) || out[2] * out[3] * out[4] >= ((int64_t)1 << 31))
+        return APS_ERR_UNSUPPORTED;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     const bool k3s2p1 = k[0] == 3 && k[1] == 3 && k[2] == 3 && s[0] == 2 && s[1] == 2 &&
                         s[2] == 2 && p[0] == 1 && p[1] == 1 && p[2] == 1;
-    if (k3s2p1 && count_include_pad && !ceil_mode && in[4] % 4 == 0 && aligned(x, 16) &&
-        aligned(y, 8)) {
-        st = launch_avgpool3d_k3s2p1_tma(x, in, y, out, cs);
+    if (k3s2p1 && !ceil_mode && in[4] % 4 == 0 && aligned(x, 16) && aligned(y, 8)) {
+        st = launch_avgpool3d_k3s2p1_tma(x, in, y, out, count_include_pad ? 1 : 0, cs);
         if (st != APS_ERR_UNSUPPORTED) return st;
     }
     return launch_avgpool3d_direct(x, in, k, s, p, count_include_pad ? 1 : 0, y, out, cs);
@@ -289,6 +316,7 @@ aps_status aps_ct3d_scale_pool_bias(const float *x, const int64_t in[5], const f
         (conv_bias && !aligned(conv_bias, 4)))
         return APS_ERR_ALIGN;
     if (numel(out, 5) == 0) return APS_OK;  // C_in == 0 alone still has bias-only outputs
+    if (!extents_ok(in, out, 5, pool_k)) return APS_ERR_UNSUPPORTED;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     bool fast = pool_k == 2 && c_out == 16 && in[1] >= 1 && in[1] <= 8;
     for (int i = 0; i < 3; ++i)
@@ -335,6 +363,7 @@ aps_status aps_convtranspose3d(const float *x, const int64_t in[5], const float 
     if (!aligned(x, 4) || !aligned(w, 4) || !aligned(y, 4) || (bias && !aligned(bias, 4)))
         return APS_ERR_ALIGN;
     if (numel(out, 5) == 0) return APS_OK;
+    if (!extents_ok(in, out, 5)) return APS_ERR_UNSUPPORTED;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     bool fast = c_out == 16 && in[1] >= 1 && in[1] <= 8;
     for (int i = 0; i < 3; ++i)
@@ -380,6 +409,7 @@ aps_status aps_convtranspose1d(const float *x, const int64_t in[3], const float 
     if (!aligned(x, 4) || !aligned(w, 4) || !aligned(y, 4) || (bias && !aligned(bias, 4)))
         return APS_ERR_ALIGN;
     if (numel(out, 3) == 0) return APS_OK;
+    if (!extents_ok(in, out, 3)) return APS_ERR_UNSUPPORTED;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     // no input channels: every output is its bias (exact at any precision)
     if (in[1] == 0) return launch_convt1d_direct(x, in, w, bias, c_out, k, s, p, d, y, out[2], cs);
@@ -396,12 +426,17 @@ aps_status aps_convtranspose1d(const float *x, const int64_t in[3], const float 
 // ------------------------------------------------------------ diagnostics
 aps_status aps_device_status(unsigned int *bits, int clear) {
     if (!bits) return APS_ERR_NULL;
-    unsigned int *p = status_word();
-    if (!p) return APS_ERR_CUDA;
+    if (!status_word()) return APS_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);   // one snapshot at a time
     if (cudaDeviceSynchronize() != cudaSuccess) return APS_ERR_CUDA;
+    const cudaError_t e = launch_plain(status_exchange_kernel, dim3(1), dim3(1), 0,
+                                       (cudaStream_t)0, clear ? 1 : 0);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return APS_ERR_CUDA;
+    }
     unsigned int v = 0;
-    if (cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return APS_ERR_CUDA;
-    if (clear && cudaMemset(p, 0, sizeof(unsigned int)) != cudaSuccess) return APS_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(&v, g_status_snapshot, sizeof(v)) != cudaSuccess) return APS_ERR_CUDA;
     *bits = v;
     return APS_OK;
 }

@@ -29,18 +29,21 @@ bool encode_tiled(CUtensorMap *map, CUtensorMapDataType type, uint32_t rank, voi
                   const cuuint64_t *dims, const cuuint64_t *strides_bytes,
                   const cuuint32_t *box, const cuuint32_t *elem_strides);
 
-// Maps the last CUDA launch error to APS_OK / APS_ERR_LAUNCH.
-aps_status launch_status();
+// Maps the launch's own result to APS_OK / APS_ERR_LAUNCH.  A failed launch's
+// error is also taken off the runtime's last-error slot, so that the caller's
+// next cudaGetLastError does not report it again; a successful launch leaves
+// that slot (and any error the caller left in it) untouched.
+aps_status launch_status(cudaError_t launch_result);
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Launches `kern` on `st` as a programmatic dependent of the kernel before it
 // on the stream (the kernel calls pdl_wait before touching global memory), so
-// that its launch and on-chip setup overlap the previous kernel's tail.  The
-// launch error, if any, is left for launch_status.
+// that its launch and on-chip setup overlap the previous kernel's tail.
+// Returns the runtime's result for the launch itself.
 template <typename... P, typename... A>
-inline void launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                       A &&...args) {
+inline cudaError_t launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, A &&...args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
@@ -51,17 +54,32 @@ inline void launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, c
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaLaunchKernelEx(&cfg, kern, static_cast<P>(args)...);
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<P>(args)...);
+}
+
+// Plain launch (no programmatic dependency); returns the launch's own result.
+template <typename... P, typename... A>
+inline cudaError_t launch_plain(void (*kern)(P...), dim3 grid, dim3 block, size_t smem,
+                                cudaStream_t st, A &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = nullptr;
+    cfg.numAttrs = 0;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<P>(args)...);
 }
 
 // ------------------------------------------------------------ launchers
 // Each launcher assumes validated arguments and a non-empty output.
 
-// AvgPool3d k3/s2/p1, count_include_pad, floor mode; W % 4 == 0, x 16-byte and
-// y 8-byte aligned.  Returns APS_ERR_UNSUPPORTED if the tensor map cannot be
-// built (the caller then uses the direct kernel).
+// AvgPool3d k3/s2/p1, floor mode, count_include_pad on or off; W % 4 == 0, x
+// 16-byte and y 8-byte aligned.  Returns APS_ERR_UNSUPPORTED if the tensor map
+// cannot be built (the caller then uses the direct kernel).
 aps_status launch_avgpool3d_k3s2p1_tma(const float *x, const int64_t in[5], float *y,
-                                       const int64_t out[5], cudaStream_t st);
+                                       const int64_t out[5], int count_include_pad,
+                                       cudaStream_t st);
 
 aps_status launch_avgpool3d_direct(const float *x, const int64_t in[5], const int k[3],
                                    const int s[3], const int p[3], int count_include_pad,

@@ -30,6 +30,12 @@
 //    stored as one float2 (each warp writes 256 contiguous bytes).
 //  * The grid is persistent: one CTA per (SM x resident CTAs), tiles dealt
 //    round-robin, so the ring stays full across tile boundaries.
+//  * With count_include_pad off (CIP = false) the same sums are divided by
+//    the number of window cells inside the input instead (the page's "18 at a
+//    face": 27 inside, 18 / 12 / 8 on a face / edge / corner, fewer where the
+//    last window of an odd extent also reaches past the high end).  Per dim
+//    the count is 3, less one at output 0 and less one where 2i + 1 is past
+//    the end; a thread takes the reciprocals of its products once per tile.
 #include "aps_dev.cuh"
 #include "aps_internal.h"
 
@@ -49,10 +55,16 @@ constexpr int SMEM_BYTES = STAGES * STAGE_STRIDE + 2 * STAGES * 8;
 static_assert((BOX_W * 4) % 16 == 0, "TMA box rows must be a multiple of 16 bytes");
 }  // namespace pool
 
+// In-range cells of a k3 s2 p1 window at output i along a dim of input length L.
+__device__ __forceinline__ int k3s2p1_cells(int i, int L) {
+    return 3 - (i == 0 ? 1 : 0) - (2 * i + 1 >= L ? 1 : 0);
+}
+
+template <bool CIP>
 __global__ void __launch_bounds__(pool::THREADS)
     avgpool3d_k3s2p1_tma_kernel(const __grid_constant__ CUtensorMap xmap, float *__restrict__ y,
-                                int Do, int Ho, int Wo, int n_ht, int n_wt, long long n_units,
-                                unsigned int *status) {
+                                int D, int H, int W, int Do, int Ho, int Wo, int n_ht, int n_wt,
+                                long long n_units, unsigned int *status) {
     using namespace pool;
     extern __shared__ __align__(1024) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_STRIDE);
@@ -123,6 +135,17 @@ __global__ void __launch_bounds__(pool::THREADS)
         const bool active = oh < Ho && ow < Wo;
         float *yp = y + ((nc * Do) * Ho + oh) * (long long)Wo + ow;
         float carry0 = 0.f, carry1 = 0.f;   // window sums of input plane 2i-1
+        // CIP off: 1 / (cells in range) for the two columns, by the D count 1..3
+        float rdiv0[3], rdiv1[3];
+        if (!CIP) {
+            const int ch = k3s2p1_cells(oh, H);
+            const int c0 = ch * k3s2p1_cells(ow, W), c1 = ch * k3s2p1_cells(ow + 1, W);
+#pragma unroll
+            for (int cd = 1; cd <= 3; ++cd) {
+                rdiv0[cd - 1] = 1.0f / (float)(cd * c0);
+                rdiv1[cd - 1] = 1.0f / (float)(cd * c1);
+            }
+        }
         for (int od = 0; od < Do; ++od, ++it) {
             const uint32_t slot = it % STAGES;
             if (!mbar_wait(&full[slot], (it / STAGES) & 1u)) {
@@ -148,8 +171,14 @@ __global__ void __launch_bounds__(pool::THREADS)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
-            const float o0 = (carry0 + s0[0] + s0[1]) * inv27;
-            const float o1 = (carry1 + s1[0] + s1[1]) * inv27;
+            float r0 = inv27, r1 = inv27;
+            if (!CIP) {
+                const int cd = k3s2p1_cells(od, D);
+                r0 = cd == 3 ? rdiv0[2] : (cd == 2 ? rdiv0[1] : rdiv0[0]);
+                r1 = cd == 3 ? rdiv1[2] : (cd == 2 ? rdiv1[1] : rdiv1[0]);
+            }
+            const float o0 = (carry0 + s0[0] + s0[1]) * r0;
+            const float o1 = (carry1 + s1[0] + s1[1]) * r1;
             carry0 = s0[1];
             carry1 = s1[1];
             if (active) *reinterpret_cast<float2 *>(yp + od * plane_out) = make_float2(o0, o1);
@@ -158,7 +187,8 @@ __global__ void __launch_bounds__(pool::THREADS)
 }
 
 aps_status launch_avgpool3d_k3s2p1_tma(const float *x, const int64_t in[5], float *y,
-                                       const int64_t out[5], cudaStream_t st) {
+                                       const int64_t out[5], int count_include_pad,
+                                       cudaStream_t st) {
     using namespace pool;
     const int64_t N = in[0], C = in[1], D = in[2], H = in[3], W = in[4];
     const int64_t NC = N * C;
@@ -180,13 +210,15 @@ aps_status launch_avgpool3d_k3s2p1_tma(const float *x, const int64_t in[5], floa
     const int n_ht = (int)ceil_div(Ho, TH), n_wt = (int)ceil_div(Wo, TW);
     const long long n_units = (long long)NC * n_ht * n_wt;
 
-    const int per_sm = resident_ctas((const void *)avgpool3d_k3s2p1_tma_kernel, THREADS,
-                                     SMEM_BYTES);
+    const auto kern = count_include_pad ? avgpool3d_k3s2p1_tma_kernel<true>
+                                        : avgpool3d_k3s2p1_tma_kernel<false>;
+    const int per_sm = resident_ctas((const void *)kern, THREADS, SMEM_BYTES);
     if (per_sm < 1) return APS_ERR_CUDA;
     const long long grid = std::min<long long>(n_units, (long long)sm_count() * per_sm);
-    avgpool3d_k3s2p1_tma_kernel<<<(unsigned)grid, THREADS, SMEM_BYTES, st>>>(
-        map, y, Do, Ho, Wo, n_ht, n_wt, n_units, status_word());
-    return launch_status();
+    const cudaError_t e =
+        launch_plain(kern, dim3((unsigned)grid), dim3(THREADS), (size_t)SMEM_BYTES, st, map, y,
+                     (int)D, (int)H, (int)W, Do, Ho, Wo, n_ht, n_wt, n_units, status_word());
+    return launch_status(e);
 }
 
 // ------------------------------------------------------------ direct kernel
@@ -233,10 +265,11 @@ aps_status launch_avgpool3d_direct(const float *x, const int64_t in[5], const in
     const int threads = 256;
     const long long blocks =
         std::min<long long>(ceil_div(total, threads), (long long)sm_count() * 16);
-    avgpool3d_direct_kernel<<<(unsigned)blocks, threads, 0, st>>>(
-        x, y, total, (int)in[2], (int)in[3], (int)in[4], (int)out[2], (int)out[3], (int)out[4],
-        k[0], k[1], k[2], s[0], s[1], s[2], p[0], p[1], p[2], count_include_pad);
-    return launch_status();
+    const cudaError_t e = launch_plain(
+        avgpool3d_direct_kernel, dim3((unsigned)blocks), dim3(threads), 0, st, x, y, total,
+        (int)in[2], (int)in[3], (int)in[4], (int)out[2], (int)out[3], (int)out[4], k[0], k[1],
+        k[2], s[0], s[1], s[2], p[0], p[1], p[2], count_include_pad);
+    return launch_status(e);
 }
 
 }  // namespace aps

@@ -289,10 +289,10 @@ static aps_status launch_tiled(const float *x, const int64_t in[3], const float 
     if (per_sm < 1) return APS_ERR_CUDA;
     const long long slots = std::max<long long>(1, (long long)per_sm * sm_count() / gy);
     const long long gx = std::min<long long>(n_units, slots);
-    launch_pdl(kern, dim3((unsigned)gx, (unsigned)gy, 1), dim3(THREADS), (size_t)smem, st, x, w,
+    const cudaError_t e = launch_pdl(kern, dim3((unsigned)gx, (unsigned)gy, 1), dim3(THREADS), (size_t)smem, st, x, w,
                bias, y, (int)in[1], (int)c_out, (int)in[2], (int)l_out, (p - PL) / S, (int)n_mtiles,
                n_units, vec);
-    return launch_status();
+    return launch_status(e);
 }
 
 aps_status launch_convt1d_tiled(const float *x, const int64_t in[3], const float *w,
@@ -350,9 +350,9 @@ aps_status launch_convt1d_direct(const float *x, const int64_t in[3], const floa
     const int threads = 256;
     const long long blocks =
         std::min<long long>(ceil_div(total, threads), (long long)sm_count() * 16);
-    launch_pdl(convt1d_direct_kernel, dim3((unsigned)blocks), dim3(threads), 0, st, x, w, bias, y,
+    const cudaError_t e = launch_pdl(convt1d_direct_kernel, dim3((unsigned)blocks), dim3(threads), 0, st, x, w, bias, y,
                total, (int)in[1], (int)c_out, (int)in[2], (int)l_out, k, s, p, d);
-    return launch_status();
+    return launch_status(e);
 }
 
 }  // namespace aps

@@ -725,10 +725,10 @@ aps_status launch_convt1d_tf32(const float *x, const int64_t in[3], const float 
     const long long n_units = (long long)N * n_mtiles;
     const long long grid = std::min<long long>(n_units, (long long)sm_count());
     const int vec = (l_out % 4 == 0) && (reinterpret_cast<uintptr_t>(y) % 16 == 0);
-    launch_pdl(kern, dim3((unsigned)grid), dim3(THREADS), smem, st, map, ymap, w, bias, y, (int)Cin,
+    const cudaError_t e = launch_pdl(kern, dim3((unsigned)grid), dim3(THREADS), smem, st, map, ymap, w, bias, y, (int)Cin,
                (int)c_out, k, s, (int)l_out, n_mtiles, n_units, win0, BW, cols, nacc, RS, nbuf,
                dgroups, vec, tma_store, CKr, XTS, taps, status_word());
-    return launch_status();
+    return launch_status(e);
 }
 
 }  // namespace aps

@@ -299,10 +299,10 @@ aps_status launch_convt3d_k3s2p1(const float *x, const int64_t in[5], const floa
     const int per_sm = resident_ctas((const void *)convt3d_k3s2p1_kernel, THREADS, (int)smem);
     if (per_sm < 1) return APS_ERR_UNSUPPORTED;
     const long long grid = std::min<long long>((long long)per_sm * sm_count(), n_units);
-    launch_pdl(convt3d_k3s2p1_kernel, dim3((unsigned)grid), dim3(THREADS), smem, st, map, w, bias,
+    const cudaError_t e = launch_pdl(convt3d_k3s2p1_kernel, dim3((unsigned)grid), dim3(THREADS), smem, st, map, w, bias,
                y, (int)Cin, (int)D, (int)H, (int)W, (int)Do, (int)Ho, (int)Wo, WB, (int)n_mhb,
                (int)n_mwb, n_units, status_word());
-    return launch_status();
+    return launch_status(e);
 }
 
 // ------------------------------------------------------------ direct kernel
@@ -364,11 +364,11 @@ aps_status launch_convt3d_direct(const float *x, const int64_t in[5], const floa
     const int threads = 256;
     const long long blocks =
         std::min<long long>(ceil_div(total, threads), (long long)sm_count() * 16);
-    launch_pdl(convt3d_direct_kernel, dim3((unsigned)blocks), dim3(threads), 0, st, x, w, bias, y,
+    const cudaError_t e = launch_pdl(convt3d_direct_kernel, dim3((unsigned)blocks), dim3(threads), 0, st, x, w, bias, y,
                total, (int)in[1], (int)c_out, (int)in[2], (int)in[3], (int)in[4], (int)out[2],
                (int)out[3], (int)out[4], k[0], k[1], k[2], s[0], s[1], s[2], p[0], p[1], p[2], d[0],
                d[1], d[2]);
-    return launch_status();
+    return launch_status(e);
 }
 
 }  // namespace aps

@@ -395,9 +395,9 @@ aps_status launch_convt3d_tc(const float *x, const int64_t in[5], const float *w
     // one CTA per SM: each holds all 512 tensor-memory columns
     if (resident_ctas((const void *)kern, THREADS, (int)smem) < 1) return APS_ERR_UNSUPPORTED;
     const long long grid = std::min<long long>(sm_count(), n_units);
-    launch_pdl(kern, dim3((unsigned)grid), dim3(THREADS), smem, st, map, w, bias, y, (int)D, (int)H,
+    const cudaError_t e = launch_pdl(kern, dim3((unsigned)grid), dim3(THREADS), smem, st, map, w, bias, y, (int)D, (int)H,
                (int)W, BW, (int)Do, (int)Ho, (int)Wo, (int)n_mhb, n_units, status_word());
-    return launch_status();
+    return launch_status(e);
 }
 
 }  // namespace aps

@@ -353,10 +353,10 @@ aps_status launch_ct3d_pool2_fast(const float *x, const int64_t in[5], const flo
     const int per_sm = resident_ctas((const void *)kern, THREADS, (int)smem);
     if (per_sm < 1) return APS_ERR_UNSUPPORTED;
     const long long grid = std::min<long long>((long long)per_sm * sm_count(), n_units);
-    launch_pdl(kern, dim3((unsigned)grid), dim3(THREADS), smem, st, map, use_tma, x, w, conv_bias,
+    const cudaError_t e = launch_pdl(kern, dim3((unsigned)grid), dim3(THREADS), smem, st, map, use_tma, x, w, conv_bias,
                bias, scale1, scale2, y, (int)Cin, (int)D, (int)H, (int)W, BW, XR, RB, WB,
                (int)n_ohb, (int)n_owb, n_units, status_word());
-    return launch_status();
+    return launch_status(e);
 }
 
 // ------------------------------------------------------------ direct kernel
@@ -428,11 +428,11 @@ aps_status launch_ct3d_pool_direct(const float *x, const int64_t in[5], const fl
     const int threads = 256;
     const long long blocks =
         std::min<long long>(ceil_div(total, threads), (long long)sm_count() * 16);
-    launch_pdl(ct3d_pool_direct_kernel, dim3((unsigned)blocks), dim3(threads), 0, st, x, w,
+    const cudaError_t e = launch_pdl(ct3d_pool_direct_kernel, dim3((unsigned)blocks), dim3(threads), 0, st, x, w,
                conv_bias, bias, scale1, scale2, y, total, (int)in[1], (int)c_out, (int)in[2],
                (int)in[3], (int)in[4], (int)out[2], (int)out[3], (int)out[4], k[0], k[1], k[2],
                s[0], s[1], s[2], p[0], p[1], p[2], d[0], d[1], d[2], pool_k);
-    return launch_status();
+    return launch_status(e);
 }
 
 }  // namespace aps

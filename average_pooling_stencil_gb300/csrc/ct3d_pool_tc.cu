@@ -377,10 +377,10 @@ aps_status launch_ct3d_pool2_tc(const float *x, const int64_t in[5], const float
     // one CTA per SM: each holds all 512 tensor-memory columns
     if (resident_ctas((const void *)kern, THREADS, (int)smem) < 1) return APS_ERR_UNSUPPORTED;
     const long long grid = std::min<long long>(sm_count(), n_units);
-    launch_pdl(kern, dim3((unsigned)grid), dim3(THREADS), smem, st, map, w, conv_bias, bias,
+    const cudaError_t e = launch_pdl(kern, dim3((unsigned)grid), dim3(THREADS), smem, st, map, w, conv_bias, bias,
                scale1, scale2, y, (int)D, (int)H, (int)W, BW, XR, RB, WB, (int)n_ohb,
                (int)n_owb, n_units, status_word());
-    return launch_status();
+    return launch_status(e);
 }
 
 }  // namespace aps

@@ -55,9 +55,10 @@ extern "C" aps_status aps_fp32_fma_probe(int packed, int blocks, int iters, floa
     if (!sink) return APS_ERR_NULL;
     if (blocks < 1 || iters < 1 || blocks > (1 << 24)) return APS_ERR_SHAPE;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    if (packed)
-        fma_probe_packed_kernel<<<blocks, fp::THREADS, 0, cs>>>(sink, iters, 0.999f, 1e-3f);
-    else
-        fma_probe_scalar_kernel<<<blocks, fp::THREADS, 0, cs>>>(sink, iters, 0.999f, 1e-3f);
-    return launch_status();
+    const cudaError_t e =
+        packed ? launch_plain(fma_probe_packed_kernel, dim3(blocks), dim3(fp::THREADS), 0, cs,
+                              sink, iters, 0.999f, 1e-3f)
+               : launch_plain(fma_probe_scalar_kernel, dim3(blocks), dim3(fp::THREADS), 0, cs,
+                              sink, iters, 0.999f, 1e-3f);
+    return launch_status(e);
 }

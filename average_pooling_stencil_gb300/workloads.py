@@ -16,6 +16,16 @@ Each workload mirrors one task traced on the Kimi-K2.6 pages:
     workload's input, emitting the full [128,16,31,63,63] tensor.
 Initialiser bounds are the usual 1/sqrt(fan) uniform ones: fan = C_out*prod(k)
 for the transposed-conv weights (432 = 16*27, 320 = 64*5, 256 = 64*4).
+
+Variants that send the same ops down their other kernels (measured beside
+the workloads above):
+  * ``fused_cin8`` / ``convt3d_cin8`` -- the fused op and the standalone
+    ConvTranspose3d with 8 input channels (the FP32-pipe kernels).
+  * ``fused_op1``  -- the fused op with output_padding 1 (pre-pool
+    [32,64,64], pooled [16,32,32]): a geometry only the general kernel serves.
+  * ``avgpool_nopad`` -- the avgpool workload with count_include_pad off.
+  * ``avgpool_k2``    -- AvgPool3d(k2, s2, p0), the pool of l2_p50's chain,
+    alone on the avgpool workload's input (the general pool kernel).
 """
 from __future__ import annotations
 
@@ -60,28 +70,47 @@ def _u(b):
     return ("uniform", -b, b)
 
 
-def _fused(name, xshape, seed):
+def _fused(name, xshape, seed, out_pad=(0, 0, 0)):
     b = 1.0 / math.sqrt(432.0)
+    cin = xshape[1]
     return Workload(
         name, "ct3d_scale_pool_bias", seed,
         {
             "x": (tuple(xshape), ("uniform", -1.0, 1.0), STREAM_X),
-            "w": ((3, 16, 3, 3, 3), _u(b), STREAM_W),
+            "w": ((cin, 16, 3, 3, 3), _u(b), STREAM_W),
             "conv_bias": ((16,), _u(b), STREAM_CONV_BIAS),
             "bias": ((16,), ("normal", 0.02), STREAM_BIAS),
         },
-        dict(c_out=16, k=(3, 3, 3), stride=(2, 2, 2), pad=(1, 1, 1), out_pad=(0, 0, 0),
+        dict(c_out=16, k=(3, 3, 3), stride=(2, 2, 2), pad=(1, 1, 1), out_pad=tuple(out_pad),
              dil=(1, 1, 1), pool_k=2, scale1=0.5, scale2=1.0),
+    )
+
+
+def _convt3d(name, xshape, seed):
+    b = 1.0 / math.sqrt(432.0)
+    return Workload(
+        name, "convtranspose3d", seed,
+        {
+            "x": (tuple(xshape), ("uniform", -1.0, 1.0), STREAM_X),
+            "w": ((xshape[1], 16, 3, 3, 3), _u(b), STREAM_W),
+            "bias": ((16,), _u(b), STREAM_CONV_BIAS),
+        },
+        dict(c_out=16, k=(3, 3, 3), stride=(2, 2, 2), pad=(1, 1, 1), out_pad=(0, 0, 0),
+             dil=(1, 1, 1), has_bias=True),
+    )
+
+
+def _avgpool(name, k, s, p, cip):
+    return Workload(
+        name, "avgpool3d", 1,
+        {"x": ((16, 32, 128, 128, 256), ("normal", 1.0), STREAM_X)},
+        dict(k=k, stride=s, pad=p, count_include_pad=cip, ceil_mode=0),
     )
 
 
 WORKLOADS = {
     0: _fused("fused_tiny", (2, 3, 8, 16, 16), 0),
-    1: Workload(
-        "avgpool", "avgpool3d", 1,
-        {"x": ((16, 32, 128, 128, 256), ("normal", 1.0), STREAM_X)},
-        dict(k=(3, 3, 3), stride=(2, 2, 2), pad=(1, 1, 1), count_include_pad=1, ceil_mode=0),
-    ),
+    1: _avgpool("avgpool", (3, 3, 3), (2, 2, 2), (1, 1, 1), 1),
     2: _fused("fused", (128, 3, 16, 32, 32), 2),
     3: Workload(
         "convt1d", "convtranspose1d", 3,
@@ -100,16 +129,12 @@ WORKLOADS = {
         },
         dict(c_out=64, k=4, stride=2, pad=1, dil=2, out_pad=1, has_bias=True),
     ),
-    5: Workload(
-        "convt3d", "convtranspose3d", 5,
-        {
-            "x": ((128, 3, 16, 32, 32), ("uniform", -1.0, 1.0), STREAM_X),
-            "w": ((3, 16, 3, 3, 3), _u(1.0 / math.sqrt(432.0)), STREAM_W),
-            "bias": ((16,), _u(1.0 / math.sqrt(432.0)), STREAM_CONV_BIAS),
-        },
-        dict(c_out=16, k=(3, 3, 3), stride=(2, 2, 2), pad=(1, 1, 1), out_pad=(0, 0, 0),
-             dil=(1, 1, 1), has_bias=True),
-    ),
+    5: _convt3d("convt3d", (128, 3, 16, 32, 32), 5),
+    6: _fused("fused_cin8", (128, 8, 16, 32, 32), 6),
+    7: _fused("fused_op1", (128, 3, 16, 32, 32), 7, out_pad=(1, 1, 1)),
+    8: _avgpool("avgpool_nopad", (3, 3, 3), (2, 2, 2), (1, 1, 1), 0),
+    9: _avgpool("avgpool_k2", (2, 2, 2), (2, 2, 2), (0, 0, 0), 1),
+    10: _convt3d("convt3d_cin8", (128, 8, 16, 32, 32), 10),
 }
 
 

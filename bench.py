@@ -13,11 +13,13 @@ also carries:
     copies the input from pinned host memory, runs the op and reads the output
     back, all inside the timed region;
   * cpu_baseline -- the fp64 oracle on the host cores, on a bounded sample of
-    (n, c) planes of the same workload;
+    (n, c) planes of the same workload, with the CPU model and thread count;
   * clocks -- nvidia-smi samples taken during the timed region;
-  * per_config -- the other workloads (fused op tiny / full size, the two
-    ConvTranspose1d workloads in fp32 and tf32, the standalone ConvTranspose3d)
-    with outputs/s and their own roofline fraction.
+  * per_config (the last key, kept compact) -- every other workload and kernel
+    path: per entry the time per launch, outputs/s, the roofline (bound,
+    achieved, fraction of the binding peak, DRAM traffic per launch from the
+    committed ncu summary of that kernel's source) and the oracle's outputs/s
+    on a sample of the same workload on the host cores.
 
 `--impl reference` times the oracle itself (the only other leg that runs
 oracle code) on the same workload and prints the same line shape.
@@ -68,6 +70,10 @@ def parse_args_from(argv):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle sample")
+    ap.add_argument("--cpu-seconds-per-config", type=float, default=2.0,
+                    help="target CPU time of each per-config oracle sample")
+    ap.add_argument("--only", type=str, default=None,
+                    help="comma-separated per-config keys to run (default: all)")
     return ap.parse_args(argv)
 
 
@@ -150,20 +156,99 @@ class ClockSampler:
                 "samples": len(sel)}
 
 
-def traffic_from_profile(kernel_file, profile_name):
-    """Per-launch DRAM bytes recorded in profiles/<profile_name> for the kernel
-    source whose sha256 prefix is recorded beside it; None if absent or stale."""
+def traffic_from_profile(kernel_file, profile_name, key):
+    """DRAM bytes per launch of per-config workload `key`, recorded in
+    profiles/<profile_name> as `traffic_bytes_per_launch[key]: <bytes>` beside the
+    sha256 prefix of the kernel source it was measured on.  Returns the bytes,
+    "stale" when the source has changed since, or None when nothing is recorded."""
     prof = os.path.join(ROOT, "profiles", profile_name)
     src = os.path.join(ROOT, "average_pooling_stencil_gb300", "csrc", kernel_file)
     if not (os.path.exists(prof) and os.path.exists(src)):
         return None
     text = open(prof).read()
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m = re.search(r"traffic_bytes_per_launch\[" + re.escape(key) + r"\]:\s*([0-9.eE+]+)", text)
     h = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", text)
     if not (m and h):
         return None
     cur = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    return float(m.group(1)) if cur == h.group(1) else None
+    return float(m.group(1)) if cur == h.group(1) else "stale"
+
+
+# kernel source and committed ncu summary behind each measured workload (the
+# summary holds that kernel's DRAM bytes per launch, keyed by workload)
+PROFILE_OF = {
+    "avgpool": ("avgpool3d.cu", "avgpool3d_k3s2p1_tma.md"),
+    "avgpool_nopad": ("avgpool3d.cu", "avgpool3d_k3s2p1_tma.md"),
+    "avgpool_k2": ("avgpool3d.cu", "avgpool3d_direct_k2s2.md"),
+    "fused": ("ct3d_pool_tc.cu", "ct3d_pool2_tc_fused.md"),
+    "fused_cin8": ("ct3d_pool.cu", "ct3d_pool2_fast_fused_cin8.md"),
+    "fused_op1": ("ct3d_pool.cu", "ct3d_pool_direct_op1.md"),
+    "convt1d": ("convt1d.cu", "convt1d_tiled_fp32.md"),
+    "convt1d_strided": ("convt1d.cu", "convt1d_tiled_fp32.md"),
+    "convt1d_tf32": ("convt1d_tc.cu", "convt1d_tf32.md"),
+    "convt1d_strided_tf32": ("convt1d_tc.cu", "convt1d_tf32.md"),
+    "convt1d_tf32x3": ("convt1d_tc.cu", "convt1d_tf32x3.md"),
+    "convt1d_strided_tf32x3": ("convt1d_tc.cu", "convt1d_tf32x3.md"),
+    "convt3d": ("convt3d_tc.cu", "convt3d_tc_k3s2p1.md"),
+    "convt3d_cin8": ("convt3d.cu", "convt3d_k3s2p1_cin8.md"),
+}
+
+# per-config workloads: key, workload id, ConvTranspose1d precision, timing mode
+PER_CONFIG = [
+    ("fused_tiny", 0, 0, "graph"),
+    ("fused", 2, 0, "rotate"),
+    ("fused_cin8", 6, 0, "rotate"),
+    ("fused_op1", 7, 0, "rotate"),
+    ("avgpool_nopad", 8, 0, "plain"),
+    ("avgpool_k2", 9, 0, "plain"),
+    ("convt1d", 3, 0, "plain"),
+    ("convt1d_tf32", 3, 1, "plain"),
+    ("convt1d_tf32x3", 3, 2, "plain"),
+    ("convt1d_strided", 4, 0, "plain"),
+    ("convt1d_strided_tf32", 4, 1, "plain"),
+    ("convt1d_strided_tf32x3", 4, 2, "plain"),
+    ("convt3d", 5, 0, "plain"),
+    ("convt3d_cin8", 10, 0, "plain"),
+]
+
+
+def sig(v, n=4):
+    """`v` rounded to n significant digits (keeps the JSON line short)."""
+    if v is None or isinstance(v, str) or v == 0 or not math.isfinite(v):
+        return v
+    return float(f"{v:.{n}g}")
+
+
+def compact_json(obj):
+    """json.dumps without spaces, integer-valued floats of 7+ digits in exponent
+    form (4.426e11 rather than 442600000000.0): the line stays short enough that
+    the per-config block at its end survives a tail of a few KB."""
+    s = json.dumps(obj, separators=(",", ":"))
+
+    def exp(m):
+        import numpy as np   # shortest exact scientific form
+        t = np.format_float_scientific(float(m.group(2)), unique=True, trim="-")
+        return m.group(1) + t.replace("e+", "e")
+    return re.sub(r"([:\[,])(\d{7,})\.0(?=[,}\]])", exp, s)
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu model")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
 
 
 # --------------------------------------------------------------- workloads
@@ -171,15 +256,50 @@ def workload_desc(wl):
     shp = "x".join(map(str, wl.tensors["x"][0]))
     p = wl.params
     if wl.op == "avgpool3d":
-        return f"avgpool3d k3 s2 p1 count_include_pad x[{shp}] fp32"
+        g = "k{}{}{} s{}{}{} p{}{}{}".format(*p["k"], *p["stride"], *p["pad"])
+        g = re.sub(r"([kps])(\d)\2\2", r"\1\2", g)
+        cip = "count_include_pad" if p["count_include_pad"] else "count_include_pad=False"
+        return f"avgpool3d {g} {cip} x[{shp}] fp32"
     if wl.op == "ct3d_scale_pool_bias":
-        return (f"convtranspose3d(k3,s2,p1)+x{p['scale1']}+avgpool3d(2)+bias+x{p['scale2']} "
+        op = "" if not any(p["out_pad"]) else ",op{}".format(p["out_pad"][0])
+        return (f"convtranspose3d(k3,s2,p1{op})+x{p['scale1']}+avgpool3d(2)+bias+x{p['scale2']} "
                 f"x[{shp}] fp32")
     if wl.op == "convtranspose3d":
         return (f"convtranspose3d k3 s2 p1 d1 op0 x[{shp}] -> C_out {p['c_out']} "
                 f"(the pre-pool tensor) fp32")
     return (f"convtranspose1d K{p['k']} s{p['stride']} p{p['pad']} d{p['dil']} "
             f"op{p['out_pad']} x[{shp}] -> C_out {p['c_out']} fp32")
+
+
+def line_config(wl, ws):
+    """The `config` object of a bench line (the same for both arms)."""
+    in_bytes = 4 * numel(wl.tensors["x"][0])
+    return {"workload": workload_desc(wl), "seed": wl.seed,
+            "l2": (f"input larger than L2 ({in_bytes / 1e9:.2f} GB read per step), no flush"
+                   if in_bytes > 2 * 129e6 else "input may stay in L2 (small case)"),
+            "parallelism": f"replicas{ws}" if ws > 1 else "single GPU"}
+
+
+_HOST = {}
+
+
+def host_tensor(torch, wl, name, pin=False):
+    """The workload tensor `name` in (optionally pinned) host memory, generated once
+    per (seed, recipe, shape) in this process and shared by the cases that use it."""
+    shape, dist, stream = wl.tensors[name]
+    key = (wl.seed, stream, tuple(shape), tuple(dist))
+    h = _HOST.get(key)
+    if h is None or (pin and not h.is_pinned()):
+        h = torch.empty(shape, dtype=torch.float32, pin_memory=pin)
+        wl.generate(name, out=h.numpy())
+        _HOST[key] = h
+    return h
+
+
+def release_host(keep=()):
+    """Drops the cached host tensors other than `keep`."""
+    for k in [k for k, v in _HOST.items() if not any(v is t for t in keep)]:
+        del _HOST[k]
 
 
 class GpuCase:
@@ -199,26 +319,40 @@ class GpuCase:
         self.host = {}
         self.d = {}
         for n in names:
-            shape = wl.tensors[n][0]
-            pin = with_host and n == "x"
-            h = torch.empty(shape, dtype=torch.float32, pin_memory=pin)
-            wl.generate(n, out=h.numpy())
+            h = host_tensor(torch, wl, n, pin=with_host and n == "x")
             self.host[n] = h
             self.d[n] = h.to(dev, non_blocking=False)
         x = self.d["x"]
+        self.tc = False
+        self.tensor_passes = 0
         if wl.op == "avgpool3d":
             st, oshape = aps.binding.aps_avgpool3d_out_shape(x.shape, p["k"], p["stride"],
                                                              p["pad"], p["ceil_mode"])
-            self.flops = 27 * numel(oshape)
+            self.flops = numel(p["k"]) * numel(oshape)        # window adds
             self.bound = "hbm"
         elif wl.op == "ct3d_scale_pool_bias":
             st, oshape = aps.binding.aps_ct3d_scale_pool_bias_out_shape(
                 x.shape, p["c_out"], p["k"], p["stride"], p["pad"], p["out_pad"], p["dil"],
                 p["pool_k"])
-            self.flops = 2 * 8 * x.shape[1] * numel(oshape)   # 8 collapsed taps per ci
+            cin = x.shape[1]
+            fast = (tuple(p["k"]) == (3, 3, 3) and tuple(p["stride"]) == (2, 2, 2)
+                    and tuple(p["pad"]) == (1, 1, 1) and not any(p["out_pad"])
+                    and tuple(p["dil"]) == (1, 1, 1) and p["pool_k"] == 2
+                    and p["c_out"] == 16 and 1 <= cin <= 8)
+            if fast:
+                self.flops = 2 * 8 * cin * numel(oshape)      # 8 collapsed taps per ci
+            else:
+                # the literal chain: every in-range tap of every pre-pool output the
+                # pooled windows cover, then the window adds
+                pairs = 1
+                for i in range(3):
+                    pairs *= convt_pairs(x.shape[2 + i], oshape[2 + i] * p["pool_k"],
+                                         p["k"][i], p["stride"][i], p["pad"][i], p["dil"][i])
+                self.flops = (2 * x.shape[0] * cin * p["c_out"] * pairs
+                              + p["pool_k"] ** 3 * numel(oshape))
             # C_in <= 3 with 16-byte input rows runs on the tensor cores (3xTF32,
             # three MMA passes), bound by HBM; otherwise on the FP32 pipe
-            self.tc = x.shape[1] <= 3 and x.shape[4] % 4 == 0
+            self.tc = fast and cin <= 3 and x.shape[4] % 4 == 0
             self.tensor_passes = 3 if self.tc else 0
             self.bound = "hbm" if self.tc else "hbm+alu"
         elif wl.op == "convtranspose3d":
@@ -229,7 +363,9 @@ class GpuCase:
                 pairs *= convt_pairs(x.shape[2 + i], oshape[2 + i], p["k"][i], p["stride"][i],
                                      p["pad"][i], p["dil"][i])
             self.flops = 2 * x.shape[0] * x.shape[1] * p["c_out"] * pairs
-            self.bound = "hbm+alu"
+            self.tc = x.shape[1] <= 3 and x.shape[4] % 4 == 0 and x.shape[4] <= 32
+            self.tensor_passes = 3 if self.tc else 0
+            self.bound = "hbm" if self.tc else "hbm+alu"
         else:
             st, oshape = aps.binding.aps_convtranspose1d_out_shape(
                 x.shape, p["c_out"], p["k"], p["stride"], p["pad"], p["dil"], p["out_pad"])
@@ -471,22 +607,23 @@ def roofline_for(case, t, peaks, src, clock_mhz):
 
 
 # ------------------------------------------------------------------ oracle
-def oracle_sample(cfg, seconds, xhost=None):
+def oracle_sample(wl, seconds, host=None, whole=False):
     """Time the oracle (as it stands) on a bounded sample of output planes of
-    workload `cfg`, sized to about `seconds` of CPU time.  `xhost` is the
-    workload's input already in host memory (generated from the same seed if
-    None).  Returns (outputs/s, threads, description, outputs, seconds)."""
+    workload `wl`, sized to about `seconds` of CPU time (`whole`: every plane).
+    `host` maps tensor names to the workload's arrays already in host memory
+    (generated from the workload's seed if absent).  Returns (outputs/s,
+    threads, description, outputs, seconds)."""
     import numpy as np
 
     import oracle
-    from average_pooling_stencil_gb300 import workloads
-    wl = workloads.get(cfg)
     p = wl.params
     xs = tuple(wl.tensors["x"][0])
     N, C = xs[0], xs[1]
     threads = oracle.threads()
-    x = np.asarray(xhost).reshape(xs) if xhost is not None else wl.generate("x")
-    tens = {n: wl.generate(n) for n in wl.tensors if n != "x"}
+    host = host or {}
+    tens = {n: (np.asarray(host[n]).reshape(wl.tensors[n][0]) if n in host else wl.generate(n))
+            for n in wl.tensors}
+    x = tens["x"]
     if wl.op == "avgpool3d":
         units = [(n, c) for n in range(N) for c in range(C)]
 
@@ -508,12 +645,15 @@ def oracle_sample(cfg, seconds, xhost=None):
                 y = oracle.convt(x, tens["w"], tens.get("bias"), p["stride"], p["pad"], p["dil"],
                                  p["out_pad"], sel=planes)
             return time.perf_counter() - t0, y.size
-    # calibrate on one plane per thread, then size the sample to `seconds`
-    k = min(len(units), max(1, threads))
-    t, _ = run(units[:k])
-    m = int(min(len(units), max(k, round(seconds * k / max(t, 1e-6)))))
-    step = max(1, len(units) // m)
-    sample = units[::step][:m]
+    if whole:
+        sample = units
+    else:
+        # calibrate on one plane per thread, then size the sample to `seconds`
+        k = min(len(units), max(1, threads))
+        t, _ = run(units[:k])
+        m = int(min(len(units), max(k, round(seconds * k / max(t, 1e-6)))))
+        step = max(1, len(units) // m)
+        sample = units[::step][:m]
     t, cnt = run(sample)
     desc = f"{len(sample)} of {len(units)} (n, c) output planes of {workload_desc(wl)}"
     return cnt / t, threads, desc, cnt, t
@@ -559,10 +699,10 @@ def run_reference(args):
     x = wl.generate("x")
     per_step = max(1.0, min(args.cpu_seconds, 60.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
-        oracle_sample(HEADLINE_CFG, per_step, x)
+        oracle_sample(wl, per_step, {"x": x})
     vals, times, desc, threads = [], [], "", 1
     for _ in range(args.steps):
-        v, threads, desc, cnt, t = oracle_sample(HEADLINE_CFG, per_step, x)
+        v, threads, desc, cnt, t = oracle_sample(wl, per_step, {"x": x})
         vals.append(v)
         times.append(t)
     value = sum(times) and sum(v * t for v, t in zip(vals, times)) / sum(times)
@@ -571,15 +711,33 @@ def run_reference(args):
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * statistics.mean(times), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workload_desc(wl), "seed": wl.seed, "l2": "n/a (host)"},
+        "config": line_config(wl, ws),
         "cpu_baseline": {"value": value, "unit": "outputs/s", "cores": threads, "kind": "oracle",
-                         "sample": f"per step: {desc}"},
+                         "model": cpu_model(), "sample": f"per step: {desc}"},
         "e2e": {"value": value, "unit": "outputs/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
     print(json.dumps(line))
     return 0
+
+
+def per_config_entry(key, c, t, peaks, peak_src, cpu_out_s):
+    """One compact per_config entry: time, outputs/s, roofline, DRAM traffic per
+    launch (or "stale" / None) and the oracle's outputs/s on the host cores."""
+    r = roofline_for(c, t, peaks, peak_src, None)
+    src = PROFILE_OF.get(key)
+    e = {"us": sig(1e6 * t), "out_s": sig(c.outputs / t), "bound": r["bound"],
+         "achieved": sig(r["achieved"]), "unit": r["unit"], "frac": sig(r["frac"], 3),
+         "traffic": sig(traffic_from_profile(src[0], src[1], key), 3) if src else None,
+         "cpu_out_s": sig(cpu_out_s, 3)}
+    if c.bound == "hbm+alu":
+        e["tflops"] = sig(r["achieved_tflops"])
+    if "frac_of_measured_ceiling" in r:
+        e["frac_meas"] = sig(r["frac_of_measured_ceiling"], 3)
+    if "tensor_frac_of_ceiling" in r:
+        e["tc_frac"] = sig(r["tensor_frac_of_ceiling"], 3)
+    return e
 
 
 def run_native(args):
@@ -674,17 +832,21 @@ def run_native(args):
 
     clocks = sampler.summary(t_wall0, t_wall1)
     roof = roofline_for(case, per_launch, peaks, peak_src, clocks.get("sm_mhz"))
-    kernel_of = {"avgpool3d": ("avgpool3d.cu", "avgpool3d_k3s2p1_tma_kernel"),
-                 "ct3d_scale_pool_bias": (("ct3d_pool_tc.cu", "ct3d_pool2_tc_kernel")
-                                          if getattr(case, "tc", False)
-                                          else ("ct3d_pool.cu", "ct3d_pool2_fast_kernel")),
-                 "convtranspose3d": ("convt3d.cu", "convt3d_k3s2p1_kernel"),
-                 "convtranspose1d": (("convt1d_tc.cu", "convt1d_tf32_kernel") if case.precision
-                                     else ("convt1d.cu", "convt1d_tiled_kernel"))}[case.wl.op]
-    roof["kernel"] = kernel_of[1]
+    kernel_of = {"avgpool3d": "avgpool3d_k3s2p1_tma_kernel",
+                 "ct3d_scale_pool_bias": ("ct3d_pool2_tc_kernel" if case.tc
+                                          else "ct3d_pool2_fast_kernel"),
+                 "convtranspose3d": "convt3d_tc_kernel" if case.tc else "convt3d_k3s2p1_kernel",
+                 "convtranspose1d": ("convt1d_tf32_kernel" if case.precision
+                                     else "convt1d_tiled_kernel")}
+    roof["kernel"] = kernel_of[case.wl.op]
     roof["algorithmic_bytes_per_launch"] = case.bytes
-    roof["traffic"] = (traffic_from_profile(kernel_of[0], "avgpool3d_k3s2p1_tma.md")
-                       if args.workload == HEADLINE_CFG and x_shape is None else None)
+    hkey = case.wl.name + ("", "_tf32", "_tf32x3")[case.precision]
+    src = PROFILE_OF.get(hkey)
+    traffic = (traffic_from_profile(src[0], src[1], hkey)
+               if src is not None and x_shape is None else None)
+    roof["traffic"] = None if traffic == "stale" else traffic
+    if traffic == "stale":
+        roof["traffic_note"] = "kernel source changed since its ncu capture"
 
     st_code, bits = aps.binding.aps_device_status(clear=True)
     if st_code != 0 or bits != 0:
@@ -694,71 +856,87 @@ def run_native(args):
         "metric": METRIC, "value": value, "unit": "outputs/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_max / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic",
-        "config": {"workload": workload_desc(case.wl), "seed": case.wl.seed,
-                   "l2": (f"data larger than L2 ({case.bytes / 1e9:.2f} GB moved per step), no flush"
-                          if case.bytes > 2 * 129e6 else "input may stay in L2 (small case)"),
-                   "parallelism": f"replicas{ws}" if ws > 1 else "single GPU"},
+        "data": "synthetic", "config": line_config(case.wl, ws),
         "roofline": roof, "e2e": e2e, "gpu_launches": args.steps, "clocks": clocks,
-        "fma_ceilings_tflops": peaks["fma_measured"],
-        "tf32_gemm_ceiling_tflops": peaks["tf32_measured"],
+        "fma_ceilings_tflops": {k: sig(v) for k, v in peaks["fma_measured"].items()},
+        "tf32_gemm_ceiling_tflops": sig(peaks["tf32_measured"]),
     }
-    xhost = case.host["x"].numpy() if args.workload == HEADLINE_CFG and x_shape is None else None
+    headline_host = {"x": case.host["x"].numpy()} if x_shape is None else None
+    headline_wl = case.wl
     del case
     torch.cuda.empty_cache()
 
-    # ---- per-config breakdown (rank 0)
+    # ---- CPU baseline: the oracle on the host cores (rank 0, N = 1 only)
+    model = cpu_model()
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        v, threads, desc, cnt, t = oracle_sample(headline_wl, args.cpu_seconds, headline_host)
+        line["cpu_baseline"] = {"value": v, "unit": "outputs/s", "cores": threads,
+                                "kind": "oracle", "model": model, "sample": desc,
+                                "seconds": sig(t)}
+
+    # ---- per-config breakdown (rank 0), the last key of the line
     if rank == 0 and not args.no_per_config:
-        per = {}
+        import oracle
+        only = set(args.only.split(",")) if args.only else None
+        want_cpu = ws == 1 and not args.no_cpu_baseline
+        per = {"_peaks": {"hbm_GB_s": peaks["hbm_gbs"],
+                          "fp32_TF_s": sig(fp32_peak_tflops(float(peaks.get("sm_max_mhz",
+                                                                             2070.0)))),
+                          "fp32_meas_TF_s": sig(peaks["fma_measured"]["packed"]),
+                          "tf32_gemm_TF_s": sig(peaks["tf32_measured"])}}
+        if want_cpu:
+            per["_cpu"] = {"model": model, "threads": oracle.threads()}
         flush = torch.empty(64 * 1024 * 1024, device="cuda")   # 256 MB > L2
-        for cfg, prec in ((0, 0), (2, 0), (3, 0), (4, 0), (3, 1), (4, 1), (3, 2), (4, 2), (5, 0)):
+        cpu_of = {}                                               # oracle outputs/s per workload
+        for key, cfg, prec, mode in PER_CONFIG:
+            if only is not None and key not in only:
+                continue
             c = GpuCase(cfg, torch, aps, precision=prec)
             for _ in range(3):
                 c.launch()
             torch.cuda.synchronize()
-            if cfg == 0:
+            t_flushed = None
+            if mode == "graph":
                 t = time_graph(torch, c)
-                how = "CUDA graph of 100 launches x 20 replays (launch-latency bound)"
-            elif cfg == 2:
-                # steady state: 4 sets of buffers (4 x 143 MB, well above L2)
-                # launched back to back in rotation; and, for the cost of a
-                # single cold launch, one launch after a 256 MB flush
+            elif mode == "rotate":
+                # steady state over 4 sets of buffers launched back to back in
+                # rotation (their total is well above L2); and, for the fused op,
+                # one launch after a 256 MB flush
                 sets = [c] + [GpuCase(cfg, torch, aps, precision=prec) for _ in range(3)]
                 for o in sets[1:]:
                     o.launch()
                 torch.cuda.synchronize()
                 t = time_rotating(torch, sets, 40)
-                t_flushed = time_launches(torch, c, 30, flush)
+                if key == "fused":
+                    t_flushed = time_launches(torch, c, 30, flush)
                 del sets
-                how = ("40 back-to-back launches rotating over 4 buffer sets (573 MB, above L2); "
-                       "us_per_launch_after_flush: 30 single launches, 256 MB L2 flush before each")
-            elif cfg == 5:
-                t = time_launches(torch, c, 20)
-                how = "20 back-to-back launches (output 1.0 GB, larger than L2)"
             else:
                 t = time_launches(torch, c, 20)
-                how = "20 back-to-back launches (input larger than L2)"
-            per[c.wl.name + ("", "_tf32", "_tf32x3")[prec]] = {
-                "workload": workload_desc(c.wl) + ("", " (tf32 tensor cores)",
-                                                   " (3xTF32 tensor cores, fp32 accuracy)")[prec],
-                "outputs_per_s": c.outputs / t,
-                "us_per_launch": 1e6 * t, "gb_per_s": c.bytes / t / 1e9,
-                "tflop_per_s": c.flops / t / 1e12, "algorithmic_bytes": c.bytes,
-                "algorithmic_flops": c.flops,
-                "roofline": roofline_for(c, t, peaks, peak_src, None), "timing": how}
-            if cfg == 2:
-                per[c.wl.name]["us_per_launch_after_flush"] = 1e6 * t_flushed
+            if want_cpu and c.wl.name not in cpu_of:
+                host = {n: h.numpy() for n, h in c.host.items()}
+                cpu_of[c.wl.name] = oracle_sample(c.wl, args.cpu_seconds_per_config, host,
+                                                  whole=(mode == "graph"))[0]
+            e = per_config_entry(key, c, t, peaks, peak_src, cpu_of.get(c.wl.name))
+            if mode == "graph":
+                e.update(bound="launch", achieved=None, unit=None, frac=None)
+            if t_flushed is not None:
+                e["us_flush"] = sig(1e6 * t_flushed)
+            per[key] = e
+            if want_cpu and mode == "graph":
+                # the tiny workload on one host thread as well
+                oracle.set_threads(1)
+                try:
+                    _, _, _, cnt, t1 = oracle_sample(c.wl, 0, None, whole=True)
+                finally:
+                    oracle.set_threads(per["_cpu"]["threads"])
+                per["_cpu"][key + "_1thread_s"] = sig(t1)
+                per["_cpu"][key + "_1thread_out_s"] = sig(cnt / t1, 3)
             del c
             torch.cuda.empty_cache()
+        release_host()
         line["per_config"] = per
-
-    # ---- CPU baseline: the oracle on the host cores (rank 0, N = 1 only)
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        v, threads, desc, cnt, t = oracle_sample(HEADLINE_CFG, args.cpu_seconds, xhost)
-        line["cpu_baseline"] = {"value": v, "unit": "outputs/s", "cores": threads,
-                                "kind": "oracle", "sample": desc, "seconds": t}
     if rank == 0:
-        print(json.dumps(line))
+        print(compact_json(line))
     if dist:
         dist.barrier()
         dist.destroy_process_group()

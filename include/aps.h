@@ -45,6 +45,13 @@
  *    completed), so stream order holds exactly as for a plain launch.
  *  - Shape queries are pure host functions; they need no GPU and no CUDA
  *    context.
+ *  - Size limits of the launches (the shape queries accept larger shapes):
+ *    every channel count and every spatial size of the input and of the
+ *    output must be below 2^30 (for aps_ct3d_scale_pool_bias also pool_k
+ *    times each pooled size), and for aps_avgpool3d the product of the three
+ *    output spatial sizes below 2^31.  A larger request with elements returns
+ *    APS_ERR_UNSUPPORTED before any CUDA call; within them every valid
+ *    request runs (at APS_PREC_FP32 for aps_convtranspose1d).
  *  - Kernels contain no unbounded waits.  A pipeline wait that exceeds its
  *    time limit makes the kernel stop early and record APS_DEVERR_TIMEOUT in a
  *    per-device status word read by aps_device_status().
@@ -102,9 +109,9 @@ const char *aps_status_string(int status);
  *
  * x: [N, C, D, H, W] device fp32.  y: [N, C, Do, Ho, Wo] device fp32 (shape
  * from aps_avgpool3d_out_shape).  Requires k >= 1, s >= 1, 0 <= 2p <= k.
- * Fast path: k = 3, s = 2, p = 1 in all dims, count_include_pad, floor mode,
- * W % 4 == 0, x 16-byte and y 8-byte aligned (TMA-tiled kernel); every other
- * valid request runs a direct-window kernel.
+ * Fast path: k = 3, s = 2, p = 1 in all dims, floor mode, count_include_pad
+ * on or off, W % 4 == 0, x 16-byte and y 8-byte aligned (TMA-tiled kernel);
+ * every other valid request runs a direct-window kernel.
  */
 aps_status aps_avgpool3d_out_shape(const int64_t in_ncdhw[5], const int k[3],
                                    const int stride[3], const int pad[3],
@@ -197,7 +204,7 @@ aps_status aps_convtranspose3d(const float *x, const int64_t in_ncdhw[5], const 
  * and the weights (K*C_in*C_out*4 bytes, twice that for APS_PREC_TF32X3, which
  * also holds two copies of each converted stage and may stage 16 channels at a
  * time) plus the staging buffers fit in one CTA's 227 KB of shared memory.
- * APS_PREC_FP32 accepts every valid shape.
+ * APS_PREC_FP32 accepts every valid shape within the size limits above.
  */
 aps_status aps_convtranspose1d_out_shape(const int64_t in_ncl[3], int64_t c_out, int k,
                                          int stride, int pad, int dil, int out_pad,
@@ -211,7 +218,10 @@ aps_status aps_convtranspose1d(const float *x, const int64_t in_ncl[3], const fl
 /* ------------------------------------------------------------ diagnostics
  * Reads (and, if clear != 0, resets) the status word of the current device:
  * a bitwise OR of APS_DEVERR_* recorded by kernels since the last reset.
- * Synchronous: it waits for all prior work on the device.
+ * Synchronous: it waits for all prior work on the device, then reads and
+ * clears the word in one atomic step on the GPU (a one-thread kernel on the
+ * legacy default stream), so a bit that a kernel still running on another
+ * stream sets meanwhile is reported by this call or the next, never lost.
  */
 aps_status aps_device_status(unsigned int *bits, int clear);
 

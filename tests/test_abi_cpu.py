@@ -59,11 +59,14 @@ def test_printed_sizes_through_shape_queries():
 
 
 def test_workload_output_shapes():
-    """Output shapes of the six workloads (cfg 4 has 131076 outputs: the
+    """Output shapes of the workloads (cfg 4 has 131076 outputs: the
     closed form (65536-1)*2 - 2 + 2*3 + 1 + 1; cfg 5 is l2_p50's pre-pool
-    tensor, (16-1)*2 - 2 + 3 = 31 and (32-1)*2 - 2 + 3 = 63)."""
+    tensor, (16-1)*2 - 2 + 3 = 31 and (32-1)*2 - 2 + 3 = 63; cfg 7's
+    output_padding 1 makes the pre-pool sizes 32 and 64, pooled 16 and 32)."""
     want = {0: (2, 16, 7, 15, 15), 1: (16, 32, 64, 64, 128), 2: (128, 16, 15, 31, 31),
-            3: (32, 64, 131084), 4: (16, 64, 131076), 5: (128, 16, 31, 63, 63)}
+            3: (32, 64, 131084), 4: (16, 64, 131076), 5: (128, 16, 31, 63, 63),
+            6: (128, 16, 15, 31, 31), 7: (128, 16, 16, 32, 32), 8: (16, 32, 64, 64, 128),
+            9: (16, 32, 64, 64, 128), 10: (128, 16, 31, 63, 63)}
     for cfg, shape in want.items():
         wl = workloads.get(cfg)
         p = wl.params
@@ -181,3 +184,27 @@ def test_convtranspose3d_shape_query_matches_closed_form_and_rejects_bad_params(
     st = B.aps_convtranspose3d(0, (1, 1, 4, 4, 4), 0, 0, 2, (3, 3, 3), (2, 2, 2), (1, 1, 1),
                                (1, 1, 1), (0, 0, 0), 0)
     assert st == B.APS_ERR_NULL
+
+
+def test_extents_beyond_the_launch_limits_are_unsupported_before_any_cuda_call():
+    """Channel counts and spatial sizes of 2^30 or more (and an avgpool output plane of
+    2^31 cells or more) are valid shapes the launches decline: APS_ERR_UNSUPPORTED, decided
+    on the host (this machine has no GPU, so any CUDA call would fail differently)."""
+    U = B.APS_ERR_UNSUPPORTED
+    big = 1 << 30
+    assert B.aps_avgpool3d(FAKE, (1, 1, 4, 4, big), 3, 2, 1, 1, 0, FAKE) == U
+    # each output size below 2^30, but 2^31 cells in a plane
+    assert B.aps_avgpool3d(FAKE, (1, 1, 2, 1 << 16, 1 << 16), 1, 1, 0, 1, 0, FAKE) == U
+    # W = 2^29 + 1: pre-pool width 2^30 + 1, pooled width 2^29 (pool_k times it is 2^30)
+    assert B.aps_ct3d_scale_pool_bias(FAKE, (1, 3, 4, 4, big // 2 + 1), FAKE, 0, FAKE, 16, 3,
+                                      2, 1, 0, 1, 2, 0.5, 1.0, FAKE) == U
+    assert B.aps_convtranspose3d(FAKE, (1, 1, 4, 4, big // 2 + 1), FAKE, 0, 2, (3, 3, 3), (2, 2, 2),
+                                 (1, 1, 1), (1, 1, 1), (0, 0, 0), FAKE) == U
+    for prec in (0, 1, 2):
+        assert B.aps_convtranspose1d(FAKE, (1, 2, big), FAKE, 0, 4, 3, 1, 0, 1, 0, prec,
+                                     FAKE) == U
+        assert B.aps_convtranspose1d(FAKE, (1, big, 8), FAKE, 0, 4, 3, 1, 0, 1, 0, prec,
+                                     FAKE) == U
+    # the shape queries still answer for such shapes
+    st, out = B.aps_convtranspose1d_out_shape((1, 2, big), 4, 3, 1, 0, 1, 0)
+    assert st == 0 and out == (1, 4, big + 2)

@@ -67,8 +67,8 @@ def test_mixed_bound_takes_the_larger_floor():
 
 
 def test_profile_traffic_is_used_only_for_the_profiled_source(tmp_path, monkeypatch):
-    """bench.py quotes a kernel's DRAM traffic from its profile summary only while the
-    kernel's source still has the hash recorded beside it."""
+    """bench.py quotes a kernel's DRAM traffic per workload from its profile summary only
+    while the kernel's source still has the hash recorded beside it."""
     import hashlib
     csrc = tmp_path / "average_pooling_stencil_gb300" / "csrc"
     prof = tmp_path / "profiles"
@@ -77,9 +77,48 @@ def test_profile_traffic_is_used_only_for_the_profiled_source(tmp_path, monkeypa
     src = csrc / "k.cu"
     src.write_text("__global__ void k() {}\n")
     sha = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
-    (prof / "k.md").write_text(f"source_sha256_16: {sha}\ntraffic_bytes_per_launch: 1.25e+09\n")
+    (prof / "k.md").write_text(f"source_sha256_16: {sha}\n"
+                               "traffic_bytes_per_launch[wa]: 1.25e+09\n"
+                               "traffic_bytes_per_launch[wb]: 3.5e8\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.traffic_from_profile("k.cu", "k.md") == pytest.approx(1.25e9)
+    assert bench.traffic_from_profile("k.cu", "k.md", "wa") == pytest.approx(1.25e9)
+    assert bench.traffic_from_profile("k.cu", "k.md", "wb") == pytest.approx(3.5e8)
+    assert bench.traffic_from_profile("k.cu", "k.md", "wc") is None
     src.write_text("__global__ void k() { }\n")            # the kernel changed
-    assert bench.traffic_from_profile("k.cu", "k.md") is None
-    assert bench.traffic_from_profile("k.cu", "missing.md") is None
+    assert bench.traffic_from_profile("k.cu", "k.md", "wa") == "stale"
+    assert bench.traffic_from_profile("k.cu", "missing.md", "wa") is None
+
+
+def test_every_measured_workload_names_a_kernel_source_and_profile():
+    csrc = os.path.join(ROOT, "average_pooling_stencil_gb300", "csrc")
+    for key, cfg, prec, mode in bench.PER_CONFIG:
+        if mode == "graph":
+            continue                      # launch-latency bound: no traffic figure
+        src, _ = bench.PROFILE_OF[key]
+        assert os.path.exists(os.path.join(csrc, src)), key
+
+
+def test_compact_json_round_trips_and_keeps_the_per_config_block_short():
+    import json
+    v = {"a": 442600000000.0, "b": [1610000000.0, 2.5], "c": 1234567.0, "d": 12345678.9,
+         "e": 8589934592, "f": 194987777516.0, "g": None, "h": "x1.0,2"}
+    s = bench.compact_json(v)
+    assert json.loads(s) == v
+    assert "4.426e11" in s and " " not in s.replace("x1.0,2", "")
+    per = {}
+    for key, cfg, prec, mode in bench.PER_CONFIG:
+        c = SimpleNamespace(bytes=1_611_000_000, flops=85_899_345_920, outputs=134_234_112,
+                            bound="alu" if prec == 0 else "hbm", tensor_passes=prec and 3)
+        per[key] = bench.per_config_entry(key, c, 303.3e-6, PEAKS, "measured", 2.1e7)
+    # the driver keeps a few KB of the line's tail; the whole block must fit in it
+    assert len(bench.compact_json({"per_config": per})) < 2800
+
+
+def test_both_arms_print_the_same_config():
+    from average_pooling_stencil_gb300 import workloads
+    wl = workloads.get(bench.HEADLINE_CFG)
+    a, b = bench.line_config(wl, 1), bench.line_config(wl, 1)
+    assert a == b and set(a) == {"workload", "seed", "l2", "parallelism"}
+    assert a["workload"] == "avgpool3d k3 s2 p1 count_include_pad x[16x32x128x128x256] fp32"
+    assert "avgpool3d k2 s2 p0 count_include_pad x" in bench.workload_desc(workloads.get(9))
+    assert "count_include_pad=False" in bench.workload_desc(workloads.get(8))

@@ -58,11 +58,15 @@ FAST_POOL_SHAPES = [(2, 3, 9, 20, 68), (1, 2, 4, 17, 132), (1, 1, 2, 2, 4), (3, 
                     (1, 1, 1, 1, 4), (2, 1, 3, 33, 260), (1, 3, 6, 16, 256)]
 
 
+@pytest.mark.parametrize("cip", [1, 0])
 @pytest.mark.parametrize("shape", FAST_POOL_SHAPES)
-def test_avgpool_k3s2p1_tma_path(shape):
+def test_avgpool_k3s2p1_tma_path(shape, cip):
+    """The TMA kernel, count_include_pad on (divisor 27) and off (divisor = cells in
+    range: odd extents also clip the last window at the high end)."""
     x = workloads.get(1).with_input_shape(shape).generate("x")
-    y = B.avgpool3d(dev(x), 3, 2, 1)
-    assert_close(y.cpu().numpy(), ora.avgpool3d(x, 3, 2, 1, 1, 0), what=f"avgpool {shape}")
+    y = B.avgpool3d(dev(x), 3, 2, 1, bool(cip))
+    assert_close(y.cpu().numpy(), ora.avgpool3d(x, 3, 2, 1, cip, 0),
+                 what=f"avgpool {shape} cip {cip}")
 
 
 @pytest.mark.parametrize("shape", [(2, 3, 9, 20, 67), (1, 1, 5, 6, 7), (1, 2, 3, 3, 2)])
@@ -99,20 +103,31 @@ def test_avgpool_repeatable_bitwise():
     assert torch.equal(a, b)
 
 
+_FULL_POOL_X = {}
+
+
+# the avgpool workload (cfg 1), the same input with count_include_pad off (cfg 8) and
+# AvgPool3d(k2, s2) on it (cfg 9, the general kernel), as the bench launches them
 @pytest.mark.slow
-def test_avgpool_full_workload_sampled_planes():
-    wl = workloads.get(1)
-    x = wl.generate("x")                                   # [16,32,128,128,256], 8.6 GB
+@pytest.mark.parametrize("cfg", [1, 8, 9])
+def test_avgpool_full_workload_sampled_planes(cfg):
+    wl = workloads.get(cfg)
+    p = wl.params
+    if "x" not in _FULL_POOL_X:
+        _FULL_POOL_X["x"] = wl.generate("x")               # [16,32,128,128,256], 8.6 GB
+    x = _FULL_POOL_X["x"]
     xd = dev(x)
-    y = B.avgpool3d(xd, 3, 2, 1)
+    y = B.avgpool3d(xd, p["k"], p["stride"], p["pad"], bool(p["count_include_pad"]))
     torch.cuda.synchronize()
     sel = [(0, 0), (0, 31), (7, 13), (15, 0), (15, 31), (9, 22)]
-    ref = ora.avgpool3d(x, 3, 2, 1, 1, 0, sel=sel)
+    ref = ora.avgpool3d(x, p["k"], p["stride"], p["pad"], p["count_include_pad"], 0, sel=sel)
     got = np.stack([y[n, c].cpu().numpy() for n, c in sel])
-    assert_close(got, ref, what="avgpool full workload")
+    assert_close(got, ref, what=f"avgpool full workload cfg {cfg}")
     assert torch.isfinite(y).all()
     del xd, y
     torch.cuda.empty_cache()
+    if cfg == 9:
+        _FULL_POOL_X.clear()
 
 
 # ------------------------------------------------------- ct3d_scale_pool_bias
@@ -128,7 +143,9 @@ def fused_gpu(x, w, cb, b, p):
                                   p["scale1"], p["scale2"]).cpu().numpy()
 
 
-@pytest.mark.parametrize("cfg", [0, 2])
+# the tiny and full workloads, and the full one with 8 input channels (the FP32-pipe
+# kernel, cfg 6) and with output_padding 1 (the general kernel, cfg 7)
+@pytest.mark.parametrize("cfg", [0, 2, 6, 7])
 def test_fused_workloads_all_outputs(cfg):
     wl = workloads.get(cfg)
     x, w, cb, b = (wl.generate(n) for n in ("x", "w", "conv_bias", "bias"))
@@ -261,8 +278,9 @@ def test_convt3d_unaligned_input_takes_the_direct_kernel():
                  what="convt3d unaligned x")
 
 
-def test_convt3d_full_workload_sampled_planes():
-    wl = workloads.get(5)
+@pytest.mark.parametrize("cfg", [5, 10])
+def test_convt3d_full_workload_sampled_planes(cfg):
+    wl = workloads.get(cfg)
     p = wl.params
     x, w, b = wl.generate("x"), wl.generate("w"), wl.generate("bias")
     y = B.convtranspose3d(dev(x), dev(w), dev(b), p["stride"], p["pad"], p["dil"], p["out_pad"])
@@ -271,7 +289,7 @@ def test_convt3d_full_workload_sampled_planes():
     sel = [(0, 0), (N - 1, C - 1), (N // 2, 7), (5, 12)]
     ref = ora.convt(x, w, b, p["stride"], p["pad"], p["dil"], p["out_pad"], sel=sel)
     got = np.stack([y[n, c].cpu().numpy() for n, c in sel])
-    assert_close(got, ref, what="convt3d full workload")
+    assert_close(got, ref, what=f"convt3d full workload cfg {cfg}")
     assert torch.isfinite(y).all()
 
 
