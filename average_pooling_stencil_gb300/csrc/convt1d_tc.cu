@@ -75,6 +75,12 @@ constexpr int EPI_WARPS = 8;      // two epilogue groups of four warps: 4..7 and
 constexpr int MAX_MMA_TAB = 256;  // (chunk, class, tap, k-step) entries of one tile
 constexpr int W_PRODUCER = 0, W_MMA = 1, W_EPI0 = 4;
 
+// Operand forms of the kernel: plain tf32; 3xTF32 with three C_out-wide MMAs per
+// product; 3xTF32 with the hi and lo weights side by side in one 2*C_out-wide B (two
+// MMAs per product: M128 N2C_out K8 + M128 N_Cout K8 instead of three M128 N_Cout K8,
+// 64 + 48 cycles against 3 x 48 at C_out = 64).
+constexpr int MODE_TF32 = 0, MODE_X3 = 1, MODE_X3_PAIRED = 2;
+
 struct Taps {
     int nclass;                        // classes (output residues) with taps
     int cls_r[MAX_CLASSES];            // residue of each such class
@@ -100,17 +106,23 @@ using namespace tc;   // named_bar, to_tf32, umma_*, tc_fence_*, tmem_ld*
 // (16 entries) keeps the loop: fully unrolled it was 1.5 % (TF32) and 2 % (3xTF32)
 // slower, and 8 per turn for 3xTF32 was 276 against 302 us in one comparison but 312 in
 // the bench.  NE == 0: any count, 4 (TF32) or 2 (3xTF32) per turn.
-template <int NE, int UNROLL, bool SPLIT>
+// MODE: MODE_TF32, MODE_X3 (three C_out-wide MMAs per entry) or MODE_X3_PAIRED (hi and lo
+// weights side by side as one 2*C_out-wide B: hi(x) [hi(w) | lo(w)], then lo(x) hi(w)).
+// `acc_cols`: accumulator columns per class (C_out, or 2*C_out when paired).
+template <int NE, int UNROLL, int MODE>
 __device__ __forceinline__ void issue_chunk(const uint32_t *tab_a, const uint64_t *bt, int n_ent,
-                                            uint64_t abase, uint32_t dbase, uint32_t cout,
-                                            uint32_t idesc, bool first_chunk, uint32_t a_lo,
-                                            uint32_t b_lo) {
+                                            uint64_t abase, uint32_t dbase, uint32_t acc_cols,
+                                            uint32_t idesc, uint32_t idesc_pair, bool first_chunk,
+                                            uint32_t a_lo, uint32_t b_lo) {
     auto one = [&](int e) {
         const uint32_t ae = tab_a[e];
         const uint32_t acc = (!first_chunk || !(ae >> 31)) ? 1u : 0u;
-        const uint32_t d = dbase + ((ae >> 16) & 0xFFu) * cout;
+        const uint32_t d = dbase + ((ae >> 16) & 0xFFu) * acc_cols;
         const uint64_t a = abase + (ae & 0xFFFFu), bw = bt[e];
-        if (SPLIT) {
+        if (MODE == MODE_X3_PAIRED) {
+            umma_tf32(d, a, bw, idesc_pair, acc);     // hi(x) [hi(w) | lo(w)]
+            umma_tf32(d, a + a_lo, bw, idesc, 1u);    // lo(x) hi(w)
+        } else if (MODE == MODE_X3) {
             umma_tf32(d, a + a_lo, bw, idesc, acc);   // lo(x) hi(w)
             umma_tf32(d, a, bw + b_lo, idesc, 1u);    // hi(x) lo(w)
             umma_tf32(d, a, bw, idesc, 1u);           // hi(x) hi(w)
@@ -121,7 +133,7 @@ __device__ __forceinline__ void issue_chunk(const uint32_t *tab_a, const uint64_
     if constexpr (NE > 0) {
 #pragma unroll UNROLL
         for (int e = 0; e < NE; ++e) one(e);
-    } else if constexpr (SPLIT) {
+    } else if constexpr (MODE != MODE_TF32) {
 #pragma unroll 2
         for (int e = 0; e < n_ent; ++e) one(e);
     } else {
@@ -131,8 +143,8 @@ __device__ __forceinline__ void issue_chunk(const uint32_t *tab_a, const uint64_
 }
 }  // namespace tc1
 
-// SPLIT: 3xTF32 (operands split into tf32 hi + lo, three MMAs per product).
-template <bool SPLIT>
+// MODE != MODE_TF32: 3xTF32 (operands split into tf32 hi + lo).
+template <int MODE>
 __global__ void __launch_bounds__(tc1::THREADS, 1)
     convt1d_tf32_kernel(const __grid_constant__ CUtensorMap xmap,
                         const __grid_constant__ CUtensorMap ymap, const float *__restrict__ w,
@@ -144,7 +156,11 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
     pdl_trigger();
     pdl_wait();
     using namespace tc1;
-    constexpr bool split = SPLIT;
+    constexpr bool split = MODE != tc1::MODE_TF32;
+    constexpr bool paired = MODE == tc1::MODE_X3_PAIRED;
+    // accumulator columns per class: the paired form keeps hi(w) and lo(w) products in
+    // two halves, summed by the epilogue
+    const uint32_t acc_cols = (uint32_t)Cout * (paired ? 2u : 1u);
     extern __shared__ __align__(1024) unsigned char smem[];
     // CKr: channels per chunk; XTS: converted-operand stages.  split: operands
     // are split as v = hi + lo (both tf32) and each product is accumulated as
@@ -160,8 +176,10 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
     const uint32_t RAW_STRIDE = (RAW_BYTES + 1023) & ~1023u;
     unsigned char *xt = smem;
     unsigned char *raw = xt + XTS * XT_STRIDE;
-    float *wt = reinterpret_cast<float *>(raw + RS * RAW_STRIDE);   // [K][Cin/4][Cout][4] (x2)
-    const uint32_t W_LO = split ? (uint32_t)K * Cin * Cout * 4u : 0u;
+    // weights: [K][Cin/4][Cout][4] (hi; the 3xTF32 lo copy W_LO bytes after it), or,
+    // paired, [K][Cin/4][hi, lo][Cout][4]
+    float *wt = reinterpret_cast<float *>(raw + RS * RAW_STRIDE);
+    const uint32_t W_LO = (split && !paired) ? (uint32_t)K * Cin * Cout * 4u : 0u;
     float *bs = wt + (size_t)K * Cin * Cout * (split ? 2 : 1);
     const int OROW = BM * S + 4;                   // staged output row (one channel)
     const int SLAB = S == 1 ? 32 : 16;             // channels per TMA-stored slab
@@ -228,15 +246,23 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
             const int ci = cb * 4 + j;
             const float v = __ldg(w + ((size_t)ci * Cout + co) * K + k);
             const uint32_t hi = to_tf32(v);
-            wtu[e] = hi;
-            if (split) wtu[total + e] = to_tf32(v - __uint_as_float(hi));
+            if (paired) {
+                // block (k, cb) holds Cout hi rows, then Cout lo rows
+                const int blk = (e >> 2) / Cout;   // k * (Cin / 4) + cb
+                const int at = blk * 2 * Cout * 4 + co * 4 + j;
+                wtu[at] = hi;
+                wtu[at + Cout * 4] = to_tf32(v - __uint_as_float(hi));
+            } else {
+                wtu[e] = hi;
+                if (split) wtu[total + e] = to_tf32(v - __uint_as_float(hi));
+            }
         }
         for (int c = threadIdx.x; c < Cout; c += THREADS) bs[c] = bias ? __ldg(bias + c) : 0.f;
     }
     int n_ent = 0;   // MMAs per chunk
     for (int c = 0; c < taps.nclass; ++c) n_ent += taps.ntaps[c] * (CKr / 8);
     if (warp == W_MMA && lane == 0) {
-        const uint32_t LBO_W = (uint32_t)Cout * 16;
+        const uint32_t LBO_W = (uint32_t)Cout * 16 * (paired ? 2u : 1u);
         const uint32_t wt_addr = smem_u32(wt);
         int e = 0;
         for (int c = 0; c < taps.nclass; ++c)
@@ -300,8 +326,8 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
     } else if (warp == W_MMA) {
         // ------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = (1u << 4) | (2u << 7) | (2u << 10) |
-                                   ((uint32_t)(Cout >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+            const uint32_t idesc = tc::idesc_tf32(BM, Cout);
+            const uint32_t idesc_pair = tc::idesc_tf32(BM, 2 * Cout);   // paired form only
             uint64_t a_stage[XT_STAGES];
             for (int st = 0; st < XT_STAGES; ++st)
                 a_stage[st] = tc1::umma_desc(smem_u32(xt) + st * XT_STRIDE, LBO_X, 128);
@@ -319,7 +345,7 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
                     break;
                 }
                 tc1::tc_fence_after();
-                const uint32_t dbase = tmem_base + b * taps.nclass * (uint32_t)Cout;
+                const uint32_t dbase = tmem_base + b * taps.nclass * acc_cols;
                 bool fail = false;
                 for (int ch = 0; ch < nchunks; ++ch) {
                     const uint32_t s = xs_i;
@@ -334,12 +360,11 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
                     const uint64_t *bt = tab_b + ch * n_ent;
                     // 20 entries: the stride-1 K5 geometry at 32-channel chunks
                     if (n_ent == 20)
-                        tc1::issue_chunk<20, 20, split>(tab_a, bt, n_ent, abase, dbase,
-                                                        (uint32_t)Cout, idesc, ch == 0, a_lo,
-                                                        b_lo);
+                        tc1::issue_chunk<20, 20, MODE>(tab_a, bt, n_ent, abase, dbase, acc_cols,
+                                                       idesc, idesc_pair, ch == 0, a_lo, b_lo);
                     else
-                        tc1::issue_chunk<0, 1, split>(tab_a, bt, n_ent, abase, dbase,
-                                                      (uint32_t)Cout, idesc, ch == 0, a_lo, b_lo);
+                        tc1::issue_chunk<0, 1, MODE>(tab_a, bt, n_ent, abase, dbase, acc_cols,
+                                                     idesc, idesc_pair, ch == 0, a_lo, b_lo);
                     issued = true;
                     tc1::umma_commit(&xt_empty[s]);
                     if (++xs_i == (uint32_t)XTS) {
@@ -411,12 +436,20 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
                     named_bar(bar_id, 128);
                     for (int c = 0; c < taps.nclass; ++c) {
                         const uint32_t col = tmem_base + ((uint32_t)(q * 32) << 16) +
-                                             (b * taps.nclass + c) * (uint32_t)Cout + c0;
+                                             (b * taps.nclass + c) * acc_cols + c0;
                         float *dst = st_buf + S * row + taps.cls_r[c];
                         const float4 *b4 = reinterpret_cast<const float4 *>(bs + c0);
                         if (SLAB == 32) {
                             uint32_t r[32];
                             tc1::tmem_ld32(col, r);
+                            if (paired) {   // + the lo(w) half
+                                uint32_t r2[32];
+                                tc1::tmem_ld32(col + (uint32_t)Cout, r2);
+#pragma unroll
+                                for (int j = 0; j < 32; ++j)
+                                    r[j] = __float_as_uint(__uint_as_float(r[j]) +
+                                                           __uint_as_float(r2[j]));
+                            }
 #pragma unroll
                             for (int j = 0; j < 32; j += 4) {
                                 const float4 bv = b4[j / 4];
@@ -428,6 +461,14 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
                         } else {
                             uint32_t r[16];
                             tc1::tmem_ld16(col, r);
+                            if (paired) {   // + the lo(w) half
+                                uint32_t r2[16];
+                                tc1::tmem_ld16(col + (uint32_t)Cout, r2);
+#pragma unroll
+                                for (int j = 0; j < 16; ++j)
+                                    r[j] = __float_as_uint(__uint_as_float(r[j]) +
+                                                           __uint_as_float(r2[j]));
+                            }
 #pragma unroll
                             for (int j = 0; j < 16; j += 4) {
                                 const float4 bv = b4[j / 4];
@@ -462,9 +503,16 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
                 const int c0 = i * 32;
                 for (int c = 0; c < taps.nclass; ++c) {
                     uint32_t r[32];
-                    tc1::tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) +
-                                       (b * taps.nclass + c) * (uint32_t)Cout + c0,
-                                   r);
+                    const uint32_t col = tmem_base + ((uint32_t)(q * 32) << 16) +
+                                         (b * taps.nclass + c) * acc_cols + c0;
+                    tc1::tmem_ld32(col, r);
+                    if (paired) {   // + the lo(w) half
+                        uint32_t r2[32];
+                        tc1::tmem_ld32(col + (uint32_t)Cout, r2);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(r2[j]));
+                    }
                     float *dst = gst + S * row + taps.cls_r[c];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) dst[j * OROW] = __uint_as_float(r[j]) + bs[c0 + j];
@@ -637,12 +685,16 @@ aps_status launch_convt1d_tf32(const float *x, const int64_t in[3], const float 
     if (BW > 256) return APS_ERR_UNSUPPORTED;
     for (int c = 0; c < taps.nclass; ++c)
         for (int t = 0; t < taps.ntaps[c]; ++t) taps.tap_row[c][t] = ph + ce[c][t] - win0;
+    // 3xTF32 pairs the hi and lo weights in one 2*C_out-wide MMA where that width is a
+    // valid N (<= 256) and two accumulator sets still fit; otherwise three MMAs
+    const bool paired = split && 2 * c_out <= 256 && taps.nclass * 4 * (int)c_out <= 512;
+    const int acc_cols = (int)c_out * (paired ? 2 : 1);
     // as many accumulator buffers as fit in the 512 tensor-memory columns (>= 2)
-    int nacc = 512 / (taps.nclass * (int)c_out);
+    int nacc = 512 / (taps.nclass * acc_cols);
     if (nacc > MAX_ACC) nacc = MAX_ACC;
     if (nacc < 2) return APS_ERR_UNSUPPORTED;
     int cols = 32;
-    while (cols < nacc * taps.nclass * (int)c_out) cols *= 2;
+    while (cols < nacc * taps.nclass * acc_cols) cols *= 2;
 
     const uint32_t LBO_X = (uint32_t)BW * 16 + 16;
     // split (3xTF32): hi and lo copies of the weights and of each converted stage
@@ -717,7 +769,9 @@ aps_status launch_convt1d_tf32(const float *x, const int64_t in[3], const float 
     } else {
         ymap = map;   // unused
     }
-    const auto kern = split ? convt1d_tf32_kernel<true> : convt1d_tf32_kernel<false>;
+    const auto kern = paired  ? convt1d_tf32_kernel<MODE_X3_PAIRED>
+                      : split ? convt1d_tf32_kernel<MODE_X3>
+                              : convt1d_tf32_kernel<MODE_TF32>;
     const int per_sm = resident_ctas((const void *)kern, THREADS, (int)smem);
     if (per_sm < 1) return APS_ERR_UNSUPPORTED;
     const int64_t M = ceil_div(l_out, s);

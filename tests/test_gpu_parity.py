@@ -478,8 +478,10 @@ TF32X3_CASES = [  # (s, K, d, p, op, Cin, Cout, L, bias)
     (1, 3, 1, 1, 0, 8, 32, 300, True),
     (2, 4, 1, 1, 1, 16, 32, 64, True),
     (3, 2, 1, 1, 2, 8, 32, 32, True),
-    (1, 2, 1, 0, 0, 32, 256, 200, True),
+    (1, 2, 1, 0, 0, 32, 256, 200, True),   # 2 x C_out > 256: three MMAs per product
     (1, 1, 1, 0, 0, 24, 64, 4, True),
+    (1, 3, 1, 1, 0, 16, 128, 200, True),   # paired hi | lo weights: one N = 256 MMA
+    (2, 4, 1, 1, 1, 16, 64, 132, True),    # two classes, paired: N = 128, two accumulators
 ]
 
 
