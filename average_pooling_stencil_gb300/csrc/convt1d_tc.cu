@@ -1,6 +1,7 @@
 // convt1d_tc.cu -- ConvTranspose1d as a TF32 implicit GEMM on the tcgen05
 // tensor cores (APS_PREC_TF32), and its 3xTF32 form at fp32 accuracy
-// (APS_PREC_TF32X3: the SPLIT instantiation, described at the end).
+// (APS_PREC_TF32X3: the MODE_X3 and MODE_X3_PAIRED instantiations, described
+// at the end).
 //
 // Operation (Kimi-K2.6__l1_p74, its gather formula): y[n,co,o] = bias[co] +
 // sum_ci sum_k w[ci,co,k] * x[n,ci,(o + p - d*k)/s], where a term exists only
@@ -43,11 +44,16 @@
 // K-major layout, one [C_in/4][C_out][4] block per tap.  Every wait is bounded;
 // a wait that times out records APS_DEVERR_TIMEOUT, the CTA drains what it has
 // in flight and frees its tensor memory before returning.
-// 3xTF32 (SPLIT): weights and every converted stage are held twice, hi =
-// tf32(v) and lo = tf32(v - hi); each table entry issues lo(x)hi(w),
-// hi(x)lo(w), hi(x)hi(w) into the same accumulator (the dropped lo*lo term is
-// ~2^-22 of each product).  The launcher picks the deepest pipeline that fits
-// 227 KB: 32- then 16-channel chunks, 3 then 2 converted stages.  Only two
+// 3xTF32: weights and every converted stage are held twice.  Weights: hi =
+// tf32(w) (round to nearest) and lo = tf32(w - hi); inputs: hi = the raw word,
+// which the MMA truncates to tf32, and lo = v - trunc_tf32(v).  Each table entry
+// issues hi(x)[hi(w) | lo(w)] as one MMA of twice C_out columns and lo(x)hi(w)
+// into the first half of the same accumulator (the epilogue adds the halves;
+// where 2*C_out is no valid N, the three products go to one accumulator as three
+// C_out-wide MMAs).  The dropped lo(x)lo(w) term is below 2^-21 of each product
+// and the truncation of lo(x) below 2^-20.  The launcher picks the deepest
+// pipeline that fits 227 KB: 32- then 16-channel chunks, 3 then 2 converted
+// stages.  Only two
 // converter warps convert in this form, each taking every second 4-channel
 // block (its hi + lo stores from eight warps at once slowed the MMAs by 4 %).
 #include <algorithm>
@@ -581,17 +587,22 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
                     // neither has bank conflicts
                     uint4 *d0 = reinterpret_cast<uint4 *>(xt + xs * XT_STRIDE + cbx * LBO_X);
                     if constexpr (split) {
+                        // hi: the raw words (the MMA reads their leading tf32 bits,
+                        // i.e. truncates); lo = v - trunc_tf32(v), exact in fp32 (the
+                        // MMA truncates it in turn).  Two integer/fp operations per
+                        // value instead of two tf32 conversions: 268 -> 249 us on the
+                        // strided K4 workload, unchanged on the stride-1 K5 one.
                         uint4 *d1 = reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(d0) + XT_LO);
+                        auto lo = [](float t) {
+                            return __float_as_uint(t - __uint_as_float(__float_as_uint(t) & 0xFFFFE000u));
+                        };
+#pragma unroll 2
                         for (int pos = lane; pos < BW; pos += 32) {
                             const float v0 = s0[pos], v1 = s0[BW + pos], v2 = s0[2 * BW + pos],
                                         v3 = s0[3 * BW + pos];
-                            const uint4 h = make_uint4(tc1::to_tf32(v0), tc1::to_tf32(v1),
-                                                       tc1::to_tf32(v2), tc1::to_tf32(v3));
-                            d0[pos] = h;
-                            d1[pos] = make_uint4(tc1::to_tf32(v0 - __uint_as_float(h.x)),
-                                                 tc1::to_tf32(v1 - __uint_as_float(h.y)),
-                                                 tc1::to_tf32(v2 - __uint_as_float(h.z)),
-                                                 tc1::to_tf32(v3 - __uint_as_float(h.w)));
+                            d0[pos] = make_uint4(__float_as_uint(v0), __float_as_uint(v1),
+                                                 __float_as_uint(v2), __float_as_uint(v3));
+                            d1[pos] = make_uint4(lo(v0), lo(v1), lo(v2), lo(v3));
                         }
                     } else {
                         // plain tf32: the MMA reads the leading 19 bits of each fp32
