@@ -16,7 +16,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libaps.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["aps_api.cu", "avgpool3d.cu", "ct3d_pool.cu", "ct3d_pool_tc.cu", "convt3d.cu",
+SOURCES = ["aps_api.cu", "avgpool3d.cu", "ct3d_pool.cu", "ct3d_pool_tc.cu", "ct3d_pool_gen.cu",
+           "convt3d.cu",
            "convt3d_tc.cu", "convt1d.cu", "convt1d_tc.cu", "fma_probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",

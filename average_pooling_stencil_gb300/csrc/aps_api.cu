@@ -328,6 +328,10 @@ aps_status aps_ct3d_scale_pool_bias(const float *x, const int64_t in[5], const f
         st = launch_ct3d_pool2_fast(x, in, w, conv_bias, bias, scale1, scale2, y, out, cs);
         if (st != APS_ERR_UNSUPPORTED) return st;
     }
+    // any other geometry: collapsed per-phase weights, else one thread per output
+    st = launch_ct3d_pool_gen(x, in, w, conv_bias, bias, c_out, k, s, p, d, pool_k, scale1,
+                              scale2, y, out, cs);
+    if (st != APS_ERR_UNSUPPORTED) return st;
     return launch_ct3d_pool_direct(x, in, w, conv_bias, bias, c_out, k, s, p, d, pool_k,
                                    scale1, scale2, y, out, cs);
 }

@@ -100,6 +100,16 @@ aps_status launch_ct3d_pool2_tc(const float *x, const int64_t in[5], const float
                                 const float *conv_bias, const float *bias, float scale1,
                                 float scale2, float *y, const int64_t out[5], cudaStream_t st);
 
+// The fused op for any geometry whose per-dim phase tables fit (at most 8
+// phases and 8 input offsets per phase per dim, kernels of at most 32 taps per
+// dim, collapsed weights of at most 96 KB); APS_ERR_UNSUPPORTED otherwise (the
+// caller then uses launch_ct3d_pool_direct).
+aps_status launch_ct3d_pool_gen(const float *x, const int64_t in[5], const float *w,
+                                const float *conv_bias, const float *bias, int64_t c_out,
+                                const int k[3], const int s[3], const int p[3], const int d[3],
+                                int pool_k, float scale1, float scale2, float *y,
+                                const int64_t out[5], cudaStream_t st);
+
 aps_status launch_ct3d_pool_direct(const float *x, const int64_t in[5], const float *w,
                                    const float *conv_bias, const float *bias, int64_t c_out,
                                    const int k[3], const int s[3], const int p[3],

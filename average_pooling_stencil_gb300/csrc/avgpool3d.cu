@@ -255,6 +255,53 @@ __global__ void avgpool3d_direct_kernel(const float *__restrict__ x, float *__re
     }
 }
 
+// Small windows known at compile time (2x2x2 and 3x3x3, any stride and
+// padding, count_include_pad on or off, floor or ceil mode): the same
+// definition as above with the window unrolled, so that all its loads are in
+// flight at once, and 32-bit index arithmetic (the launcher checks that every
+// index fits).  One thread per output, consecutive threads on consecutive
+// output columns.
+template <int K>
+__global__ void __launch_bounds__(256)
+    avgpool3d_win_kernel(const float *__restrict__ x, float *__restrict__ y, unsigned total,
+                         int D, int H, int W, int Do, int Ho, int Wo, int sd, int sh, int sw,
+                         int pd, int ph, int pw, int count_include_pad) {
+    const unsigned in_plane = (unsigned)D * H * W;
+    for (unsigned idx = blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += gridDim.x * blockDim.x) {
+        const int ow = (int)(idx % (unsigned)Wo);
+        unsigned t = idx / (unsigned)Wo;
+        const int oh = (int)(t % (unsigned)Ho);
+        t /= (unsigned)Ho;
+        const int od = (int)(t % (unsigned)Do);
+        const unsigned nc = t / (unsigned)Do;
+        const int d0 = od * sd - pd, h0 = oh * sh - ph, w0 = ow * sw - pw;
+        const float *xp = x + (size_t)nc * in_plane;
+        float sum = 0.f;
+#pragma unroll
+        for (int a = 0; a < K; ++a)
+#pragma unroll
+            for (int b = 0; b < K; ++b)
+#pragma unroll
+                for (int c = 0; c < K; ++c) {
+                    const int id = d0 + a, ih = h0 + b, iw = w0 + c;
+                    const bool in = (unsigned)id < (unsigned)D && (unsigned)ih < (unsigned)H &&
+                                    (unsigned)iw < (unsigned)W;
+                    sum += in ? __ldg(xp + ((unsigned)id * H + ih) * W + iw) : 0.f;
+                }
+        int div;
+        if (count_include_pad) {
+            // the window clipped at the end of the right padding (ceil mode)
+            div = (min(d0 + K, D + pd) - d0) * (min(h0 + K, H + ph) - h0) *
+                  (min(w0 + K, W + pw) - w0);
+        } else {
+            div = (min(d0 + K, D) - max(d0, 0)) * (min(h0 + K, H) - max(h0, 0)) *
+                  (min(w0 + K, W) - max(w0, 0));
+        }
+        y[idx] = div > 0 ? sum / (float)div : 0.f;
+    }
+}
+
 aps_status launch_avgpool3d_direct(const float *x, const int64_t in[5], const int k[3],
                                    const int s[3], const int p[3], int count_include_pad,
                                    float *y, const int64_t out[5], cudaStream_t st) {
@@ -265,6 +312,16 @@ aps_status launch_avgpool3d_direct(const float *x, const int64_t in[5], const in
     const int threads = 256;
     const long long blocks =
         std::min<long long>(ceil_div(total, threads), (long long)sm_count() * 16);
+    const bool cube = k[0] == k[1] && k[1] == k[2] && (k[0] == 2 || k[0] == 3);
+    // 32-bit output index (with headroom for the grid stride) and plane offsets
+    if (cube && total <= ((int64_t)1 << 31) && in[2] * in[3] * in[4] < ((int64_t)1 << 31)) {
+        const auto kern = k[0] == 2 ? avgpool3d_win_kernel<2> : avgpool3d_win_kernel<3>;
+        const cudaError_t e = launch_plain(
+            kern, dim3((unsigned)blocks), dim3(threads), 0, st, x, y, (unsigned)total, (int)in[2],
+            (int)in[3], (int)in[4], (int)out[2], (int)out[3], (int)out[4], s[0], s[1], s[2], p[0],
+            p[1], p[2], count_include_pad);
+        return launch_status(e);
+    }
     const cudaError_t e = launch_plain(
         avgpool3d_direct_kernel, dim3((unsigned)blocks), dim3(threads), 0, st, x, y, total,
         (int)in[2], (int)in[3], (int)in[4], (int)out[2], (int)out[3], (int)out[4], k[0], k[1],

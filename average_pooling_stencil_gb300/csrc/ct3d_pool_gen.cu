@@ -1,0 +1,300 @@
+// ct3d_pool_gen.cu -- the fused ConvTranspose3d -> x scale1 -> AvgPool3d(q) ->
+// + bias -> x scale2 op for any geometry (kernel, stride, padding, dilation,
+// output padding per dim; any pool size q; any channel counts).
+//
+// Kimi-K2.6__l2_p50 derives, for its k3 s2 p1 / pool 2 model, that a pooled
+// output reads a fixed 2x2x2 neighbourhood of the input with 8 collapsed
+// weights (the 27 taps grouped by the input cell they read), and sketches the
+// same idea for other geometries.  Written out per dim: pooled output P covers
+// the pre-pool positions o in [qP, qP + q); tap k of o reads input
+// i = (o + p - d*k) / s where that quotient is an integer.  The (i - base, k)
+// pattern repeats every T = s / gcd(q, s) pooled outputs (the window moves by
+// lcm(q, s) pre-pool positions, i.e. by q*T/s inputs), so per dim and phase
+// phi = P mod T there is a short list of input offsets delta, each with the set
+// of taps that reaches it.  The pooled output is then
+//   y[n,co,P] = bias' + sum_ci sum_delta x[n,ci,base(P) + delta] * Weff[phi][ci][co][delta]
+// with Weff the sum of w over each delta's taps (per dim, the product of the
+// three dims' tap sets) times scale1*scale2/q^3, and bias' = (conv_bias*scale1 +
+// bias)*scale2.  Input cells outside the tensor contribute nothing (they are
+// the transposed convolution's missing terms, not zero padding of x).
+//
+// Kernel: each CTA builds Weff for all phase combinations in shared memory
+// (host-built per-dim tables come in the launch parameters), then each thread
+// takes one pooled position and accumulates 16 output channels at a time in
+// registers: one input load feeds 16 FMAs whose weights are a broadcast
+// 16-float shared-memory read when the warp's threads share a phase (always
+// for q a multiple of s).  Threads run along the pooled W axis, so input and
+// output accesses are coalesced.  Geometries whose tables exceed the limits
+// below fall back to the per-output direct kernel in ct3d_pool.cu.
+#include <algorithm>
+
+#include "aps_dev.cuh"
+#include "aps_internal.h"
+
+namespace aps {
+namespace gen {
+constexpr int MAX_PHASE = 8;    // T = s / gcd(q, s)
+constexpr int MAX_DELTA = 8;    // input offsets per phase
+constexpr int MAX_TAPS = 32;    // kernel size per dim (tap sets are bit masks)
+constexpr int CO_T = 16;        // output channels per register block
+constexpr int THREADS = 128;
+constexpr int MAX_WEFF_BYTES = 96 * 1024;
+
+struct Dim {
+    int T;                               // phases
+    int step;                            // input advance per T pooled outputs
+    int md;                              // max offsets over the phases
+    int nd[MAX_PHASE];                   // offsets of each phase
+    int i0[MAX_PHASE];                   // first input of phase phi at P = phi
+    uint32_t kmask[MAX_PHASE][MAX_DELTA];  // taps reaching each offset
+};
+struct Geom {
+    Dim d[3];
+};
+
+// Sum of w[ci][co][kd][kh][kw] over the three tap sets (bit masks).
+__device__ __forceinline__ float tap_set_sum(const float *__restrict__ wp, int kH, int kW,
+                                             uint32_t md, uint32_t mh, uint32_t mw) {
+    float acc = 0.f;
+    for (uint32_t a = md; a; a &= a - 1) {
+        const int kd = __ffs(a) - 1;
+        for (uint32_t b = mh; b; b &= b - 1) {
+            const int kh = __ffs(b) - 1;
+            for (uint32_t c = mw; c; c &= c - 1) {
+                const int kw = __ffs(c) - 1;
+                acc += __ldg(wp + (kd * kH + kh) * kW + kw);
+            }
+        }
+    }
+    return acc;
+}
+}  // namespace gen
+
+// ND > 0: every phase of every dim reads at most ND input offsets; the cell
+// loops are unrolled and the loads of one input channel (ND^3 of them) are all
+// in flight before their FMAs.  ND == 0: any count, run-time loops.
+template <int ND>
+__global__ void __launch_bounds__(gen::THREADS)
+    ct3d_pool_gen_kernel(const float *__restrict__ x, const float *__restrict__ w,
+                         const float *__restrict__ conv_bias, const float *__restrict__ bias,
+                         float wscale, float scale1, float scale2, float *__restrict__ y,
+                         long long n_pos, int Cin, int Cout, int COP, int D, int H, int W,
+                         int Do, int Ho, int Wo, int kD, int kH, int kW,
+                         const __grid_constant__ gen::Geom g) {
+    using namespace gen;
+    pdl_trigger();
+    pdl_wait();
+    extern __shared__ __align__(16) float weff[];   // [combo][ci][dd][dh][dw][COP]
+    const Dim &GD = g.d[0], &GH = g.d[1], &GW = g.d[2];
+    const int MD = GD.md, MH = GH.md, MW = GW.md;
+    const int taps = MD * MH * MW;
+    const int combos = GD.T * GH.T * GW.T;
+    // ---- collapsed weights (scaled by scale1 * scale2 / q^3)
+    const long long total = (long long)combos * Cin * taps * COP;
+    for (long long e = threadIdx.x; e < total; e += blockDim.x) {
+        long long t = e;
+        const int co = (int)(t % COP);
+        t /= COP;
+        const int tw = (int)(t % MW);
+        t /= MW;
+        const int th = (int)(t % MH);
+        t /= MH;
+        const int td = (int)(t % MD);
+        t /= MD;
+        const int ci = (int)(t % Cin);
+        const int combo = (int)(t / Cin);
+        const int fw = combo % GW.T, fh = (combo / GW.T) % GH.T, fd = combo / (GW.T * GH.T);
+        float v = 0.f;
+        if (co < Cout && td < GD.nd[fd] && th < GH.nd[fh] && tw < GW.nd[fw])
+            v = tap_set_sum(w + ((long long)ci * Cout + co) * kD * kH * kW, kH, kW,
+                            GD.kmask[fd][td], GH.kmask[fh][th], GW.kmask[fw][tw]) *
+                wscale;
+        weff[e] = v;
+    }
+    __syncthreads();
+
+    const long long in_plane = (long long)D * H * W;
+    const long long out_plane = (long long)Do * Ho * Wo;
+    for (long long pos = blockIdx.x * (long long)blockDim.x + threadIdx.x; pos < n_pos;
+         pos += (long long)gridDim.x * blockDim.x) {
+        const int pw = (int)(pos % Wo);
+        long long t = pos / Wo;
+        const int ph = (int)(t % Ho);
+        t /= Ho;
+        const int pd = (int)(t % Do);
+        const long long n = t / Do;
+        const int fd = pd % GD.T, fh = ph % GH.T, fw = pw % GW.T;
+        const int bd = (pd / GD.T) * GD.step + GD.i0[fd];
+        const int bh = (ph / GH.T) * GH.step + GH.i0[fh];
+        const int bw = (pw / GW.T) * GW.step + GW.i0[fw];
+        // offsets of this position that land inside the input
+        const int d0 = max(0, -bd), d1 = min(GD.nd[fd], D - bd);
+        const int h0 = max(0, -bh), h1 = min(GH.nd[fh], H - bh);
+        const int w0 = max(0, -bw), w1 = min(GW.nd[fw], W - bw);
+        const int combo = (fd * GH.T + fh) * GW.T + fw;
+        const float *xn = x + n * Cin * in_plane;
+        float *yp = y + n * Cout * out_plane + ((long long)pd * Ho + ph) * Wo + pw;
+        for (int co0 = 0; co0 < Cout; co0 += CO_T) {
+            float acc[CO_T];
+#pragma unroll
+            for (int j = 0; j < CO_T; ++j) acc[j] = 0.f;
+            for (int ci = 0; ci < Cin; ++ci) {
+                const float *xc = xn + ci * in_plane;
+                const float *wc = weff + ((long long)(combo * Cin + ci) * taps) * COP + co0;
+                if constexpr (ND > 0) {
+                    // taps beyond a phase's count have zero weights, so cells past
+                    // the end of the input or of the phase load nothing and add 0
+                    float xv[ND][ND][ND];
+#pragma unroll
+                    for (int a = 0; a < ND; ++a)
+#pragma unroll
+                        for (int b = 0; b < ND; ++b)
+#pragma unroll
+                            for (int c = 0; c < ND; ++c) {
+                                const bool in = a >= d0 && a < d1 && b >= h0 && b < h1 &&
+                                                c >= w0 && c < w1;
+                                xv[a][b][c] =
+                                    in ? __ldg(xc + ((long long)(bd + a) * H + (bh + b)) * W +
+                                               (bw + c))
+                                       : 0.f;
+                            }
+#pragma unroll
+                    for (int a = 0; a < ND; ++a)
+#pragma unroll
+                        for (int b = 0; b < ND; ++b)
+#pragma unroll
+                            for (int c = 0; c < ND; ++c) {
+                                const float4 *w4 = reinterpret_cast<const float4 *>(
+                                    wc + ((a * MH + b) * MW + c) * COP);
+#pragma unroll
+                                for (int j = 0; j < CO_T / 4; ++j) {
+                                    const float4 q4 = w4[j];
+                                    acc[4 * j + 0] = fmaf(xv[a][b][c], q4.x, acc[4 * j + 0]);
+                                    acc[4 * j + 1] = fmaf(xv[a][b][c], q4.y, acc[4 * j + 1]);
+                                    acc[4 * j + 2] = fmaf(xv[a][b][c], q4.z, acc[4 * j + 2]);
+                                    acc[4 * j + 3] = fmaf(xv[a][b][c], q4.w, acc[4 * j + 3]);
+                                }
+                            }
+                } else {
+                    for (int a = d0; a < d1; ++a)
+                        for (int b = h0; b < h1; ++b) {
+                            const float *xr = xc + ((long long)(bd + a) * H + (bh + b)) * W + bw;
+                            const float *wr = wc + ((a * MH + b) * MW) * COP;
+                            for (int c = w0; c < w1; ++c) {
+                                const float xv = __ldg(xr + c);
+                                const float4 *w4 = reinterpret_cast<const float4 *>(wr + c * COP);
+#pragma unroll
+                                for (int j = 0; j < CO_T / 4; ++j) {
+                                    const float4 q4 = w4[j];
+                                    acc[4 * j + 0] = fmaf(xv, q4.x, acc[4 * j + 0]);
+                                    acc[4 * j + 1] = fmaf(xv, q4.y, acc[4 * j + 1]);
+                                    acc[4 * j + 2] = fmaf(xv, q4.z, acc[4 * j + 2]);
+                                    acc[4 * j + 3] = fmaf(xv, q4.w, acc[4 * j + 3]);
+                                }
+                            }
+                        }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < CO_T; ++j) {
+                const int co = co0 + j;
+                if (co < Cout) {
+                    const float cb = conv_bias ? __ldg(conv_bias + co) : 0.f;
+                    yp[(long long)co * out_plane] =
+                        acc[j] + (cb * scale1 + __ldg(bias + co)) * scale2;
+                }
+            }
+        }
+    }
+}
+
+namespace {
+int gcd_i(int a, int b) {
+    while (b) {
+        const int t = a % b;
+        a = b;
+        b = t;
+    }
+    return a;
+}
+int floordiv_i(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
+
+// Per-dim phase tables; false if the geometry exceeds the table limits.
+bool build_dim(int K, int s, int p, int d, int q, gen::Dim &t) {
+    using namespace gen;
+    if (K > MAX_TAPS) return false;
+    const int g = gcd_i(q, s);
+    t = gen::Dim{};
+    t.T = s / g;
+    t.step = q / g;
+    if (t.T > MAX_PHASE) return false;
+    t.md = 0;
+    for (int f = 0; f < t.T; ++f) {
+        int lo = 1 << 30, hi = -(1 << 30);
+        for (int o = q * f; o < q * f + q; ++o)
+            for (int k = 0; k < K; ++k) {
+                const long long num = (long long)o + p - (long long)d * k;
+                if (((num % s) + s) % s) continue;
+                const int i = floordiv_i((int)num, s);
+                lo = std::min(lo, i);
+                hi = std::max(hi, i);
+            }
+        if (lo > hi) {   // no tap reaches this phase: bias only
+            t.nd[f] = 0;
+            t.i0[f] = 0;
+            continue;
+        }
+        if (hi - lo + 1 > MAX_DELTA) return false;
+        t.nd[f] = hi - lo + 1;
+        t.i0[f] = lo;
+        t.md = std::max(t.md, t.nd[f]);
+        for (int o = q * f; o < q * f + q; ++o)
+            for (int k = 0; k < K; ++k) {
+                const long long num = (long long)o + p - (long long)d * k;
+                if (((num % s) + s) % s) continue;
+                t.kmask[f][floordiv_i((int)num, s) - lo] |= 1u << k;
+            }
+    }
+    if (t.md == 0) t.md = 1;
+    return true;
+}
+}  // namespace
+
+aps_status launch_ct3d_pool_gen(const float *x, const int64_t in[5], const float *w,
+                                const float *conv_bias, const float *bias, int64_t c_out,
+                                const int k[3], const int s[3], const int p[3], const int d[3],
+                                int pool_k, float scale1, float scale2, float *y,
+                                const int64_t out[5], cudaStream_t st) {
+    using namespace gen;
+    if (pool_k > 64) return APS_ERR_UNSUPPORTED;   // o and the tap loops stay small
+    gen::Geom g;
+    for (int i = 0; i < 3; ++i)
+        if (!build_dim(k[i], s[i], p[i], d[i], pool_k, g.d[i])) return APS_ERR_UNSUPPORTED;
+    const int COP = (int)((c_out + CO_T - 1) / CO_T) * CO_T;
+    // offsets per phase at most 2 in every dim (the pages' geometry and its
+    // output-padding / pool variants): unrolled cells
+    const bool nd2 = g.d[0].md <= 2 && g.d[1].md <= 2 && g.d[2].md <= 2;
+    if (nd2)
+        for (int i = 0; i < 3; ++i) g.d[i].md = 2;   // Weff laid out 2 x 2 x 2 per (ci, phase)
+    const long long weff_floats = (long long)g.d[0].T * g.d[1].T * g.d[2].T * in[1] * g.d[0].md *
+                            g.d[1].md * g.d[2].md * COP;
+    if (weff_floats * 4 > MAX_WEFF_BYTES) return APS_ERR_UNSUPPORTED;
+    const int smem = (int)std::max<long long>(16, weff_floats * 4);
+    const auto kern = nd2 ? ct3d_pool_gen_kernel<2> : ct3d_pool_gen_kernel<0>;
+    const int per_sm = resident_ctas((const void *)kern, THREADS, smem);
+    if (per_sm < 1) return APS_ERR_UNSUPPORTED;
+    const long long n_pos = out[0] * out[2] * out[3] * out[4];
+    const long long grid =
+        std::max<long long>(1, std::min<long long>(ceil_div(n_pos, THREADS),
+                                                   (long long)sm_count() * per_sm));
+    const float q3 = (float)pool_k * pool_k * pool_k;
+    const float wscale = scale1 * scale2 / q3;
+    const cudaError_t e = launch_pdl(
+        kern, dim3((unsigned)grid), dim3(THREADS), (size_t)smem, st, x, w,
+        conv_bias, bias, wscale, scale1, scale2, y, n_pos, (int)in[1], (int)c_out, COP,
+        (int)in[2], (int)in[3], (int)in[4], (int)out[2], (int)out[3], (int)out[4], k[0], k[1],
+        k[2], g);
+    return launch_status(e);
+}
+
+}  // namespace aps

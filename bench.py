@@ -107,6 +107,19 @@ def convt_pairs(L, L_out, K, s, p, d):
     return n
 
 
+def pooled_cells(L, P_out, K, s, p, d, q):
+    """Input cells read, summed over the pooled outputs of one dim: pooled output P
+    covers pre-pool positions [qP, qP + q), whose taps read inputs (o + p - d*k)/s
+    where that is an integer in [0, L); each distinct input counts once (the
+    collapsed weights of the fused op)."""
+    n = 0
+    for P in range(P_out):
+        cells = {(o + p - d * k) // s for o in range(q * P, q * P + q) for k in range(K)
+                 if (o + p - d * k) % s == 0 and 0 <= (o + p - d * k) // s < L}
+        n += len(cells)
+    return n
+
+
 class ClockSampler:
     """nvidia-smi samples of the SM clock and throttle reasons, in the background."""
     FIELDS = ["timestamp", "clocks.sm", "clocks.max.sm", "power.draw",
@@ -342,14 +355,14 @@ class GpuCase:
             if fast:
                 self.flops = 2 * 8 * cin * numel(oshape)      # 8 collapsed taps per ci
             else:
-                # the literal chain: every in-range tap of every pre-pool output the
-                # pooled windows cover, then the window adds
-                pairs = 1
+                # the collapsed form of any geometry: per pooled output and input
+                # channel, one multiply-add per input cell its window reads
+                cells = 1
                 for i in range(3):
-                    pairs *= convt_pairs(x.shape[2 + i], oshape[2 + i] * p["pool_k"],
-                                         p["k"][i], p["stride"][i], p["pad"][i], p["dil"][i])
-                self.flops = (2 * x.shape[0] * cin * p["c_out"] * pairs
-                              + p["pool_k"] ** 3 * numel(oshape))
+                    cells *= pooled_cells(x.shape[2 + i], oshape[2 + i], p["k"][i],
+                                          p["stride"][i], p["pad"][i], p["dil"][i],
+                                          p["pool_k"])
+                self.flops = 2 * x.shape[0] * cin * p["c_out"] * cells
             # C_in <= 3 with 16-byte input rows runs on the tensor cores (3xTF32,
             # three MMA passes), bound by HBM; otherwise on the FP32 pipe
             self.tc = fast and cin <= 3 and x.shape[4] % 4 == 0

@@ -88,7 +88,10 @@ def test_avgpool_unaligned_input_takes_direct_path():
 @pytest.mark.parametrize("k,s,p,cip,ceil", [
     ((2, 3, 4), (1, 2, 3), (1, 1, 2), 1, 0), ((3, 3, 3), (2, 2, 2), (1, 1, 1), 0, 0),
     ((3, 3, 3), (2, 2, 2), (1, 1, 1), 1, 1), ((3, 3, 3), (2, 2, 2), (1, 1, 1), 0, 1),
-    ((5, 2, 3), (3, 2, 1), (2, 0, 1), 0, 1), ((1, 1, 1), (1, 1, 1), (0, 0, 0), 1, 0)])
+    ((5, 2, 3), (3, 2, 1), (2, 0, 1), 0, 1), ((1, 1, 1), (1, 1, 1), (0, 0, 0), 1, 0),
+    # cubic windows of 2 and 3 take the unrolled-window kernel
+    ((2, 2, 2), (2, 2, 2), (0, 0, 0), 1, 0), ((2, 2, 2), (1, 2, 3), (1, 1, 0), 0, 1),
+    ((2, 2, 2), (3, 1, 2), (1, 0, 1), 1, 1), ((3, 3, 3), (1, 3, 2), (0, 1, 1), 1, 0)])
 def test_avgpool_general_windows(k, s, p, cip, ceil):
     x, = rng_inputs(3, (2, 2, 7, 9, 10))
     y = B.avgpool3d(dev(x), k, s, p, bool(cip), bool(ceil))
@@ -219,6 +222,26 @@ def test_fused_general_geometry(cout, k, s, p, op, d, q):
     prm = dict(stride=s, pad=p, out_pad=op, dil=d, pool_k=q, scale1=0.5, scale2=1.5)
     ref = ora.ct3d_scale_pool_bias(x, w, cb, b, s, p, op, d, q, 0.5, 1.5)
     assert_close(fused_gpu(x, w, cb, b, prm), ref, what=f"fused general {k} {s} {p} {op} {d} {q}")
+
+
+# the general kernel's per-dim phase tables: pool sizes that are not multiples of the
+# stride (3 and 2 phases per dim), stride 4 with pool 1 (two of the four phases reached
+# by no tap: bias only), several 16-channel output blocks with a ragged last one; and,
+# past the tables' limits (9 input offsets per phase with dilation 3; 9 phases), the
+# per-output direct kernel
+@pytest.mark.parametrize("xs,cout,k,s,p,op,d,q", [
+    ((2, 5, 5, 7, 41), 20, (3, 3, 4), (3, 2, 4), (1, 0, 2), (0, 1, 3), (1, 1, 1), 2),
+    ((3, 3, 4, 6, 33), 33, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (1, 1, 1), 2),
+    ((1, 2, 3, 4, 37), 6, (2, 2, 2), (1, 1, 4), (0, 0, 1), (0, 0, 0), (1, 1, 1), 1),
+    ((1, 2, 6, 5, 9), 7, (2, 3, 3), (2, 1, 3), (0, 2, 1), (1, 0, 2), (2, 3, 1), 3),
+    ((1, 2, 3, 4, 5), 6, (2, 2, 3), (1, 1, 9), (0, 0, 1), (0, 0, 0), (1, 1, 1), 1)])
+def test_fused_general_geometry_tables(xs, cout, k, s, p, op, d, q):
+    x, = rng_inputs(9, xs)
+    w, cb, b = rng_inputs(10, (xs[1], cout) + k, (cout,), (cout,), lo=-0.2, hi=0.2)
+    prm = dict(stride=s, pad=p, out_pad=op, dil=d, pool_k=q, scale1=0.75, scale2=-1.25)
+    ref = ora.ct3d_scale_pool_bias(x, w, cb, b, s, p, op, d, q, 0.75, -1.25)
+    assert_close(fused_gpu(x, w, cb, b, prm), ref,
+                 what=f"fused general {xs} {k} {s} {p} {op} {d} {q}")
 
 
 # ------------------------------------------------------------ convtranspose3d
