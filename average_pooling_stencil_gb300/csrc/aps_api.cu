@@ -373,7 +373,7 @@ aps_status aps_convtranspose3d(const float *x, const int64_t in[5], const float 
     for (int i = 0; i < 3; ++i)
         fast = fast && k[i] == 3 && s[i] == 2 && p[i] == 1 && d[i] == 1 && op[i] <= 1;
     if (fast) {
-        // tensor cores (C_in <= 3, W <= 32, 16-byte input rows), else the FP32 pipe
+        // tensor cores (W <= 32, 16-byte input rows), else the FP32 pipe
         st = launch_convt3d_tc(x, in, w, bias, y, out, cs);
         if (st != APS_ERR_UNSUPPORTED) return st;
         st = launch_convt3d_k3s2p1(x, in, w, bias, y, out, cs);

@@ -119,7 +119,7 @@ aps_status launch_ct3d_pool_direct(const float *x, const int64_t in[5], const fl
 // ConvTranspose3d, fp32: the k3 s2 p1 d1 kernel (C_out 16, C_in <= 8, TMA
 // staging) and the direct per-output kernel for any geometry.
 // Standalone ConvTranspose3d k3 s2 p1 on the tensor cores (3xTF32: fp32
-// accuracy) for C_in <= 3, W <= 32 and 16-byte input rows; APS_ERR_UNSUPPORTED
+// accuracy) for C_in <= 8, W <= 32 and 16-byte input rows; APS_ERR_UNSUPPORTED
 // otherwise (the caller then uses launch_convt3d_k3s2p1).
 aps_status launch_convt3d_tc(const float *x, const int64_t in[5], const float *w,
                              const float *bias, float *y, const int64_t out[5], cudaStream_t st);

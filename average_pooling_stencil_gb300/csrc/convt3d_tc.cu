@@ -35,6 +35,11 @@
 // Every wait is bounded; the group barrier also carries each warp's go-on
 // vote, so that a group whose wait ran out leaves together, drains what it
 // issued and frees the tensor memory.
+// C_in 4..8: the A row grows to 16*C_in columns (the accumulator then starts
+// at column 128 of the group's 256) and B to 8 KB per input channel, so the
+// staging blocks no longer fit beside the ring: the epilogue writes each
+// thread's outputs straight from registers instead (for each channel, its two
+// r_w outputs; a warp's 32 lanes cover 64 consecutive outputs of one row).
 #include <algorithm>
 #include <cstring>
 
@@ -46,7 +51,7 @@ namespace aps {
 namespace c3t {
 constexpr int COUT = 16;
 constexpr int NCOL = 8 * COUT;             // MMA N: 8 parity classes x 16 channels
-constexpr int CIN_MAX = 3;
+constexpr int CIN_MAX = 8;
 constexpr int GROUPS = 2;
 constexpr int WORKERS = 4 * GROUPS;        // warps 0..7
 constexpr int W_FILL = WORKERS;            // warp 8: the TMA loads of the input ring
@@ -58,7 +63,8 @@ constexpr int OROWS = 2 * MROWS;           // output rows per unit
 constexpr int STAGES = 4 * GROUPS;         // input ring: four units in flight per group
 constexpr int TMEM_COLS = 512;
 constexpr int GROUP_COLS = TMEM_COLS / GROUPS;   // 256
-constexpr int D_COL = 64;                  // accumulator: 128 columns after A hi + lo (48)
+// accumulator: 128 columns after A hi + lo (16 * C_in columns)
+__host__ __device__ constexpr int d_col_of(int cin) { return 16 * cin <= 64 ? 64 : 128; }
 // Fixed head of the dynamic shared memory (bytes); stages and staging follow.
 constexpr int OFF_FULL = 0;                // uint64 [STAGES]
 constexpr int OFF_EMPTY = 64;              // uint64 [STAGES]
@@ -69,9 +75,12 @@ constexpr int OFF_SLOT = 192;              // Slot [STAGES]
 constexpr int OFF_BIAS = 448;              // float [16]
 constexpr int OFF_B = 512;                 // B, hi then lo: [C_in][2][128][4] words each
 constexpr int B_CI_BYTES = 2 * NCOL * 16;  // one input channel's K-step of 8: 4096 bytes
-constexpr int HEAD_BYTES = OFF_B + 2 * CIN_MAX * B_CI_BYTES;   // 25088, a multiple of 128
-static_assert(HEAD_BYTES % 128 == 0, "stages start 128-byte aligned");
-static_assert(D_COL >= 16 * CIN_MAX && D_COL + NCOL <= GROUP_COLS, "tile buffer layout");
+__host__ __device__ constexpr int head_bytes_of(int cin) { return OFF_B + 2 * cin * B_CI_BYTES; }
+// outputs straight from registers (no staging blocks) above 3 input channels
+__host__ __device__ constexpr bool direct_of(int cin) { return cin > 3; }
+static_assert(head_bytes_of(1) % 128 == 0, "stages start 128-byte aligned");
+static_assert(d_col_of(CIN_MAX) >= 16 * CIN_MAX && d_col_of(CIN_MAX) + NCOL <= GROUP_COLS,
+              "tile buffer layout");
 static_assert(STAGES % GROUPS == 0, "a group's units always use the same stages");
 
 struct Slot {
@@ -98,7 +107,15 @@ __host__ __device__ inline int staging_floats_of(int Wo, int ac, int ap) {
 }
 }  // namespace c3t
 
-// CIN: input channels (1..3).
+// 32 lanes x 8 columns from registers (the caller waits with tmem_st_wait).
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t *v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+        : "memory");
+}
+
+// CIN: input channels (1..8).
 template <int CIN>
 __global__ void __launch_bounds__(c3t::THREADS, 1)
     convt3d_tc_kernel(const __grid_constant__ CUtensorMap xmap, const float *__restrict__ w,
@@ -108,6 +125,8 @@ __global__ void __launch_bounds__(c3t::THREADS, 1)
     pdl_trigger();
     pdl_wait();
     using namespace c3t;
+    constexpr int D_COL = d_col_of(CIN), HEAD_BYTES = head_bytes_of(CIN);
+    constexpr bool DIRECT = direct_of(CIN);
     extern __shared__ __align__(128) unsigned char smraw[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smraw + OFF_FULL);
     uint64_t *empty = reinterpret_cast<uint64_t *>(smraw + OFF_EMPTY);
@@ -227,7 +246,26 @@ __global__ void __launch_bounds__(c3t::THREADS, 1)
 
             // ---- the A row of input position (mh0 + q, lane): hi and lo of
             // its 8*C_in neighbourhood values
-            if (ok) {
+            if constexpr (CIN > 3) {
+              if (ok) {
+                // one input channel at a time: its 8 hi and 8 lo columns
+                const float *xp = xs + s * stage_stride + q * BW + lane;
+#pragma unroll
+                for (int ci = 0; ci < CIN; ++ci) {
+                    uint32_t hv[8], lv[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int a = e >> 2, b = (e >> 1) & 1, c = e & 1;
+                        const float v = xp[((ci * 2 + a) * XR + b) * BW + c];
+                        hv[e] = __float_as_uint(v) & 0xFFFFE000u;
+                        lv[e] = __float_as_uint(v - __uint_as_float(hv[e]));
+                    }
+                    tmem_st8(tmem + lane_q + gcol + 8 * ci, hv);
+                    tmem_st8(tmem + lane_q + gcol + 8 * CIN + 8 * ci, lv);
+                }
+                tc::tmem_st_wait();
+              }
+            } else if (ok) {
                 const float *xp = xs + s * stage_stride + q * BW + lane;
                 uint32_t av[16 * CIN];   // hi[0 .. 8*CIN), then lo
 #pragma unroll
@@ -280,17 +318,13 @@ __global__ void __launch_bounds__(c3t::THREADS, 1)
                 *abort_flag = 1;
             }
             okd = __all_sync(0xffffffffu, okd);
-            // the group's previous copies (each issued by its own lane) have
-            // read its staging block before this unit's epilogue rewrites it:
-            // they had this unit's gather and MMAs to do so
-            bulk_wait_read<0>();
-            __syncwarp();
-            if (tc::named_bar_or(gbar, 128, !okd)) break;
-            const int oh0 = 2 * gmh0;
-            const int nrows = Ho - oh0 < OROWS ? Ho - oh0 : OROWS;
-            float *y0 = y + ((gn * COUT) * Do + 2 * gmd) * plane + (long long)oh0 * Wo;
-            const int a0 = (int)((reinterpret_cast<uintptr_t>(y0) >> 2) & 3u);
-            {
+            if constexpr (DIRECT) {
+                if (tc::named_bar_or(gbar, 128, !okd)) break;
+                // outputs straight from registers: lane l holds output columns 2l
+                // and 2l + 1 of every channel of its (r_d, r_h) row
+                const int oh0 = 2 * gmh0;
+                const int nrows = Ho - oh0 < OROWS ? Ho - oh0 : OROWS;
+                float *y0 = y + ((gn * COUT) * Do + 2 * gmd) * plane + (long long)oh0 * Wo;
                 tc::tc_fence_after();
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
@@ -299,50 +333,84 @@ __global__ void __launch_bounds__(c3t::THREADS, 1)
                     tc::tmem_ld32(tmem + lane_q + gcol + D_COL + 32 * c, v);
                     const int row = 2 * q + rh;
                     if (2 * gmd + rd < Do && row < nrows && in_w) {
-                        float *sp = og + rd * RDS + a0 + row * Wo + 2 * lane;
+                        float *yp = y0 + rd * plane + (long long)row * Wo + 2 * lane;
                         const bool w1 = 2 * lane + 1 < Wo;
 #pragma unroll
                         for (int co = 0; co < COUT; ++co) {
-                            sp[0] = __uint_as_float(v[co]) + bias_r[co];
-                            if (w1) sp[1] = __uint_as_float(v[16 + co]) + bias_r[co];
-                            sp += CH;
+                            yp[0] = __uint_as_float(v[co]) + bias_r[co];
+                            if (w1) yp[1] = __uint_as_float(v[16 + co]) + bias_r[co];
+                            yp += cstride;
                         }
                     }
                 }
-            }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            tc::named_bar(gbar, 128);   // the staging block is complete
-
-            // ---- each (r_d, co) run: its 16-byte-aligned middle by one bulk copy,
-            // the at most 3 + 3 head and tail floats by plain stores.  Warp q takes
-            // channels 4q..4q+3 of both planes; lane i < 8 issues run i's copy.
-            const int run = nrows * Wo;
-            {
-                const int i = lane & 7;
-                const int rd = i >> 2, co = 4 * q + (i & 3);
-                const uint32_t off = (uint32_t)(a0 + co * ac + rd * ap) & 3u;
-                const int hd = (int)((4u - off) & 3u);
-                const int mid = run > hd ? (run - hd) & ~3 : 0;
-                float *yc = y0 + co * cstride + rd * plane;
-                const float *sc = og + rd * RDS + co * CH + a0;
-                if (lane < 8 && 2 * gmd + rd < Do && mid > 0) {
-                    bulk_store(yc + hd, sc + hd, (uint32_t)mid * 4u);
-                    bulk_commit();
+                // the accumulator is read: the next unit's MMAs may overwrite it
+                tc::tc_fence_before();
+                continue;
+            } else {
+                // the group's previous copies (each issued by its own lane) have
+                // read its staging block before this unit's epilogue rewrites it:
+                // they had this unit's gather and MMAs to do so
+                bulk_wait_read<0>();
+                __syncwarp();
+                if (tc::named_bar_or(gbar, 128, !okd)) break;
+                const int oh0 = 2 * gmh0;
+                const int nrows = Ho - oh0 < OROWS ? Ho - oh0 : OROWS;
+                float *y0 = y + ((gn * COUT) * Do + 2 * gmd) * plane + (long long)oh0 * Wo;
+                const int a0 = (int)((reinterpret_cast<uintptr_t>(y0) >> 2) & 3u);
+                {
+                    tc::tc_fence_after();
+    #pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        const int rd = c >> 1, rh = c & 1;
+                        uint32_t v[32];   // v[rw*16 + co]
+                        tc::tmem_ld32(tmem + lane_q + gcol + D_COL + 32 * c, v);
+                        const int row = 2 * q + rh;
+                        if (2 * gmd + rd < Do && row < nrows && in_w) {
+                            float *sp = og + rd * RDS + a0 + row * Wo + 2 * lane;
+                            const bool w1 = 2 * lane + 1 < Wo;
+    #pragma unroll
+                            for (int co = 0; co < COUT; ++co) {
+                                sp[0] = __uint_as_float(v[co]) + bias_r[co];
+                                if (w1) sp[1] = __uint_as_float(v[16 + co]) + bias_r[co];
+                                sp += CH;
+                            }
+                        }
+                    }
                 }
-#pragma unroll 1
-                for (int r = 0; r < 8; ++r) {   // head and tail of run r of this warp
-                    const int rd2 = r >> 2, co2 = 4 * q + (r & 3);
-                    if (2 * gmd + rd2 >= Do) break;
-                    const uint32_t off2 = (uint32_t)(a0 + co2 * ac + rd2 * ap) & 3u;
-                    const int hd2 = (int)((4u - off2) & 3u);
-                    const int head = run < hd2 ? run : hd2;
-                    const int mid2 = run > hd2 ? (run - hd2) & ~3 : 0;
-                    const int tail0 = head + mid2;
-                    float *yc2 = y0 + co2 * cstride + rd2 * plane;
-                    const float *sc2 = og + rd2 * RDS + co2 * CH + a0;
-                    if (lane < head) yc2[lane] = sc2[lane];
-                    if (tail0 + lane < run) yc2[tail0 + lane] = sc2[tail0 + lane];
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                tc::named_bar(gbar, 128);   // the staging block is complete
+
+                // ---- each (r_d, co) run: its 16-byte-aligned middle by one bulk copy,
+                // the at most 3 + 3 head and tail floats by plain stores.  Warp q takes
+                // channels 4q..4q+3 of both planes; lane i < 8 issues run i's copy.
+                const int run = nrows * Wo;
+                {
+                    const int i = lane & 7;
+                    const int rd = i >> 2, co = 4 * q + (i & 3);
+                    const uint32_t off = (uint32_t)(a0 + co * ac + rd * ap) & 3u;
+                    const int hd = (int)((4u - off) & 3u);
+                    const int mid = run > hd ? (run - hd) & ~3 : 0;
+                    float *yc = y0 + co * cstride + rd * plane;
+                    const float *sc = og + rd * RDS + co * CH + a0;
+                    if (lane < 8 && 2 * gmd + rd < Do && mid > 0) {
+                        bulk_store(yc + hd, sc + hd, (uint32_t)mid * 4u);
+                        bulk_commit();
+                    }
+    #pragma unroll 1
+                    for (int r = 0; r < 8; ++r) {   // head and tail of run r of this warp
+                        const int rd2 = r >> 2, co2 = 4 * q + (r & 3);
+                        if (2 * gmd + rd2 >= Do) break;
+                        const uint32_t off2 = (uint32_t)(a0 + co2 * ac + rd2 * ap) & 3u;
+                        const int hd2 = (int)((4u - off2) & 3u);
+                        const int head = run < hd2 ? run : hd2;
+                        const int mid2 = run > hd2 ? (run - hd2) & ~3 : 0;
+                        const int tail0 = head + mid2;
+                        float *yc2 = y0 + co2 * cstride + rd2 * plane;
+                        const float *sc2 = og + rd2 * RDS + co2 * CH + a0;
+                        if (lane < head) yc2[lane] = sc2[lane];
+                        if (tail0 + lane < run) yc2[tail0 + lane] = sc2[tail0 + lane];
+                    }
                 }
             }
         }
@@ -386,12 +454,15 @@ aps_status launch_convt3d_tc(const float *x, const int64_t in[5], const float *w
                       strides, box, estr))
         return APS_ERR_UNSUPPORTED;
     const int ac = (int)((Do * Ho * Wo) & 3), ap = (int)((Ho * Wo) & 3);
-    const size_t smem = (size_t)HEAD_BYTES +
-                        ((size_t)STAGES * stage_stride_of((int)Cin) +
-                         (size_t)GROUPS * staging_floats_of((int)Wo, ac, ap)) * 4;
-    const auto kern = Cin == 1 ? convt3d_tc_kernel<1>
-                    : Cin == 2 ? convt3d_tc_kernel<2>
-                               : convt3d_tc_kernel<3>;
+    const size_t smem =
+        (size_t)head_bytes_of((int)Cin) +
+        ((size_t)STAGES * stage_stride_of((int)Cin) +
+         (direct_of((int)Cin) ? 0 : (size_t)GROUPS * staging_floats_of((int)Wo, ac, ap))) * 4;
+    void (*const kerns[CIN_MAX])(const CUtensorMap, const float *, const float *, float *, int,
+                                 int, int, int, int, int, int, int, long long, unsigned int *) = {
+        convt3d_tc_kernel<1>, convt3d_tc_kernel<2>, convt3d_tc_kernel<3>, convt3d_tc_kernel<4>,
+        convt3d_tc_kernel<5>, convt3d_tc_kernel<6>, convt3d_tc_kernel<7>, convt3d_tc_kernel<8>};
+    const auto kern = kerns[Cin - 1];
     // one CTA per SM: each holds all 512 tensor-memory columns
     if (resident_ctas((const void *)kern, THREADS, (int)smem) < 1) return APS_ERR_UNSUPPORTED;
     const long long grid = std::min<long long>(sm_count(), n_units);

@@ -376,7 +376,7 @@ class GpuCase:
                 pairs *= convt_pairs(x.shape[2 + i], oshape[2 + i], p["k"][i], p["stride"][i],
                                      p["pad"][i], p["dil"][i])
             self.flops = 2 * x.shape[0] * x.shape[1] * p["c_out"] * pairs
-            self.tc = x.shape[1] <= 3 and x.shape[4] % 4 == 0 and x.shape[4] <= 32
+            self.tc = x.shape[1] <= 8 and x.shape[4] % 4 == 0 and x.shape[4] <= 32
             self.tensor_passes = 3 if self.tc else 0
             self.bound = "hbm" if self.tc else "hbm+alu"
         else:

@@ -246,14 +246,21 @@ def test_fused_general_geometry_tables(xs, cout, k, s, p, op, d, q):
 
 # ------------------------------------------------------------ convtranspose3d
 CONVT3D_CASES = [  # (x shape, C_out, k, s, p, d, op, bias)
-    # the k3 s2 p1 d1 kernel: one and two column blocks, C_in 1..8, output padding
-    ((2, 3, 5, 9, 12), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (0, 0, 0), True),
+    # W > 32: the FP32-pipe k3 s2 p1 d1 kernel (one and two column blocks, C_in 1..8,
+    # output padding)
     ((1, 3, 4, 19, 36), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (0, 0, 0), True),
+    ((1, 8, 3, 9, 40), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (1, 1, 1), False),
+    ((1, 5, 2, 7, 36), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (0, 1, 0), True),
+    ((1, 3, 2, 2, 68), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (1, 0, 1), True),
+    # W <= 32: the tensor-core kernel, C_in 1..3 with staged output runs and C_in 4..8
+    # with outputs from registers (output padding in every dim, H not a multiple of 4, a
+    # single input plane, no bias)
+    ((2, 3, 5, 9, 12), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (0, 0, 0), True),
     ((2, 8, 3, 17, 8), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (1, 1, 1), False),
     ((1, 1, 6, 6, 4), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (0, 1, 0), True),
-    ((1, 3, 2, 2, 68), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (1, 0, 1), True),
-    # C_in <= 3, W <= 32: the tensor-core kernel (output padding in every dim, H not a
-    # multiple of 4, a single input plane, no bias)
+    ((1, 5, 3, 6, 32), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (0, 0, 1), True),
+    ((2, 4, 4, 9, 20), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (1, 0, 0), True),
+    ((1, 7, 2, 5, 12), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (0, 0, 0), False),
     ((3, 2, 3, 9, 16), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (1, 1, 1), True),
     ((1, 3, 1, 7, 32), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (0, 0, 0), False),
     ((2, 1, 4, 4, 28), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (1, 0, 1), True),
@@ -275,9 +282,10 @@ def test_convt3d_cases(xs, cout, k, s, p, d, op, has_bias):
                  what=f"convt3d {xs} k{k} s{s} p{p} d{d} op{op}")
 
 
-# C_in 8 (and C_in 3 at W 36): the FP32-pipe kernel, with ~1500 units, several per CTA of
-# its persistent grid, so its double-buffered ring wraps many times
-@pytest.mark.parametrize("xs", [(48, 8, 16, 3, 4), (24, 3, 16, 3, 36)])
+# ~1500 units, several per CTA of the persistent grids, so the input rings wrap many
+# times: C_in 8 at W 4 (tensor cores, outputs from registers), C_in 3 and 8 at W 36 (the
+# FP32-pipe kernel)
+@pytest.mark.parametrize("xs", [(48, 8, 16, 3, 4), (24, 3, 16, 3, 36), (12, 8, 16, 3, 36)])
 def test_convt3d_fp32_kernel_many_units_per_cta(xs):
     x, = rng_inputs(47, xs)
     w, b = rng_inputs(48, (xs[1], 16, 3, 3, 3), (16,), lo=-0.3, hi=0.3)
