@@ -19,9 +19,10 @@
 // divided by the number of classes that have taps; it is persistent and walks
 // (batch row, m-tile) units.  A warp owns 8 output channels and each lane Q
 // consecutive m.  Input channels stream through shared memory in chunks of 8
-// with one continuous double-buffered cp.async pipeline over the CTA's
-// (unit, chunk) sequence: warp w stages channel w of the chunk's window
-// (32*Q + span samples, zero outside [0, L)).  Window rows are padded by one
+// (16, through three stages, where the resident weights leave room) with one
+// continuous cp.async pipeline over the CTA's (unit, chunk) sequence: warp w
+// stages channels w, w + 8 of the chunk's window (32*Q + span samples, zero
+// outside [0, L)).  Window rows are padded by one
 // word per Q samples, so lane l's j-th window register sits at row offset
 // (Q+1)*l + j + j/Q -- an immediate per j -- and, Q+1 being odd, the 32 lanes
 // hit 32 different banks.  The weights, stored [ci][k][co] so a warp's 8
@@ -46,6 +47,12 @@ constexpr int WARPS = THREADS / 32;
 constexpr int CO_T = 8;                 // output channels per warp
 constexpr int CO_B = WARPS * CO_T;      // 64 output channels per CTA
 constexpr int CI_C = WARPS;             // input channels per staged chunk (one per warp)
+// "wide" staging: 16 channels per chunk through 3 window stages (one CTA barrier
+// per chunk instead of two, half as many chunks), used when the resident weights
+// leave room for it: 1720 -> 1632 us on the stride-1 K5 workload; the strided K4
+// workload's weights leave no room (staging its weights per chunk was slower)
+constexpr int CI_W = 2 * WARPS;
+constexpr int NB_W = 3;
 // Resident weights while the CTA's shared memory stays within this, so that
 // two CTAs share an SM.
 constexpr int RESIDENT_SMEM = 110 * 1024;
@@ -93,10 +100,11 @@ struct Taps {
     static constexpr int XP = XW + XW / Q + 1;           // padded row (one word per Q)
     static constexpr int XS = CI_C * XP;                 // floats per window stage
     static constexpr int WC = CI_C * K * CO_B;           // floats of one chunk's weights
+    static constexpr int XS_W = CI_W * XP;               // ... with wide staging
 };
 }  // namespace ct1
 
-template <int S, int K, int DIL, int PL, bool RES>
+template <int S, int K, int DIL, int PL, bool RES, bool WIDE>
 __global__ void __launch_bounds__(ct1::THREADS, 2)
     convt1d_tiled_kernel(const float *__restrict__ x, const float *__restrict__ w,
                          const float *__restrict__ bias, float *__restrict__ y, int Cin,
@@ -106,16 +114,19 @@ __global__ void __launch_bounds__(ct1::THREADS, 2)
     pdl_wait();
     using namespace ct1;
     using T = Taps<S, K, DIL, PL>;
-    constexpr int XW = T::XW, XP = T::XP, XS = T::XS, WC = T::WC;
+    static_assert(RES || !WIDE, "wide staging keeps the weights resident");
+    constexpr int CIC = WIDE ? CI_W : CI_C;   // channels per chunk
+    constexpr int NB = WIDE ? NB_W : 2;       // window stages
+    constexpr int XW = T::XW, XP = T::XP, XS = CIC * XP, WC = T::WC;
     constexpr int SPAN = T::SPAN, E_MIN = T::E_MIN, Q = T::Q, TM = T::TM;
     extern __shared__ __align__(16) float sm[];
     // resident: ws = [Cin][K][CO_B]; staged: ws = [2][CI_C][K][CO_B]
     float *ws = sm;
-    float *xs = sm + (RES ? (size_t)Cin * K * CO_B : (size_t)2 * WC);   // [2][CI_C][XP]
+    float *xs = sm + (RES ? (size_t)Cin * K * CO_B : (size_t)2 * WC);   // [NB][CIC][XP]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int co_base = blockIdx.y * CO_B;
-    const int nchunks = (Cin + CI_C - 1) / CI_C;
+    const int nchunks = (Cin + CIC - 1) / CIC;
 
     // weights of input channels c0 .. c0+nci-1: global [ci][co][k] -> shared
     // [ci - c0][k][co] (zeros for channels past C_out)
@@ -142,20 +153,22 @@ __global__ void __launch_bounds__(ct1::THREADS, 2)
     // (xn) and its window start i_lo; samples j in [j_lo, j_hi) lie inside
     // [0, L), the rest are zeros.
     auto stage = [&](const float *xn, long long i_lo, int c0, int b) {
-        if (!RES) load_w(c0, min(CI_C, Cin - c0), ws + b * WC, true);
+        if (!RES) load_w(c0, min(CIC, Cin - c0), ws + b * WC, true);
         const long long rem = (long long)L - i_lo;   // samples left in the row
         const int j_lo = i_lo >= 0 ? 0 : (-i_lo < XW ? (int)-i_lo : XW);
         const int j_hi = rem <= 0 ? 0 : (rem < XW ? (int)rem : XW);
-        const bool chan = c0 + warp < Cin;
-        const float *src = xn + (long long)(chan ? c0 + warp : 0) * L + i_lo + lane;
-        const uint32_t dst = smem_u32(xs + b * XS + warp * XP + lane + lane / Q);
+        for (int cw = warp; cw < CIC; cw += WARPS) {
+            const bool chan = c0 + cw < Cin;
+            const float *src = xn + (long long)(chan ? c0 + cw : 0) * L + i_lo + lane;
+            const uint32_t dst = smem_u32(xs + b * XS + cw * XP + lane + lane / Q);
 #pragma unroll 3
-        for (int j = lane, t = 0; j < XW; j += 32, ++t) {
-            const bool in = chan && j >= j_lo && j < j_hi;
-            asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(
-                             dst + 4u * (uint32_t)(t * (32 + 32 / Q))),
-                         "l"(in ? src + 32 * t : x), "r"(in ? 4 : 0)
-                         : "memory");
+            for (int j = lane, t = 0; j < XW; j += 32, ++t) {
+                const bool in = chan && j >= j_lo && j < j_hi;
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(
+                                 dst + 4u * (uint32_t)(t * (32 + 32 / Q))),
+                             "l"(in ? src + 32 * t : x), "r"(in ? 4 : 0)
+                             : "memory");
+            }
         }
     };
     auto unit_origin = [&](long long u, const float *&xn, long long &i_lo) {
@@ -186,7 +199,8 @@ __global__ void __launch_bounds__(ct1::THREADS, 2)
             un = u + gridDim.x;
             if (un < n_units) unit_origin(un, xn_next, i_lo_next);
         }
-        if (un < n_units) stage(xn_next, i_lo_next, chn * CI_C, b ^ 1);
+        const int bn = b + 1 == NB ? 0 : b + 1;
+        if (un < n_units) stage(xn_next, i_lo_next, chn * CIC, bn);
         cp_async_commit();
         cp_async_wait<1>();
         __syncthreads();
@@ -199,8 +213,8 @@ __global__ void __launch_bounds__(ct1::THREADS, 2)
                     for (int r = 0; r < S; ++r) acc[c2][q][r] = make_float2(0.f, 0.f);
         }
         const float *xl = xs + b * XS + (Q + 1) * lane;
-        const float *wb = (RES ? ws + (size_t)ch * WC : ws + b * WC) + warp * CO_T;
-        const int nci = min(CI_C, Cin - ch * CI_C);
+        const float *wb = (RES ? ws + (size_t)ch * CIC * K * CO_B : ws + b * WC) + warp * CO_T;
+        const int nci = min(CIC, Cin - ch * CIC);
 #pragma unroll 1
         for (int cl = 0; cl < nci; ++cl) {
             float xr[Q + SPAN];
@@ -225,7 +239,10 @@ __global__ void __launch_bounds__(ct1::THREADS, 2)
                 }
             }
         }
-        __syncthreads();   // buffer b is free for the stage issued next iteration
+        // buffer b is free for the stage issued next iteration (with three stages,
+        // the next stage goes to the buffer every warp left before this
+        // iteration's barrier)
+        if (NB == 2) __syncthreads();
         if (ch == nchunks - 1) {
             // ---- epilogue: bias, then Q*S consecutive outputs per channel
             const long long n = u / n_mtiles;
@@ -259,7 +276,7 @@ __global__ void __launch_bounds__(ct1::THREADS, 2)
         }
         u = un;
         ch = chn;
-        b ^= 1;
+        b = bn;
         xn = xn_next;
         i_lo = i_lo_next;
     }
@@ -279,12 +296,15 @@ static aps_status launch_tiled(const float *x, const int64_t in[3], const float 
     const int vec = (l_out % 4 == 0) && (reinterpret_cast<uintptr_t>(y) % 16 == 0);
     // resident weights when the CTA's slab and two window stages leave room for
     // two CTAs per SM, otherwise weights staged with each chunk
+    const int64_t wsmem = (in[1] * K * CO_B + NB_W * T::XS_W) * 4;
     const int64_t rsmem = (in[1] * K * CO_B + 2 * T::XS) * 4;
     const int ssmem = (2 * T::WC + 2 * T::XS) * 4;
+    const bool wide = wsmem <= RESIDENT_SMEM && in[1] >= CI_W;
     const bool res = rsmem <= RESIDENT_SMEM;
-    const auto kern = res ? convt1d_tiled_kernel<S, K, DIL, PL, true>
-                          : convt1d_tiled_kernel<S, K, DIL, PL, false>;
-    const int smem = res ? (int)rsmem : ssmem;
+    const auto kern = wide ? convt1d_tiled_kernel<S, K, DIL, PL, true, true>
+                    : res  ? convt1d_tiled_kernel<S, K, DIL, PL, true, false>
+                           : convt1d_tiled_kernel<S, K, DIL, PL, false, false>;
+    const int smem = wide ? (int)wsmem : res ? (int)rsmem : ssmem;
     const int per_sm = resident_ctas((const void *)kern, THREADS, smem);
     if (per_sm < 1) return APS_ERR_CUDA;
     const long long slots = std::max<long long>(1, (long long)per_sm * sm_count() / gy);

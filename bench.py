@@ -192,10 +192,10 @@ def traffic_from_profile(kernel_file, profile_name, key):
 PROFILE_OF = {
     "avgpool": ("avgpool3d.cu", "avgpool3d_k3s2p1_tma.md"),
     "avgpool_nopad": ("avgpool3d.cu", "avgpool3d_k3s2p1_tma.md"),
-    "avgpool_k2": ("avgpool3d.cu", "avgpool3d_direct_k2s2.md"),
+    "avgpool_k2": ("avgpool3d.cu", "avgpool3d_win_k2s2.md"),
     "fused": ("ct3d_pool_tc.cu", "ct3d_pool2_tc_fused.md"),
     "fused_cin8": ("ct3d_pool.cu", "ct3d_pool2_fast_fused_cin8.md"),
-    "fused_op1": ("ct3d_pool.cu", "ct3d_pool_direct_op1.md"),
+    "fused_op1": ("ct3d_pool_gen.cu", "ct3d_pool_gen_op1.md"),
     "convt1d": ("convt1d.cu", "convt1d_tiled_fp32.md"),
     "convt1d_strided": ("convt1d.cu", "convt1d_tiled_fp32.md"),
     "convt1d_tf32": ("convt1d_tc.cu", "convt1d_tf32.md"),
@@ -203,7 +203,7 @@ PROFILE_OF = {
     "convt1d_tf32x3": ("convt1d_tc.cu", "convt1d_tf32x3.md"),
     "convt1d_strided_tf32x3": ("convt1d_tc.cu", "convt1d_tf32x3.md"),
     "convt3d": ("convt3d_tc.cu", "convt3d_tc_k3s2p1.md"),
-    "convt3d_cin8": ("convt3d.cu", "convt3d_k3s2p1_cin8.md"),
+    "convt3d_cin8": ("convt3d_tc.cu", "convt3d_tc_k3s2p1_cin8.md"),
 }
 
 # per-config workloads: key, workload id, ConvTranspose1d precision, timing mode

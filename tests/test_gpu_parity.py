@@ -421,6 +421,10 @@ CONVT_CASES = [  # (s, K, d, p, op, Cin, Cout, L, bias)
     (1, 5, 3, 0, 0, 4, 12, 40, True),
     (1, 1, 1, 0, 0, 1, 8, 1, True),
     (4, 3, 5, 2, 3, 2, 3, 11, True),
+    # 16-channel chunks through three window stages (resident weights with room to
+    # spare), with a ragged last chunk
+    (2, 4, 1, 1, 1, 40, 32, 200, True),
+    (1, 5, 3, 0, 0, 24, 64, 333, True),
     # weight slabs too large to stay resident: staged with each input chunk
     (2, 4, 2, 1, 1, 128, 64, 300, True),
     (1, 5, 3, 0, 0, 96, 64, 700, False),
