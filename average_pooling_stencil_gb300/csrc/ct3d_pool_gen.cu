@@ -134,48 +134,77 @@ __global__ void __launch_bounds__(gen::THREADS)
         const int combo = (fd * GH.T + fh) * GW.T + fw;
         const float *xn = x + n * Cin * in_plane;
         float *yp = y + n * Cout * out_plane + ((long long)pd * Ho + ph) * Wo + pw;
+        // ND > 0: the cells of this position (offsets within an input plane and
+        // whether they lie inside it) once, for every channel block and input
+        // channel
+        constexpr int NC = ND > 0 ? ND * ND * ND : 1;
+        int coff[NC];
+        unsigned cin_mask = 0;
+        if constexpr (ND > 0) {
+#pragma unroll
+            for (int a = 0; a < ND; ++a)
+#pragma unroll
+                for (int b = 0; b < ND; ++b)
+#pragma unroll
+                    for (int c = 0; c < ND; ++c) {
+                        const int e = (a * ND + b) * ND + c;
+                        const bool in = a >= d0 && a < d1 && b >= h0 && b < h1 && c >= w0 &&
+                                        c < w1;
+                        coff[e] = in ? ((bd + a) * H + (bh + b)) * W + (bw + c) : 0;
+                        cin_mask |= (in ? 1u : 0u) << e;
+                    }
+        }
         for (int co0 = 0; co0 < Cout; co0 += CO_T) {
             float acc[CO_T];
 #pragma unroll
             for (int j = 0; j < CO_T; ++j) acc[j] = 0.f;
-            for (int ci = 0; ci < Cin; ++ci) {
-                const float *xc = xn + ci * in_plane;
-                const float *wc = weff + ((long long)(combo * Cin + ci) * taps) * COP + co0;
-                if constexpr (ND > 0) {
-                    // taps beyond a phase's count have zero weights, so cells past
-                    // the end of the input or of the phase load nothing and add 0
-                    float xv[ND][ND][ND];
+            if constexpr (ND > 0) {
+                // channel pairs by the packed fp32x2 FMA (two exactly rounded FMAs
+                // per instruction)
+                float2 acc2[CO_T / 2];
 #pragma unroll
-                    for (int a = 0; a < ND; ++a)
+                for (int j = 0; j < CO_T / 2; ++j) acc2[j] = make_float2(0.f, 0.f);
+                // the cells of input channel ci + 1 load while channel ci's FMAs
+                // run (two register sets, the loop unrolled by two)
+                auto load = [&](float (&xv)[NC], int ci) {
+                    const float *xc = xn + ci * in_plane;
 #pragma unroll
-                        for (int b = 0; b < ND; ++b)
+                    for (int e = 0; e < NC; ++e)
+                        xv[e] = (cin_mask >> e) & 1u ? __ldg(xc + coff[e]) : 0.f;
+                };
+                auto fma = [&](const float (&xv)[NC], int ci) {
+                    const float *wc = weff + ((long long)(combo * Cin + ci) * NC) * COP + co0;
 #pragma unroll
-                            for (int c = 0; c < ND; ++c) {
-                                const bool in = a >= d0 && a < d1 && b >= h0 && b < h1 &&
-                                                c >= w0 && c < w1;
-                                xv[a][b][c] =
-                                    in ? __ldg(xc + ((long long)(bd + a) * H + (bh + b)) * W +
-                                               (bw + c))
-                                       : 0.f;
-                            }
+                    for (int e = 0; e < NC; ++e) {
+                        const float4 *w4 = reinterpret_cast<const float4 *>(wc + e * COP);
+                        const float2 xx = make_float2(xv[e], xv[e]);
 #pragma unroll
-                    for (int a = 0; a < ND; ++a)
+                        for (int j = 0; j < CO_T / 4; ++j) {
+                            const float4 q4 = w4[j];
+                            acc2[2 * j] = __ffma2_rn(xx, make_float2(q4.x, q4.y), acc2[2 * j]);
+                            acc2[2 * j + 1] =
+                                __ffma2_rn(xx, make_float2(q4.z, q4.w), acc2[2 * j + 1]);
+                        }
+                    }
+                };
+                float xa[NC], xb[NC];
+                if (Cin > 0) load(xa, 0);
+                for (int ci = 0; ci < Cin; ci += 2) {
+                    if (ci + 1 < Cin) load(xb, ci + 1);
+                    fma(xa, ci);
+                    if (ci + 1 >= Cin) break;
+                    if (ci + 2 < Cin) load(xa, ci + 2);
+                    fma(xb, ci + 1);
+                }
 #pragma unroll
-                        for (int b = 0; b < ND; ++b)
-#pragma unroll
-                            for (int c = 0; c < ND; ++c) {
-                                const float4 *w4 = reinterpret_cast<const float4 *>(
-                                    wc + ((a * MH + b) * MW + c) * COP);
-#pragma unroll
-                                for (int j = 0; j < CO_T / 4; ++j) {
-                                    const float4 q4 = w4[j];
-                                    acc[4 * j + 0] = fmaf(xv[a][b][c], q4.x, acc[4 * j + 0]);
-                                    acc[4 * j + 1] = fmaf(xv[a][b][c], q4.y, acc[4 * j + 1]);
-                                    acc[4 * j + 2] = fmaf(xv[a][b][c], q4.z, acc[4 * j + 2]);
-                                    acc[4 * j + 3] = fmaf(xv[a][b][c], q4.w, acc[4 * j + 3]);
-                                }
-                            }
-                } else {
+                for (int j = 0; j < CO_T / 2; ++j) {
+                    acc[2 * j] = acc2[j].x;
+                    acc[2 * j + 1] = acc2[j].y;
+                }
+            } else {
+                for (int ci = 0; ci < Cin; ++ci) {
+                    const float *xc = xn + ci * in_plane;
+                    const float *wc = weff + ((long long)(combo * Cin + ci) * taps) * COP + co0;
                     for (int a = d0; a < d1; ++a)
                         for (int b = h0; b < h1; ++b) {
                             const float *xr = xc + ((long long)(bd + a) * H + (bh + b)) * W + bw;
@@ -267,6 +296,8 @@ aps_status launch_ct3d_pool_gen(const float *x, const int64_t in[5], const float
                                 const int64_t out[5], cudaStream_t st) {
     using namespace gen;
     if (pool_k > 64) return APS_ERR_UNSUPPORTED;   // o and the tap loops stay small
+    // cell offsets within an input plane in 32 bits
+    if (in[2] * in[3] * in[4] >= ((int64_t)1 << 31)) return APS_ERR_UNSUPPORTED;
     gen::Geom g;
     for (int i = 0; i < 3; ++i)
         if (!build_dim(k[i], s[i], p[i], d[i], pool_k, g.d[i])) return APS_ERR_UNSUPPORTED;
