@@ -39,7 +39,7 @@ EXPORTS = [
     "aps_ct3d_scale_pool_bias_out_shape", "aps_ct3d_scale_pool_bias",
     "aps_convtranspose3d_out_shape", "aps_convtranspose3d",
     "aps_convtranspose1d_out_shape", "aps_convtranspose1d", "aps_device_status",
-    "aps_fp32_fma_probe", "aps_debug_fail_launches",
+    "aps_fp32_fma_probe", "aps_debug_fail_launches", "aps_debug_stall_next_pool",
 ]
 
 _lib = None
@@ -85,8 +85,11 @@ def lib():
         L.aps_fp32_fma_probe.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _VP, _VP]
         L.aps_debug_fail_launches.argtypes = [ctypes.c_int]
         L.aps_debug_fail_launches.restype = None
+        L.aps_debug_stall_next_pool.argtypes = [ctypes.c_ulonglong]
+        L.aps_debug_stall_next_pool.restype = None
         for name in EXPORTS:
-            if name not in ("aps_status_string", "aps_abi_version", "aps_debug_fail_launches"):
+            if name not in ("aps_status_string", "aps_abi_version", "aps_debug_fail_launches",
+                            "aps_debug_stall_next_pool"):
                 getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -181,6 +184,12 @@ APS_PROBE_THREADS = 256
 def aps_debug_fail_launches(n: int) -> None:
     """Test hook: the next n launches report APS_ERR_LAUNCH (the kernels still run)."""
     lib().aps_debug_fail_launches(int(n))
+
+
+def aps_debug_stall_next_pool(wait_limit_ns: int) -> None:
+    """Test hook: the next TMA-path avgpool launch withholds one input box and its
+    waits give up after wait_limit_ns (0 clears)."""
+    lib().aps_debug_stall_next_pool(int(wait_limit_ns))
 
 
 def aps_fp32_fma_probe(packed, blocks, iters, sink_ptr, stream=0) -> int:

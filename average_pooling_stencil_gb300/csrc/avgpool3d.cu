@@ -36,10 +36,16 @@
 //    last window of an odd extent also reaches past the high end).  Per dim
 //    the count is 3, less one at output 0 and less one where 2i + 1 is past
 //    the end; a thread takes the reciprocals of its products once per tile.
+#include <atomic>
+
 #include "aps_dev.cuh"
 #include "aps_internal.h"
 
 namespace aps {
+// aps_debug_stall_next_pool: the wait limit (ns) of the next TMA pool launch, which
+// also withholds its first input box; 0 = no stall.
+static std::atomic<unsigned long long> g_stall_next_pool{0};
+
 namespace pool {
 constexpr int TW = 64;               // output columns per tile (2 per lane)
 constexpr int TH = 16;               // output rows per tile (1 per consumer warp)
@@ -64,7 +70,8 @@ template <bool CIP>
 __global__ void __launch_bounds__(pool::THREADS)
     avgpool3d_k3s2p1_tma_kernel(const __grid_constant__ CUtensorMap xmap, float *__restrict__ y,
                                 int D, int H, int W, int Do, int Ho, int Wo, int n_ht, int n_wt,
-                                long long n_units, unsigned int *status) {
+                                long long n_units, unsigned int *status,
+                                unsigned long long wait_ns, int withhold_first_box) {
     using namespace pool;
     extern __shared__ __align__(1024) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_STRIDE);
@@ -99,7 +106,7 @@ __global__ void __launch_bounds__(pool::THREADS)
                 for (int od = 0; od < Do; ++od, ++it) {
                     const uint32_t slot = it % STAGES;
                     if (it >= (uint32_t)STAGES &&
-                        !mbar_wait(&empty[slot], ((it / STAGES) & 1u) ^ 1u)) {
+                        !mbar_wait_for(&empty[slot], ((it / STAGES) & 1u) ^ 1u, wait_ns)) {
                         record_error(status, APS_DEVERR_TIMEOUT);
                         abort_flag = 1;
                         ok = false;
@@ -107,15 +114,18 @@ __global__ void __launch_bounds__(pool::THREADS)
                     }
                     if (abort_flag) { ok = false; break; }
                     mbar_arrive_expect_tx(&full[slot], STAGE_BYTES);
+                    // the test hook's withheld box: its barrier expects bytes that never come
+                    if (withhold_first_box && blockIdx.x == 0 && it == 0) continue;
                     tma_load_4d(smem + slot * STAGE_STRIDE, &xmap, &full[slot], c0, c1, 2 * od,
                                 nc);
                 }
             }
             if (!ok) {
-                // Let every box still in flight land before the CTA exits.
+                // Let every box still in flight land before the CTA exits (a box
+                // whose wait runs out does not end the waits for the others).
                 const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
                 for (uint32_t j = first; j < it; ++j)
-                    if (!mbar_wait(&full[j % STAGES], (j / STAGES) & 1u)) break;
+                    mbar_wait_for(&full[j % STAGES], (j / STAGES) & 1u, wait_ns);
             }
         }
         return;
@@ -148,7 +158,7 @@ __global__ void __launch_bounds__(pool::THREADS)
         }
         for (int od = 0; od < Do; ++od, ++it) {
             const uint32_t slot = it % STAGES;
-            if (!mbar_wait(&full[slot], (it / STAGES) & 1u)) {
+            if (!mbar_wait_for(&full[slot], (it / STAGES) & 1u, wait_ns)) {
                 record_error(status, APS_DEVERR_TIMEOUT);
                 abort_flag = 1;
                 return;
@@ -215,9 +225,12 @@ aps_status launch_avgpool3d_k3s2p1_tma(const float *x, const int64_t in[5], floa
     const int per_sm = resident_ctas((const void *)kern, THREADS, SMEM_BYTES);
     if (per_sm < 1) return APS_ERR_CUDA;
     const long long grid = std::min<long long>(n_units, (long long)sm_count() * per_sm);
-    const cudaError_t e =
-        launch_plain(kern, dim3((unsigned)grid), dim3(THREADS), (size_t)SMEM_BYTES, st, map, y,
-                     (int)D, (int)H, (int)W, Do, Ho, Wo, n_ht, n_wt, n_units, status_word());
+    // the test hook (aps_debug_stall_next_pool) applies to one launch
+    const unsigned long long stall = g_stall_next_pool.exchange(0);
+    const cudaError_t e = launch_plain(
+        kern, dim3((unsigned)grid), dim3(THREADS), (size_t)SMEM_BYTES, st, map, y, (int)D, (int)H,
+        (int)W, Do, Ho, Wo, n_ht, n_wt, n_units, status_word(),
+        (unsigned long long)(stall ? stall : kWaitLimitNs), stall ? 1 : 0);
     return launch_status(e);
 }
 
@@ -330,3 +343,7 @@ aps_status launch_avgpool3d_direct(const float *x, const int64_t in[5], const in
 }
 
 }  // namespace aps
+
+extern "C" void aps_debug_stall_next_pool(unsigned long long wait_limit_ns) {
+    aps::g_stall_next_pool.store(wait_limit_ns);
+}

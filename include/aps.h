@@ -244,6 +244,17 @@ aps_status aps_fp32_fma_probe(int packed, int blocks, int iters, float *sink,
  * callers see it.  Host-only, thread-safe. */
 void aps_debug_fail_launches(int n);
 
+/* Test hook for a wait that runs out (not part of any op): the next
+ * aps_avgpool3d launch that takes the TMA-tiled kernel withholds the first
+ * input box of its first CTA -- the box's barrier still expects its bytes --
+ * and every pipeline wait of that launch gives up after wait_limit_ns instead
+ * of the usual 2 s.  The consumers of that CTA then record APS_DEVERR_TIMEOUT
+ * in the status word and return; its producer waits (bounded) for the boxes it
+ * did issue and returns; the other CTAs finish normally, and the CUDA context
+ * stays usable.  wait_limit_ns = 0 clears a pending stall.  Host-only,
+ * thread-safe; the CTA's outputs of that launch are left unwritten. */
+void aps_debug_stall_next_pool(unsigned long long wait_limit_ns);
+
 #ifdef __cplusplus
 }
 #endif

@@ -772,3 +772,23 @@ def test_a_rejected_launch_reaches_the_caller(name):
         B.aps_debug_fail_launches(0)
     run(out)
     assert_close(out.cpu().numpy(), want, tol=tol, what=name)
+
+
+def test_a_pipeline_wait_that_runs_out_is_recorded_and_the_context_stays_usable():
+    """A wait made to run out on the host's request (one input box withheld, its barrier
+    still expecting the bytes, a 50 ms limit): the launch returns, the kernel records
+    APS_DEVERR_TIMEOUT in the status word instead of hanging, and the next launch on the
+    same context is normal and correct."""
+    x = workloads.get(1).with_input_shape((2, 3, 9, 20, 68)).generate("x")
+    xd = dev(x)
+    st, _ = B.aps_device_status(clear=True)
+    assert st == 0
+    B.aps_debug_stall_next_pool(50_000_000)
+    B.avgpool3d(xd, 3, 2, 1)
+    torch.cuda.synchronize()
+    st, bits = B.aps_device_status(clear=True)
+    assert st == 0 and bits & B.APS_DEVERR_TIMEOUT, bits
+    y = B.avgpool3d(xd, 3, 2, 1)
+    assert_close(y.cpu().numpy(), ora.avgpool3d(x, 3, 2, 1, 1, 0), what="after a timed-out launch")
+    st, bits = B.aps_device_status(clear=True)
+    assert st == 0 and bits == 0
