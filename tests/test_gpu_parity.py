@@ -517,6 +517,10 @@ TF32X3_CASES = [  # (s, K, d, p, op, Cin, Cout, L, bias)
     (1, 1, 1, 0, 0, 24, 64, 4, True),
     (1, 3, 1, 1, 0, 16, 128, 200, True),   # paired hi | lo weights: one N = 256 MMA
     (2, 4, 1, 1, 1, 16, 64, 132, True),    # two classes, paired: N = 128, two accumulators
+    # stride 2 with the one class on even outputs (odd L_out: direct stores; L_out a
+    # multiple of 4: TMA stores)
+    (2, 2, 2, 0, 0, 32, 64, 200, True),
+    (2, 2, 4, 0, 1, 32, 64, 200, False),
 ]
 
 
