@@ -32,6 +32,7 @@ APS_DEVERR_TIMEOUT = 1
 APS_PREC_FP32 = 0
 APS_PREC_TF32 = 1
 APS_PREC_TF32X3 = 2
+APS_PREC_FP32_FMA = 3
 
 # Every symbol include/aps.h declares.
 EXPORTS = [

@@ -408,7 +408,7 @@ aps_status aps_convtranspose1d(const float *x, const int64_t in[3], const float 
     if (!present(x, numel(in, 3)) || !present(w, in[1]) || !present(y, numel(out, 3)))
         return APS_ERR_NULL;
     if (precision != APS_PREC_FP32 && precision != APS_PREC_TF32 &&
-        precision != APS_PREC_TF32X3)
+        precision != APS_PREC_TF32X3 && precision != APS_PREC_FP32_FMA)
         return APS_ERR_SHAPE;
     if (!aligned(x, 4) || !aligned(w, 4) || !aligned(y, 4) || (bias && !aligned(bias, 4)))
         return APS_ERR_ALIGN;
@@ -417,9 +417,14 @@ aps_status aps_convtranspose1d(const float *x, const int64_t in[3], const float 
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     // no input channels: every output is its bias (exact at any precision)
     if (in[1] == 0) return launch_convt1d_direct(x, in, w, bias, c_out, k, s, p, d, y, out[2], cs);
-    if (precision != APS_PREC_FP32)
+    if (precision == APS_PREC_TF32 || precision == APS_PREC_TF32X3)
         return launch_convt1d_tf32(x, in, w, bias, c_out, k, s, p, d, y, out[2],
                                    precision == APS_PREC_TF32X3, cs);
+    if (precision == APS_PREC_FP32) {
+        // fp32 accuracy: 3xTF32 on the tensor cores where the shape allows
+        st = launch_convt1d_tf32(x, in, w, bias, c_out, k, s, p, d, y, out[2], true, cs);
+        if (st != APS_ERR_UNSUPPORTED) return st;
+    }
     if (in[1] >= 1) {
         st = launch_convt1d_tiled(x, in, w, bias, c_out, k, s, p, d, y, out[2], cs);
         if (st != APS_ERR_UNSUPPORTED) return st;

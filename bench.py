@@ -61,8 +61,10 @@ def parse_args_from(argv):
     ap.add_argument("--e2e-steps", type=int, default=8, help="0 skips the e2e leg")
     ap.add_argument("--workload", type=int, default=HEADLINE_CFG,
                     help="workload of the headline line (default: the avgpool workload)")
-    ap.add_argument("--precision", choices=["fp32", "tf32", "tf32x3"], default="fp32",
-                    help="ConvTranspose1d precision of the headline workload")
+    ap.add_argument("--precision", choices=["fp32", "tf32", "tf32x3", "fp32_fma"],
+                    default="fp32",
+                    help="ConvTranspose1d precision of the headline workload (fp32: the "
+                         "library's choice at the fp32 bound; fp32_fma: the FP32 pipe)")
     ap.add_argument("--x-shape", type=str, default=None,
                     help="override the input shape of the headline workload (profiling "
                          "runs on small cases), e.g. 2,32,128,128,256")
@@ -206,7 +208,8 @@ PROFILE_OF = {
     "convt3d_cin8": ("convt3d_tc.cu", "convt3d_tc_k3s2p1_cin8.md"),
 }
 
-# per-config workloads: key, workload id, ConvTranspose1d precision, timing mode
+# per-config workloads: key, workload id, ConvTranspose1d precision (the C ABI's value:
+# 0 fp32 as the library routes it, 1 tf32, 2 3xTF32, 3 fp32 on the FP32 pipe), timing mode
 PER_CONFIG = [
     ("fused_tiny", 0, 0, "graph"),
     ("fused", 2, 0, "rotate"),
@@ -214,10 +217,10 @@ PER_CONFIG = [
     ("fused_op1", 7, 0, "rotate"),
     ("avgpool_nopad", 8, 0, "plain"),
     ("avgpool_k2", 9, 0, "plain"),
-    ("convt1d", 3, 0, "plain"),
+    ("convt1d", 3, 3, "plain"),
     ("convt1d_tf32", 3, 1, "plain"),
     ("convt1d_tf32x3", 3, 2, "plain"),
-    ("convt1d_strided", 4, 0, "plain"),
+    ("convt1d_strided", 4, 3, "plain"),
     ("convt1d_strided_tf32", 4, 1, "plain"),
     ("convt1d_strided_tf32x3", 4, 2, "plain"),
     ("convt3d", 5, 0, "plain"),
@@ -322,6 +325,7 @@ class GpuCase:
         from average_pooling_stencil_gb300 import workloads
         self.cfg = cfg
         self.precision = precision
+        self.kind = None          # ConvTranspose1d: the precision the library actually ran
         self.wl = wl = workloads.get(cfg)
         if x_shape is not None:
             self.wl = wl = wl.with_input_shape(x_shape)
@@ -384,12 +388,23 @@ class GpuCase:
                 x.shape, p["c_out"], p["k"], p["stride"], p["pad"], p["dil"], p["out_pad"])
             pairs = convt_pairs(x.shape[2], oshape[2], p["k"], p["stride"], p["pad"], p["dil"])
             self.flops = 2 * x.shape[0] * x.shape[1] * p["c_out"] * pairs
-            # fp32 FMA path is bound by the FP32 pipe; the tf32 tensor path by HBM
-            self.bound = "alu" if precision == 0 else "hbm"
-            self.tensor_passes = {0: 0, 1: 1, 2: 3}[precision]
         assert st == 0
         self.oshape = oshape
         self.y = torch.empty(oshape, device=dev, dtype=torch.float32)
+        if wl.op == "convtranspose1d":
+            # APS_PREC_FP32 runs the 3xTF32 kernel where it takes the shape, else
+            # the FP32 pipe: one 3xTF32 launch tells which
+            self.kind = precision
+            if precision == 0:
+                bias = self.d["bias"].data_ptr() if "bias" in self.d else 0
+                st = aps.binding.aps_convtranspose1d(
+                    self.d["x"].data_ptr(), x.shape, self.d["w"].data_ptr(), bias, p["c_out"],
+                    p["k"], p["stride"], p["pad"], p["dil"], p["out_pad"], 2,
+                    self.y.data_ptr(), torch.cuda.current_stream().cuda_stream)
+                self.kind = 2 if st == 0 else 3
+            # the FP32-pipe kernels are bound by the FP32 pipe, the tensor-core ones by HBM
+            self.bound = "alu" if self.kind == 3 else "hbm"
+            self.tensor_passes = {3: 0, 1: 1, 2: 3}[self.kind]
         self.bytes = 4 * (sum(numel(t.shape) for t in self.d.values()) + numel(oshape))
         self.outputs = numel(oshape)
         self.aps = aps
@@ -782,7 +797,7 @@ def run_native(args):
     # ---- headline: each rank runs its own full workload (weak scaling)
     x_shape = tuple(int(v) for v in args.x_shape.split(",")) if args.x_shape else None
     case = GpuCase(args.workload, torch, aps, with_host=args.e2e_steps > 0, x_shape=x_shape,
-                   precision={"fp32": 0, "tf32": 1, "tf32x3": 2}[args.precision])
+                   precision={"fp32": 0, "tf32": 1, "tf32x3": 2, "fp32_fma": 3}[args.precision])
     for _ in range(max(3, args.warmup)):
         case.launch()
     barrier()
@@ -849,11 +864,11 @@ def run_native(args):
                  "ct3d_scale_pool_bias": ("ct3d_pool2_tc_kernel" if case.tc
                                           else "ct3d_pool2_fast_kernel"),
                  "convtranspose3d": "convt3d_tc_kernel" if case.tc else "convt3d_k3s2p1_kernel",
-                 "convtranspose1d": ("convt1d_tf32_kernel" if case.precision
-                                     else "convt1d_tiled_kernel")}
+                 "convtranspose1d": ("convt1d_tiled_kernel" if case.kind == 3
+                                     else "convt1d_tf32_kernel")}
     roof["kernel"] = kernel_of[case.wl.op]
     roof["algorithmic_bytes_per_launch"] = case.bytes
-    hkey = case.wl.name + ("", "_tf32", "_tf32x3")[case.precision]
+    hkey = case.wl.name + {None: "", 3: "", 1: "_tf32", 2: "_tf32x3"}[case.kind]
     src = PROFILE_OF.get(hkey)
     traffic = (traffic_from_profile(src[0], src[1], hkey)
                if src is not None and x_shape is None else None)

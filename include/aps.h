@@ -86,12 +86,16 @@ typedef enum {
 #define APS_DEVERR_TIMEOUT 1u
 
 /* Precision choices of aps_convtranspose1d. */
-#define APS_PREC_FP32 0   /* fp32 FMA; max |y - exact| <= 1e-5 * (1 + |exact|) */
+#define APS_PREC_FP32 0   /* fp32 accuracy: max |y - exact| <= 1e-5 * (1 + |exact|);
+                             runs as APS_PREC_TF32X3 where that form accepts the shape
+                             (3x the speed at the same bound), else as APS_PREC_FP32_FMA */
 #define APS_PREC_TF32 1   /* tcgen05 tensor cores, tf32 operands, fp32 accumulate;
                              ||y - exact||_F <= 5e-3 * ||exact||_F */
 #define APS_PREC_TF32X3 2 /* tensor cores, each operand split v = hi + lo (tf32) and
                              each product summed as lo*hi + hi*lo + hi*hi (3xTF32);
                              max |y - exact| <= 1e-5 * (1 + |exact|), as fp32 */
+#define APS_PREC_FP32_FMA 3 /* fp32 FMAs on the FP32 pipe only (no tensor cores);
+                               max |y - exact| <= 1e-5 * (1 + |exact|) */
 
 /* Version of this ABI (bumped on any incompatible change). */
 int aps_abi_version(void);
@@ -194,8 +198,8 @@ aps_status aps_convtranspose3d(const float *x, const int64_t in_ncdhw[5], const 
  * x: [N, C_in, L]; w: [C_in, C_out, K]; bias: [C_out] or NULL (no bias);
  * y: [N, C_out, L_out] (shape from aps_convtranspose1d_out_shape).  Requires
  * K, s, d >= 1, p >= 0, 0 <= out_pad < max(s, d).  precision: APS_PREC_FP32,
- * APS_PREC_TF32 or APS_PREC_TF32X3 (tolerances above).  The two tensor-core
- * precisions return APS_ERR_UNSUPPORTED
+ * APS_PREC_TF32, APS_PREC_TF32X3 or APS_PREC_FP32_FMA (tolerances above).  The
+ * two explicit tensor-core precisions return APS_ERR_UNSUPPORTED
  * (nothing launched) unless: C_in % 8 == 0 and, above 32, C_in % 32 == 0;
  * C_out % 32 == 0 and (number of output residues mod s that some tap reaches)
  * x C_out <= 256; L % 4 == 0 and x 16-byte aligned; s <= 8, at most 4
@@ -204,7 +208,8 @@ aps_status aps_convtranspose3d(const float *x, const int64_t in_ncdhw[5], const 
  * and the weights (K*C_in*C_out*4 bytes, twice that for APS_PREC_TF32X3, which
  * also holds two copies of each converted stage and may stage 16 channels at a
  * time) plus the staging buffers fit in one CTA's 227 KB of shared memory.
- * APS_PREC_FP32 accepts every valid shape within the size limits above.
+ * APS_PREC_FP32 and APS_PREC_FP32_FMA accept every valid shape within the size
+ * limits above.
  */
 aps_status aps_convtranspose1d_out_shape(const int64_t in_ncl[3], int64_t c_out, int k,
                                          int stride, int pad, int dil, int out_pad,

@@ -32,6 +32,17 @@ def test_header_declares_the_binding_exports():
     assert header_functions() == sorted(B.EXPORTS)
 
 
+def test_header_constants_match_the_binding():
+    text = open(HEADER).read()
+    defines = dict(re.findall(r"#define\s+(APS_PREC_[A-Z0-9_]+)\s+(\d+)", text))
+    assert set(defines) == {"APS_PREC_FP32", "APS_PREC_TF32", "APS_PREC_TF32X3",
+                            "APS_PREC_FP32_FMA"}
+    for name, v in defines.items():
+        assert getattr(B, name) == int(v), name
+    for name, v in re.findall(r"\b(APS_(?:OK|ERR_[A-Z]+))\s*=\s*(-?\d+)", text):
+        assert getattr(B, name) == int(v), name
+
+
 def test_library_exports_every_declared_symbol():
     lib = ctypes.CDLL(B.LIB_PATH)
     for name in header_functions():

@@ -432,14 +432,18 @@ CONVT_CASES = [  # (s, K, d, p, op, Cin, Cout, L, bias)
 ]
 
 
+# APS_PREC_FP32_FMA: the FP32-pipe kernels; APS_PREC_FP32: the library's choice (the
+# 3xTF32 tensor-core kernel where it takes the shape, else the FP32 pipe), at the same bound
+@pytest.mark.parametrize("prec", [3, 0])
 @pytest.mark.parametrize("s,K,d,p,op,cin,cout,L,has_bias", CONVT_CASES)
-def test_convt1d_cases(s, K, d, p, op, cin, cout, L, has_bias):
+def test_convt1d_cases(s, K, d, p, op, cin, cout, L, has_bias, prec):
     x, = rng_inputs(11, (2, cin, L))
     w, b = rng_inputs(12, (cin, cout, K), (cout,), lo=-0.3, hi=0.3)
     b = b if has_bias else None
-    y = B.convtranspose1d(dev(x), dev(w), None if b is None else dev(b), s, p, d, op)
+    y = B.convtranspose1d(dev(x), dev(w), None if b is None else dev(b), s, p, d, op,
+                          precision=prec)
     assert_close(y.cpu().numpy(), ora.convt(x, w, b, s, p, d, op),
-                 what=f"convt1d s{s} K{K} d{d} p{p} op{op} {cin}->{cout} L{L}")
+                 what=f"convt1d s{s} K{K} d{d} p{p} op{op} {cin}->{cout} L{L} prec {prec}")
 
 
 def test_convt1d_unaligned_output():
@@ -448,7 +452,8 @@ def test_convt1d_unaligned_output():
     L_out = 129 + 12
     buf = torch.empty(2 * 16 * L_out + 1, device="cuda")
     out = buf[1:].view(2, 16, L_out)
-    B.convtranspose1d(dev(x), dev(w), None, 1, 0, 3, 0, out=out)
+    B.convtranspose1d(dev(x), dev(w), None, 1, 0, 3, 0, out=out,
+                      precision=B.APS_PREC_FP32_FMA)
     assert_close(out.cpu().numpy(), ora.convt(x, w, None, 1, 0, 3, 0), what="unaligned out")
 
 
@@ -460,7 +465,7 @@ def test_convt1d_full_workload_sampled_planes(cfg):
     x, w = wl.generate("x"), wl.generate("w")
     b = wl.generate("bias") if p["has_bias"] else None
     y = B.convtranspose1d(dev(x), dev(w), None if b is None else dev(b), p["stride"], p["pad"],
-                          p["dil"], p["out_pad"])
+                          p["dil"], p["out_pad"], precision=B.APS_PREC_FP32_FMA)
     torch.cuda.synchronize()
     N, C = y.shape[0], y.shape[1]
     sel = [(0, 0), (N - 1, C - 1), (N // 2, 17), (3, C // 2), (N - 1, 0)]
@@ -619,7 +624,7 @@ def test_empty_batch_every_op():
     y = B.convtranspose3d(torch.empty((0, 3, 4, 4, 4), device="cuda"), w3, b, 2, 1, 1, 0)
     assert tuple(y.shape) == (0, 16, 7, 7, 7)
     w1, b1 = (dev(a) for a in rng_inputs(42, (32, 64, 5), (64,)))
-    for prec in (B.APS_PREC_FP32, B.APS_PREC_TF32, B.APS_PREC_TF32X3):
+    for prec in (B.APS_PREC_FP32, B.APS_PREC_TF32, B.APS_PREC_TF32X3, B.APS_PREC_FP32_FMA):
         y = B.convtranspose1d(torch.empty((0, 32, 100), device="cuda"), w1, b1, 1, 0, 3, 0,
                               precision=prec)
         assert tuple(y.shape) == (0, 64, 112)
@@ -630,7 +635,7 @@ def test_zero_input_channels_give_the_bias():
     b1, = rng_inputs(43, (8,))
     x1, w1 = np.zeros((2, 0, 9), np.float32), np.zeros((0, 8, 3), np.float32)
     want = ora.convt(x1, w1, b1, 2, 1, 1, 0)
-    for prec in (B.APS_PREC_FP32, B.APS_PREC_TF32, B.APS_PREC_TF32X3):
+    for prec in (B.APS_PREC_FP32, B.APS_PREC_TF32, B.APS_PREC_TF32X3, B.APS_PREC_FP32_FMA):
         y = B.convtranspose1d(torch.empty((2, 0, 9), device="cuda"),
                               torch.empty((0, 8, 3), device="cuda"), dev(b1), 2, 1, 1, 0,
                               precision=prec)
@@ -718,7 +723,7 @@ def _canary_cases():
         return want, lambda out: B.convtranspose1d(
             dev(x), dev(w), dev(b), p["stride"], p["pad"], p["dil"], p["out_pad"],
             precision=prec, out=out), tol
-    cases["convt1d_fp32"] = lambda: convt1d(base4, (2, 64, 300), B.APS_PREC_FP32, 1e-5)
+    cases["convt1d_fp32"] = lambda: convt1d(base4, (2, 64, 300), B.APS_PREC_FP32_FMA, 1e-5)
     cases["convt1d_tf32"] = lambda: convt1d(base3, (2, 32, 400), B.APS_PREC_TF32, None)
     cases["convt1d_tf32x3"] = lambda: convt1d(base3, (2, 32, 400), B.APS_PREC_TF32X3, 1e-5)
 
