@@ -320,7 +320,7 @@ aps_status aps_ct3d_scale_pool_bias(const float *x, const int64_t in[5], const f
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     bool fast = pool_k == 2 && c_out == 16 && in[1] >= 1 && in[1] <= 8;
     for (int i = 0; i < 3; ++i)
-        fast = fast && k[i] == 3 && s[i] == 2 && p[i] == 1 && op[i] == 0 && d[i] == 1;
+        fast = fast && k[i] == 3 && s[i] == 2 && p[i] == 1 && op[i] <= 1 && d[i] == 1;
     if (fast) {
         // tensor cores (C_in <= 3, 16-byte input rows), else the FP32-pipe kernel
         st = launch_ct3d_pool2_tc(x, in, w, conv_bias, bias, scale1, scale2, y, out, cs);

@@ -1,7 +1,7 @@
 // ct3d_pool.cu -- fused ConvTranspose3d -> x scale1 -> AvgPool3d(pool_k) ->
 // + bias -> x scale2 (the model of Kimi-K2.6__l2_p50).
 //
-// Fast path (k3, s2, p1, output_padding 0, dilation 1, pool 2, C_out = 16):
+// Fast path (k3, s2, p1, output_padding 0 or 1, dilation 1, pool 2, C_out = 16):
 // per dimension an even pre-pool position 2d takes input d with tap 1 and an
 // odd one 2d+1 takes input d with tap 2 and input d+1 with tap 0 (the page's
 // per-parity analysis).  Averaging the 2x2x2 window therefore touches only the
@@ -13,7 +13,10 @@
 //     beff[co]          = (conv_bias[co]*scale1 + bias[co]) * scale2
 // and the pooled output is the 2x2x2 valid correlation
 //     y[n,co,d,h,w] = beff[co] + sum_ci sum_abc x[n,ci,d+a,h+b,w+c] * Weff[ci,co,a,b,c],
-// with pooled size = input size - 1 in each dim.  This equals the literal
+// with pooled size = input size - 1 in a dim with output_padding 0 and = input
+// size with output_padding 1: the extra pooled position averages pre-pool
+// positions 2D-2 and 2D-1, the latter the output_padding row, whose input
+// offset 1 lies past the end of x and counts as zero.  This equals the literal
 // chain in exact arithmetic; in fp32 it differs by rounding only (the page
 // argues the reassociation is far inside an fp32 tolerance).
 //
@@ -82,13 +85,12 @@ __global__ void __launch_bounds__(ct3::THREADS, BW_T ? 2 : 1)
                            const float *__restrict__ x, const float *__restrict__ w,
                            const float *__restrict__ conv_bias, const float *__restrict__ bias,
                            float scale1, float scale2, float *__restrict__ y, int Cin, int D,
-                           int H, int W, int BW_rt, int XR, int RB, int WB, int n_ohb,
+                           int H, int W, int Do, int Ho, int Wo, int BW_rt, int XR, int RB, int WB, int n_ohb,
                            int n_owb, long long n_units, unsigned int *status) {
     pdl_trigger();
     pdl_wait();
     using namespace ct3;
     const int BW = BW_T ? BW_T : BW_rt;
-    const int Do = D - 1, Ho = H - 1, Wo = W - 1;
     extern __shared__ __align__(128) float sm[];
     const int stage_floats = Cin * 2 * XR * BW;
     const int stage_stride = stage_stride_of(Cin, XR, BW);   // 128-byte aligned stages
@@ -136,7 +138,7 @@ __global__ void __launch_bounds__(ct3::THREADS, BW_T ? 2 : 1)
                 t /= XR;
                 const int a = t & 1, ci = t >> 1;
                 const int ih = g.oh0 + r, iw = g.ow0 + col;
-                const bool in = ih < H && iw < W;
+                const bool in = g.od + a < D && ih < H && iw < W;
                 const float *src =
                     in ? x + (((g.n * Cin + ci) * D + g.od + a) * (long long)H + ih) * W + iw : x;
                 asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(
@@ -354,7 +356,8 @@ aps_status launch_ct3d_pool2_fast(const float *x, const int64_t in[5], const flo
     if (per_sm < 1) return APS_ERR_UNSUPPORTED;
     const long long grid = std::min<long long>((long long)per_sm * sm_count(), n_units);
     const cudaError_t e = launch_pdl(kern, dim3((unsigned)grid), dim3(THREADS), smem, st, map, use_tma, x, w, conv_bias,
-               bias, scale1, scale2, y, (int)Cin, (int)D, (int)H, (int)W, BW, XR, RB, WB,
+               bias, scale1, scale2, y, (int)Cin, (int)D, (int)H, (int)W, (int)Do, (int)Ho,
+               (int)Wo, BW, XR, RB, WB,
                (int)n_ohb, (int)n_owb, n_units, status_word());
     return launch_status(e);
 }

@@ -103,12 +103,11 @@ template <int CIN, int BW_T>
 __global__ void __launch_bounds__(ctc::THREADS, 1)
     ct3d_pool2_tc_kernel(const __grid_constant__ CUtensorMap xmap, const float *__restrict__ w,
                          const float *__restrict__ conv_bias, const float *__restrict__ bias,
-                         float scale1, float scale2, float *__restrict__ y, int D, int H, int W,
+                         float scale1, float scale2, float *__restrict__ y, int Do, int Ho, int Wo,
                          int BW_rt, int XR, int RB, int WB, int n_ohb, int n_owb,
                          long long n_units, unsigned int *status) {
     using namespace ctc;
     const int BW = BW_T ? BW_T : BW_rt;
-    const int Do = D - 1, Ho = H - 1, Wo = W - 1;
     extern __shared__ __align__(128) unsigned char smraw[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smraw + OFF_FULL);
     uint64_t *empty = reinterpret_cast<uint64_t *>(smraw + OFF_EMPTY);
@@ -378,7 +377,7 @@ aps_status launch_ct3d_pool2_tc(const float *x, const int64_t in[5], const float
     if (resident_ctas((const void *)kern, THREADS, (int)smem) < 1) return APS_ERR_UNSUPPORTED;
     const long long grid = std::min<long long>(sm_count(), n_units);
     const cudaError_t e = launch_pdl(kern, dim3((unsigned)grid), dim3(THREADS), smem, st, map, w, conv_bias, bias,
-               scale1, scale2, y, (int)D, (int)H, (int)W, BW, XR, RB, WB, (int)n_ohb,
+               scale1, scale2, y, (int)Do, (int)Ho, (int)Wo, BW, XR, RB, WB, (int)n_ohb,
                (int)n_owb, n_units, status_word());
     return launch_status(e);
 }

@@ -70,18 +70,19 @@ def _u(b):
     return ("uniform", -b, b)
 
 
-def _fused(name, xshape, seed, out_pad=(0, 0, 0)):
-    b = 1.0 / math.sqrt(432.0)
+def _fused(name, xshape, seed, out_pad=(0, 0, 0), k=(3, 3, 3)):
+    # U(+-1/sqrt(fan)), fan = C_out * prod(k) (432 for the pages' k = 3)
+    b = 1.0 / math.sqrt(16.0 * k[0] * k[1] * k[2])
     cin = xshape[1]
     return Workload(
         name, "ct3d_scale_pool_bias", seed,
         {
             "x": (tuple(xshape), ("uniform", -1.0, 1.0), STREAM_X),
-            "w": ((cin, 16, 3, 3, 3), _u(b), STREAM_W),
+            "w": ((cin, 16) + tuple(k), _u(b), STREAM_W),
             "conv_bias": ((16,), _u(b), STREAM_CONV_BIAS),
             "bias": ((16,), ("normal", 0.02), STREAM_BIAS),
         },
-        dict(c_out=16, k=(3, 3, 3), stride=(2, 2, 2), pad=(1, 1, 1), out_pad=tuple(out_pad),
+        dict(c_out=16, k=tuple(k), stride=(2, 2, 2), pad=(1, 1, 1), out_pad=tuple(out_pad),
              dil=(1, 1, 1), pool_k=2, scale1=0.5, scale2=1.0),
     )
 
@@ -135,6 +136,7 @@ WORKLOADS = {
     8: _avgpool("avgpool_nopad", (3, 3, 3), (2, 2, 2), (1, 1, 1), 0),
     9: _avgpool("avgpool_k2", (2, 2, 2), (2, 2, 2), (0, 0, 0), 1),
     10: _convt3d("convt3d_cin8", (128, 8, 16, 32, 32), 10),
+    11: _fused("fused_k4", (128, 3, 16, 32, 32), 11, k=(4, 4, 4)),
 }
 
 

@@ -197,7 +197,8 @@ PROFILE_OF = {
     "avgpool_k2": ("avgpool3d.cu", "avgpool3d_win_k2s2.md"),
     "fused": ("ct3d_pool_tc.cu", "ct3d_pool2_tc_fused.md"),
     "fused_cin8": ("ct3d_pool.cu", "ct3d_pool2_fast_fused_cin8.md"),
-    "fused_op1": ("ct3d_pool_gen.cu", "ct3d_pool_gen_op1.md"),
+    "fused_op1": ("ct3d_pool_tc.cu", "ct3d_pool2_tc_fused.md"),
+    "fused_k4": ("ct3d_pool_gen.cu", "ct3d_pool_gen_k4.md"),
     "convt1d": ("convt1d.cu", "convt1d_tiled_fp32.md"),
     "convt1d_strided": ("convt1d.cu", "convt1d_tiled_fp32.md"),
     "convt1d_tf32": ("convt1d_tc.cu", "convt1d_tf32.md"),
@@ -215,6 +216,7 @@ PER_CONFIG = [
     ("fused", 2, 0, "rotate"),
     ("fused_cin8", 6, 0, "rotate"),
     ("fused_op1", 7, 0, "rotate"),
+    ("fused_k4", 11, 0, "rotate"),
     ("avgpool_nopad", 8, 0, "plain"),
     ("avgpool_k2", 9, 0, "plain"),
     ("convt1d", 3, 3, "plain"),
@@ -353,7 +355,7 @@ class GpuCase:
                 p["pool_k"])
             cin = x.shape[1]
             fast = (tuple(p["k"]) == (3, 3, 3) and tuple(p["stride"]) == (2, 2, 2)
-                    and tuple(p["pad"]) == (1, 1, 1) and not any(p["out_pad"])
+                    and tuple(p["pad"]) == (1, 1, 1) and all(o <= 1 for o in p["out_pad"])
                     and tuple(p["dil"]) == (1, 1, 1) and p["pool_k"] == 2
                     and p["c_out"] == 16 and 1 <= cin <= 8)
             if fast:

@@ -136,16 +136,19 @@ aps_status aps_avgpool3d(const float *x, const int64_t in_ncdhw[5], const int k[
  * NULL (treated as zeros); bias: [C_out]; y: [N, C_out, Do, Ho, Wo] (shape from
  * aps_ct3d_scale_pool_bias_out_shape).  Requires k, s, dil >= 1, pad >= 0,
  * 0 <= out_pad < max(s, dil), pool_k >= 1.
- * Fast path: k = 3, s = 2, p = 1, out_pad = 0, dil = 1, pool_k = 2, C_out = 16,
- * 1 <= C_in <= 8: the pooled output then equals a 2x2x2 valid correlation of x
- * with 8 collapsed weights per (ci, co) plus a folded bias (the page's
+ * Fast path: k = 3, s = 2, p = 1, out_pad 0 or 1 (per dim), dil = 1, pool_k = 2,
+ * C_out = 16, 1 <= C_in <= 8: the pooled output then equals a 2x2x2 correlation of x
+ * (zero past the input's end, which only the last pooled position of a dim with
+ * out_pad 1 reaches) with 8 collapsed weights per (ci, co) plus a folded bias (the page's
  * grouping of the 27 taps by input neighbour), computed in one kernel whose
  * CTAs collapse the weights themselves.  With C_in <= 3, W % 4 == 0 and x
  * 16-byte aligned that kernel runs the correlation on the tensor cores as
  * 3xTF32 (each operand split v = hi + lo, each product summed as lo*hi + hi*lo
  * + hi*hi in fp32); otherwise on the FP32 pipe.  Both meet
- * max |y - exact| <= 1e-5 * (1 + |exact|).  Every other valid geometry runs a
- * direct per-output kernel.
+ * max |y - exact| <= 1e-5 * (1 + |exact|).  Every other valid geometry runs on
+ * per-phase collapsed weights while its per-dim phase tables fit (at most 8
+ * phases and 8 input offsets per phase per dim, at most 32 taps per dim, at
+ * most 96 KB of collapsed weights), else on a direct per-output kernel.
  */
 aps_status aps_ct3d_scale_pool_bias_out_shape(const int64_t in_ncdhw[5], int64_t c_out,
                                               const int k[3], const int stride[3],

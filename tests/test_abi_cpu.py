@@ -73,11 +73,12 @@ def test_workload_output_shapes():
     """Output shapes of the workloads (cfg 4 has 131076 outputs: the
     closed form (65536-1)*2 - 2 + 2*3 + 1 + 1; cfg 5 is l2_p50's pre-pool
     tensor, (16-1)*2 - 2 + 3 = 31 and (32-1)*2 - 2 + 3 = 63; cfg 7's
-    output_padding 1 makes the pre-pool sizes 32 and 64, pooled 16 and 32)."""
+    output_padding 1 makes the pre-pool sizes 32 and 64, pooled 16 and 32, and so do
+    cfg 11's 4-tap kernels: (16-1)*2 - 2 + 4 = 32)."""
     want = {0: (2, 16, 7, 15, 15), 1: (16, 32, 64, 64, 128), 2: (128, 16, 15, 31, 31),
             3: (32, 64, 131084), 4: (16, 64, 131076), 5: (128, 16, 31, 63, 63),
             6: (128, 16, 15, 31, 31), 7: (128, 16, 16, 32, 32), 8: (16, 32, 64, 64, 128),
-            9: (16, 32, 64, 64, 128), 10: (128, 16, 31, 63, 63)}
+            9: (16, 32, 64, 64, 128), 10: (128, 16, 31, 63, 63), 11: (128, 16, 16, 32, 32)}
     for cfg, shape in want.items():
         wl = workloads.get(cfg)
         p = wl.params

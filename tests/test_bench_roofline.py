@@ -108,7 +108,8 @@ def test_compact_json_round_trips_and_keeps_the_per_config_block_short():
     per = {}
     for key, cfg, prec, mode in bench.PER_CONFIG:
         c = SimpleNamespace(bytes=1_611_000_000, flops=85_899_345_920, outputs=134_234_112,
-                            bound="alu" if prec == 0 else "hbm", tensor_passes=prec and 3)
+                            bound="alu" if prec == 3 else "hbm",
+                            tensor_passes={0: 3, 1: 1, 2: 3, 3: 0}[prec])
         per[key] = bench.per_config_entry(key, c, 303.3e-6, PEAKS, "measured", 2.1e7)
     # the driver keeps a few KB of the line's tail; the whole block must fit in it
     assert len(bench.compact_json({"per_config": per})) < 2800

@@ -147,8 +147,9 @@ def fused_gpu(x, w, cb, b, p):
 
 
 # the tiny and full workloads, and the full one with 8 input channels (the FP32-pipe
-# kernel, cfg 6) and with output_padding 1 (the general kernel, cfg 7)
-@pytest.mark.parametrize("cfg", [0, 2, 6, 7])
+# kernel, cfg 6), with output_padding 1 (cfg 7, the tensor-core kernel) and with 4-tap
+# kernels (cfg 11, the general kernel)
+@pytest.mark.parametrize("cfg", [0, 2, 6, 7, 11])
 def test_fused_workloads_all_outputs(cfg):
     wl = workloads.get(cfg)
     x, w, cb, b = (wl.generate(n) for n in ("x", "w", "conv_bias", "bias"))
@@ -171,6 +172,24 @@ def test_fused_fast_path_shapes(shape):
     x, w, cb, b = (wl.generate(n) for n in ("x", "w", "conv_bias", "bias"))
     assert_close(fused_gpu(x, w, cb, b, wl.params), fused_ref(wl, x, w, cb, b),
                  what=f"fused {shape}")
+
+
+# output_padding 1 in some dims keeps the fast path: the extra pooled position of such a
+# dim reads input offset 1 past the end of x, which the TMA box (tensor cores, FP32 pipe)
+# or the element copies (rows that are not 16-byte strided) fill with zeros.  Whole rows of
+# 32 (a 36-column staged window), several row and column blocks, C_in 1..8
+@pytest.mark.parametrize("shape,op", [
+    ((2, 3, 4, 8, 32), (1, 1, 1)), ((1, 2, 3, 9, 12), (0, 1, 1)), ((2, 3, 5, 7, 8), (1, 0, 0)),
+    ((1, 1, 3, 40, 40), (0, 0, 1)), ((1, 3, 2, 33, 36), (1, 1, 0)), ((1, 5, 3, 6, 20), (1, 1, 0)),
+    ((1, 4, 3, 5, 7), (1, 1, 1)), ((2, 8, 2, 9, 33), (0, 1, 1)), ((1, 3, 2, 2, 4), (1, 1, 1))])
+def test_fused_fast_path_with_output_padding(shape, op):
+    x, = rng_inputs(47, shape)
+    w, cb, b = rng_inputs(48, (shape[1], 16, 3, 3, 3), (16,), (16,), lo=-0.2, hi=0.2)
+    one = (1, 1, 1)
+    prm = dict(stride=(2, 2, 2), pad=one, out_pad=op, dil=one, pool_k=2, scale1=0.5, scale2=1.25)
+    ref = ora.ct3d_scale_pool_bias(x, w, cb, b, (2, 2, 2), one, op, one, 2, 0.5, 1.25)
+    assert ref.shape[2:] == tuple(shape[2 + i] - 1 + op[i] for i in range(3))
+    assert_close(fused_gpu(x, w, cb, b, prm), ref, what=f"fused op {op} {shape}")
 
 
 def test_fused_unaligned_input_takes_the_fp32_kernel():
