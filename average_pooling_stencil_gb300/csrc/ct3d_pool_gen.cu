@@ -303,15 +303,22 @@ aps_status launch_ct3d_pool_gen(const float *x, const int64_t in[5], const float
         if (!build_dim(k[i], s[i], p[i], d[i], pool_k, g.d[i])) return APS_ERR_UNSUPPORTED;
     const int COP = (int)((c_out + CO_T - 1) / CO_T) * CO_T;
     // offsets per phase at most 2 in every dim (the pages' geometry and its
-    // output-padding / pool variants): unrolled cells
-    const bool nd2 = g.d[0].md <= 2 && g.d[1].md <= 2 && g.d[2].md <= 2;
-    if (nd2)
-        for (int i = 0; i < 3; ++i) g.d[i].md = 2;   // Weff laid out 2 x 2 x 2 per (ci, phase)
+    // pool variants), or at most 3 (4-tap kernels at stride 2, pool 2): unrolled
+    // cells, Weff laid out ND x ND x ND per (ci, phase); the rest run-time loops
+    int nd = 0;
+    if (g.d[0].md <= 2 && g.d[1].md <= 2 && g.d[2].md <= 2)
+        nd = 2;
+    else if (g.d[0].md <= 3 && g.d[1].md <= 3 && g.d[2].md <= 3)
+        nd = 3;
+    if (nd)
+        for (int i = 0; i < 3; ++i) g.d[i].md = nd;
     const long long weff_floats = (long long)g.d[0].T * g.d[1].T * g.d[2].T * in[1] * g.d[0].md *
                             g.d[1].md * g.d[2].md * COP;
     if (weff_floats * 4 > MAX_WEFF_BYTES) return APS_ERR_UNSUPPORTED;
     const int smem = (int)std::max<long long>(16, weff_floats * 4);
-    const auto kern = nd2 ? ct3d_pool_gen_kernel<2> : ct3d_pool_gen_kernel<0>;
+    const auto kern = nd == 2 ? ct3d_pool_gen_kernel<2>
+                    : nd == 3 ? ct3d_pool_gen_kernel<3>
+                              : ct3d_pool_gen_kernel<0>;
     const int per_sm = resident_ctas((const void *)kern, THREADS, smem);
     if (per_sm < 1) return APS_ERR_UNSUPPORTED;
     const long long n_pos = out[0] * out[2] * out[3] * out[4];

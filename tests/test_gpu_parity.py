@@ -253,7 +253,15 @@ def test_fused_general_geometry(cout, k, s, p, op, d, q):
     ((3, 3, 4, 6, 33), 33, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (1, 1, 1), 2),
     ((1, 2, 3, 4, 37), 6, (2, 2, 2), (1, 1, 4), (0, 0, 1), (0, 0, 0), (1, 1, 1), 1),
     ((1, 2, 6, 5, 9), 7, (2, 3, 3), (2, 1, 3), (0, 2, 1), (1, 0, 2), (2, 3, 1), 3),
-    ((1, 2, 3, 4, 5), 6, (2, 2, 3), (1, 1, 9), (0, 0, 1), (0, 0, 0), (1, 1, 1), 1)])
+    ((1, 2, 3, 4, 5), 6, (2, 2, 3), (1, 1, 9), (0, 0, 1), (0, 0, 0), (1, 1, 1), 1),
+    # at most 3 input offsets per phase in every dim: the unrolled 3 x 3 x 3 cells (4-tap
+    # kernels, a 4-tap dim beside 3-tap ones, 5 taps with padding 2, dilation 2), and one
+    # with 4 offsets in a dim (run-time loops)
+    ((2, 3, 5, 6, 7), 16, (4, 4, 4), (2, 2, 2), (1, 1, 1), (0, 0, 0), (1, 1, 1), 2),
+    ((1, 2, 4, 5, 9), 20, (3, 4, 3), (2, 2, 2), (1, 1, 1), (1, 0, 1), (1, 1, 1), 2),
+    ((1, 3, 3, 7, 10), 7, (5, 5, 3), (2, 2, 2), (2, 2, 1), (0, 0, 0), (1, 1, 1), 2),
+    ((2, 2, 4, 6, 8), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (0, 0, 0), (2, 1, 1), 2),
+    ((1, 2, 4, 5, 6), 9, (4, 4, 2), (2, 2, 1), (1, 2, 0), (0, 1, 0), (1, 1, 1), 3)])
 def test_fused_general_geometry_tables(xs, cout, k, s, p, op, d, q):
     x, = rng_inputs(9, xs)
     w, cb, b = rng_inputs(10, (xs[1], cout) + k, (cout,), (cout,), lo=-0.2, hi=0.2)
