@@ -28,8 +28,10 @@
 //    3xTF32 split into hi and lo.  Because rows are 16 bytes apart, the operand of
 //    tap k is the same buffer with its start moved by 16 bytes per row of tap
 //    offset: one transposed copy serves every tap of every class.
-//  * warp 1, lane 0  -- MMA issuer: walks a per-CTA table of descriptors and,
-//    per chunk and (class, tap), issues CKr/8 tcgen05.mma
+//  * warp 1, lane 0  -- MMA issuer: walks a per-CTA table of descriptors (held in
+//    registers for the one- and two-chunk geometries of the stride-1 K5 and strided
+//    K4 workloads; the waits for the next stage and accumulator asked early, without
+//    blocking) and, per chunk and (class, tap), issues CKr/8 tcgen05.mma
 //    kind::tf32 of 128 x C_out x 8 into the class's accumulator in tensor memory
 //    (a ring of up to 8 tiles' accumulators, as many as 512 columns hold, so the
 //    epilogue's latency never stalls the MMAs), then tcgen05.commit to release the
@@ -53,10 +55,12 @@
 // C_out-wide MMAs).  The dropped lo(x)lo(w) term is below 2^-21 of each product
 // and the truncation of lo(x) below 2^-20.  The launcher picks the deepest
 // pipeline that fits 227 KB: 32- then 16-channel chunks, 3 then 2 converted
-// stages.  Only two
-// converter warps convert in this form, each taking every second 4-channel
-// block (its hi + lo stores from eight warps at once slowed the MMAs by 4 %).
+// stages.  With chunks of 16 MMA entries or more only two converter warps convert
+// in this form, each taking every second 4-channel block (hi + lo stores from eight
+// warps at once slowed those MMAs by 3-4 %); shorter chunks use all eight.
 #include <algorithm>
+
+#include <type_traits>
 
 #include "aps_dev.cuh"
 #include "aps_internal.h"
@@ -115,26 +119,50 @@ using namespace tc;   // named_bar, to_tf32, umma_*, tc_fence_*, tmem_ld*
 // MODE: MODE_TF32, MODE_X3 (three C_out-wide MMAs per entry) or MODE_X3_PAIRED (hi and lo
 // weights side by side as one 2*C_out-wide B: hi(x) [hi(w) | lo(w)], then lo(x) hi(w)).
 // `acc_cols`: accumulator columns per class (C_out, or 2*C_out when paired).
+// The MMAs of one table entry: its A offset word `ae` and B descriptor `bw`.
+template <int MODE>
+__device__ __forceinline__ void issue_entry(uint32_t ae, uint64_t bw, uint64_t abase, uint32_t dbase,
+                                            uint32_t acc_cols, uint32_t idesc, uint32_t idesc_pair,
+                                            bool first_chunk, uint32_t a_lo, uint32_t b_lo) {
+    const uint32_t acc = (!first_chunk || !(ae >> 31)) ? 1u : 0u;
+    const uint32_t d = dbase + ((ae >> 16) & 0xFFu) * acc_cols;
+    const uint64_t a = abase + (ae & 0xFFFFu);
+    if (MODE == MODE_X3_PAIRED) {
+        umma_tf32(d, a, bw, idesc_pair, acc);     // hi(x) [hi(w) | lo(w)]
+        umma_tf32(d, a + a_lo, bw, idesc, 1u);    // lo(x) hi(w)
+    } else if (MODE == MODE_X3) {
+        umma_tf32(d, a + a_lo, bw, idesc, acc);   // lo(x) hi(w)
+        umma_tf32(d, a, bw + b_lo, idesc, 1u);    // hi(x) lo(w)
+        umma_tf32(d, a, bw, idesc, 1u);           // hi(x) hi(w)
+    } else {
+        umma_tf32(d, a, bw, idesc, acc);
+    }
+}
+
+// One chunk's MMAs from a table held in registers: `ra` the A words and `rb` the
+// low words of chunk 0's B descriptors.  Chunk ch's weights start ch*CK/4 rows of
+// 16-byte K groups further on, so its low words are chunk 0's plus `bdel`; the
+// high words (SBO and version) are the same for every entry: `bhi`.
+template <int NE, int MODE>
+__device__ __forceinline__ void issue_chunk_reg(const uint32_t (&ra)[NE], const uint32_t (&rb)[NE],
+                                                uint32_t bdel, bool first_chunk, uint32_t bhi,
+                                                uint64_t abase, uint32_t dbase, uint32_t acc_cols,
+                                                uint32_t idesc, uint32_t idesc_pair,
+                                                uint32_t a_lo, uint32_t b_lo) {
+#pragma unroll
+    for (int e = 0; e < NE; ++e)
+        issue_entry<MODE>(ra[e], ((uint64_t)bhi << 32) | (rb[e] + bdel), abase, dbase, acc_cols,
+                          idesc, idesc_pair, first_chunk, a_lo, b_lo);
+}
+
 template <int NE, int UNROLL, int MODE>
 __device__ __forceinline__ void issue_chunk(const uint32_t *tab_a, const uint64_t *bt, int n_ent,
                                             uint64_t abase, uint32_t dbase, uint32_t acc_cols,
                                             uint32_t idesc, uint32_t idesc_pair, bool first_chunk,
                                             uint32_t a_lo, uint32_t b_lo) {
     auto one = [&](int e) {
-        const uint32_t ae = tab_a[e];
-        const uint32_t acc = (!first_chunk || !(ae >> 31)) ? 1u : 0u;
-        const uint32_t d = dbase + ((ae >> 16) & 0xFFu) * acc_cols;
-        const uint64_t a = abase + (ae & 0xFFFFu), bw = bt[e];
-        if (MODE == MODE_X3_PAIRED) {
-            umma_tf32(d, a, bw, idesc_pair, acc);     // hi(x) [hi(w) | lo(w)]
-            umma_tf32(d, a + a_lo, bw, idesc, 1u);    // lo(x) hi(w)
-        } else if (MODE == MODE_X3) {
-            umma_tf32(d, a + a_lo, bw, idesc, acc);   // lo(x) hi(w)
-            umma_tf32(d, a, bw + b_lo, idesc, 1u);    // hi(x) lo(w)
-            umma_tf32(d, a, bw, idesc, 1u);           // hi(x) hi(w)
-        } else {
-            umma_tf32(d, a, bw, idesc, acc);
-        }
+        issue_entry<MODE>(tab_a[e], bt[e], abase, dbase, acc_cols, idesc, idesc_pair, first_chunk,
+                          a_lo, b_lo);
     };
     if constexpr (NE > 0) {
 #pragma unroll UNROLL
@@ -157,7 +185,7 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
                         const float *__restrict__ bias, float *__restrict__ y, int Cin, int Cout,
                         int K, int S, int L_out, int n_mtiles, long long n_units, int win0, int BW,
                         int tmem_cols, int nacc, int RS, int nbuf, int dgroups, int vec_store,
-                        int tma_store, int CKr, int XTS,
+                        int tma_store, int CKr, int XTS, int nconv,
                         const __grid_constant__ tc1::Taps taps, unsigned int *status) {
     pdl_trigger();
     pdl_wait();
@@ -339,48 +367,96 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
                 a_stage[st] = tc1::umma_desc(smem_u32(xt) + st * XT_STRIDE, LBO_X, 128);
             // lo halves: the same descriptors with the start address moved
             const uint32_t a_lo = XT_LO >> 4, b_lo = W_LO >> 4;
-            uint32_t tile = 0;
-            uint32_t xs_i = 0, xs_ph = 0;   // converted stage and its phase parity
             bool issued = false;
-            for (long long u = blockIdx.x; u < n_units && !abort_flag; u += gridDim.x, ++tile) {
-                const uint32_t b = tile % (uint32_t)nacc;
-                if (tile >= (uint32_t)nacc &&
-                    !mbar_wait(&acc_empty[b], ((tile / nacc) & 1u) ^ 1u)) {
-                    record_error(status, APS_DEVERR_TIMEOUT);
-                    abort_flag = 1;
-                    break;
+            // Every shared-memory access of this thread waits behind the tensor core's
+            // operand reads (about 150 cycles each, even a wait on a phase that has
+            // completed), so the loop makes as few as it can: for the unrolled
+            // geometries the chunk's table sits in registers (it is the same for every
+            // tile), and the waits for the next stage and the next tile's accumulator are
+            // asked early, without blocking, and answered while this chunk's MMAs issue.
+            // (Measured per stride-1 K5 tile: 40 MMAs in 2740-2970 cycles plus 800 of
+            // table loads, waits and loop with the table and waits in line.)
+            auto mma_loop = [&](auto ne_c, auto nch_c) {
+                constexpr int NE = decltype(ne_c)::value, NCH = decltype(nch_c)::value;
+                uint32_t ra[NE > 0 ? NE : 1], rb[NE > 0 ? NE : 1], bhi = 0, bstep = 0;
+                if constexpr (NE > 0) {
+#pragma unroll
+                    for (int e = 0; e < NE; ++e) {
+                        ra[e] = tab_a[e];
+                        rb[e] = (uint32_t)tab_b[e];
+                    }
+                    bhi = (uint32_t)(tab_b[0] >> 32);
+                    // the same step for every entry (the table is built that way)
+                    if (NCH > 1) bstep = (uint32_t)tab_b[NE] - rb[0];
                 }
-                tc1::tc_fence_after();
-                const uint32_t dbase = tmem_base + b * taps.nclass * acc_cols;
-                bool fail = false;
-                for (int ch = 0; ch < nchunks; ++ch) {
-                    const uint32_t s = xs_i;
-                    if (!mbar_wait(&xt_full[s], xs_ph)) {
+                uint32_t tile = 0, b = 0;
+                uint32_t xs_i = 0, xs_ph = 0;        // converted stage and its phase parity
+                bool acc_ready = false, xt_ready = false;   // early answers for what comes next
+                for (long long u = blockIdx.x; u < n_units; u += gridDim.x, ++tile) {
+                    if (tile >= (uint32_t)nacc && !acc_ready &&
+                        !mbar_wait(&acc_empty[b], ((tile / nacc) & 1u) ^ 1u)) {
                         record_error(status, APS_DEVERR_TIMEOUT);
                         abort_flag = 1;
-                        fail = true;
                         break;
                     }
                     tc1::tc_fence_after();
-                    const uint64_t abase = s == 0 ? a_stage[0] : (s == 1 ? a_stage[1] : a_stage[2]);
-                    const uint64_t *bt = tab_b + ch * n_ent;
-                    // 20 entries: the stride-1 K5 geometry at 32-channel chunks
-                    if (n_ent == 20)
-                        tc1::issue_chunk<20, 20, MODE>(tab_a, bt, n_ent, abase, dbase, acc_cols,
-                                                       idesc, idesc_pair, ch == 0, a_lo, b_lo);
-                    else
-                        tc1::issue_chunk<0, 1, MODE>(tab_a, bt, n_ent, abase, dbase, acc_cols,
-                                                     idesc, idesc_pair, ch == 0, a_lo, b_lo);
-                    issued = true;
-                    tc1::umma_commit(&xt_empty[s]);
-                    if (++xs_i == (uint32_t)XTS) {
-                        xs_i = 0;
-                        xs_ph ^= 1u;
-                    }
+                    const uint32_t dbase = tmem_base + b * taps.nclass * acc_cols;
+                    const uint32_t bn = b + 1 == (uint32_t)nacc ? 0u : b + 1;
+                    bool fail = false;
+                    // one chunk's MMAs; false if its stage never came
+                    auto chunk = [&](int ch) {
+                        const uint32_t s = xs_i;
+                        if (!xt_ready && !mbar_wait(&xt_full[s], xs_ph)) {
+                            record_error(status, APS_DEVERR_TIMEOUT);
+                            abort_flag = 1;
+                            return false;
+                        }
+                        tc1::tc_fence_after();
+                        const uint32_t ns = s + 1 == (uint32_t)XTS ? 0u : s + 1;
+                        const uint32_t nph = s + 1 == (uint32_t)XTS ? xs_ph ^ 1u : xs_ph;
+                        xt_ready = mbar_test(&xt_full[ns], nph);
+                        if (ch == nchunks - 1)
+                            acc_ready = tile + 1 < (uint32_t)nacc ||
+                                        mbar_test(&acc_empty[bn], (((tile + 1) / nacc) & 1u) ^ 1u);
+                        const uint64_t abase = s == 0 ? a_stage[0] : (s == 1 ? a_stage[1] : a_stage[2]);
+                        if constexpr (NE > 0) {
+                            tc1::issue_chunk_reg<NE, MODE>(ra, rb, (uint32_t)ch * bstep, ch == 0,
+                                                           bhi, abase, dbase, acc_cols, idesc,
+                                                           idesc_pair, a_lo, b_lo);
+                        } else {
+                            const uint64_t *bt = tab_b + ch * n_ent;
+                            // 20 entries: the stride-1 K5 geometry at 32-channel chunks
+                            if (n_ent == 20)
+                                tc1::issue_chunk<20, 20, MODE>(tab_a, bt, n_ent, abase, dbase,
+                                                               acc_cols, idesc, idesc_pair, ch == 0,
+                                                               a_lo, b_lo);
+                            else
+                                tc1::issue_chunk<0, 1, MODE>(tab_a, bt, n_ent, abase, dbase,
+                                                             acc_cols, idesc, idesc_pair, ch == 0,
+                                                             a_lo, b_lo);
+                        }
+                        issued = true;
+                        tc1::umma_commit(&xt_empty[s]);
+                        xs_i = ns;
+                        xs_ph = nph;
+                        return true;
+                    };
+#pragma unroll 1
+                    for (int ch = 0; ch < nchunks && !fail; ++ch)
+                        if (!chunk(ch)) fail = true;
+                    if (fail) break;
+                    tc1::umma_commit(&acc_full[b]);
+                    b = bn;
                 }
-                if (fail) break;
-                tc1::umma_commit(&acc_full[b]);
-            }
+            };
+            // the stride-1 K5 workload (20 entries, one chunk) and the strided K4 one
+            // (16 entries, two chunks); other geometries read the table per MMA
+            if (n_ent == 20 && nchunks == 1)
+                mma_loop(std::integral_constant<int, 20>{}, std::integral_constant<int, 1>{});
+            else if (n_ent == 16 && nchunks == 2)
+                mma_loop(std::integral_constant<int, 16>{}, std::integral_constant<int, 2>{});
+            else
+                mma_loop(std::integral_constant<int, 0>{}, std::integral_constant<int, 1>{});
             if (issued) {
                 // everything issued has completed before tensor memory is freed
                 tc1::umma_commit(drain);
@@ -561,11 +637,12 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
     } else {
         // ------------------------------------------------------ converters
         // converter warp cb owns channels 4cbx..4cbx+3 of every chunk, cbx = cb,
-        // cb + ACTIVE, ...  The split form writes twice the bytes per channel, and
-        // its shared-memory stores then slow the tensor core's operand reads: two
-        // busy converters (the rest only arrive) leave the MMA more of the port.
+        // cb + ACTIVE, ...; the launcher sets ACTIVE (`nconv`).  The split form writes
+        // twice the bytes per channel, and its shared-memory stores then slow the
+        // tensor core's operand reads: with long chunks two busy converters (the rest
+        // only arrive) leave the MMA more of the port.
         const int cb = converter_id(warp);
-        constexpr int ACTIVE = split ? 2 : tc1::CONVERTERS;
+        const int ACTIVE = nconv;
         uint32_t it = 0;
         uint32_t xs_i = 0, xs_ph = 0;   // converted stage and its phase parity
         for (long long u = blockIdx.x; u < n_units && !abort_flag; u += gridDim.x) {
@@ -780,6 +857,13 @@ aps_status launch_convt1d_tf32(const float *x, const int64_t in[3], const float 
     } else {
         ymap = map;   // unused
     }
+    // converting warps: all eight for tf32; for the split form two where a chunk
+    // has 16 MMA entries or more (their hi + lo stores then cost the MMAs' operand
+    // reads less: stride-1 K5 workload 407.6 us against 419.3 with 4 or 8), else all
+    // eight (strided K4 workload, 8-entry chunks: 267 against 274 us with 2)
+    int n_ent_chunk = 0;
+    for (int c = 0; c < taps.nclass; ++c) n_ent_chunk += taps.ntaps[c] * (CKr / 8);
+    const int nconv = (split && n_ent_chunk >= 16) ? 2 : CONVERTERS;
     const auto kern = paired  ? convt1d_tf32_kernel<MODE_X3_PAIRED>
                       : split ? convt1d_tf32_kernel<MODE_X3>
                               : convt1d_tf32_kernel<MODE_TF32>;
@@ -792,7 +876,7 @@ aps_status launch_convt1d_tf32(const float *x, const int64_t in[3], const float 
     const int vec = (l_out % 4 == 0) && (reinterpret_cast<uintptr_t>(y) % 16 == 0);
     const cudaError_t e = launch_pdl(kern, dim3((unsigned)grid), dim3(THREADS), smem, st, map, ymap, w, bias, y, (int)Cin,
                (int)c_out, k, s, (int)l_out, n_mtiles, n_units, win0, BW, cols, nacc, RS, nbuf,
-               dgroups, vec, tma_store, CKr, XTS, taps, status_word());
+               dgroups, vec, tma_store, CKr, XTS, nconv, taps, status_word());
     return launch_status(e);
 }
 
