@@ -29,9 +29,8 @@
 //    tap k is the same buffer with its start moved by 16 bytes per row of tap
 //    offset: one transposed copy serves every tap of every class.
 //  * warp 1, lane 0  -- MMA issuer: walks a per-CTA table of descriptors (held in
-//    registers for the one- and two-chunk geometries of the stride-1 K5 and strided
-//    K4 workloads; the waits for the next stage and accumulator asked early, without
-//    blocking) and, per chunk and (class, tap), issues CKr/8 tcgen05.mma
+//    registers for the one-chunk, 20-entry stride-1 K5 geometry) and, per chunk and
+//    (class, tap), issues CKr/8 tcgen05.mma
 //    kind::tf32 of 128 x C_out x 8 into the class's accumulator in tensor memory
 //    (a ring of up to 8 tiles' accumulators, as many as 512 columns hold, so the
 //    epilogue's latency never stalls the MMAs), then tcgen05.commit to release the
@@ -55,12 +54,10 @@
 // C_out-wide MMAs).  The dropped lo(x)lo(w) term is below 2^-21 of each product
 // and the truncation of lo(x) below 2^-20.  The launcher picks the deepest
 // pipeline that fits 227 KB: 32- then 16-channel chunks, 3 then 2 converted
-// stages.  With chunks of 16 MMA entries or more only two converter warps convert
-// in this form, each taking every second 4-channel block (hi + lo stores from eight
-// warps at once slowed those MMAs by 3-4 %); shorter chunks use all eight.
+// stages.  Only two converter warps convert in this form, each taking every second
+// 4-channel block (hi + lo stores from eight warps at once slowed the MMAs by 3-4 %;
+// the strided K4 workload's short chunks run the same with 2, 4 or 8).
 #include <algorithm>
-
-#include <type_traits>
 
 #include "aps_dev.cuh"
 #include "aps_internal.h"
@@ -139,20 +136,18 @@ __device__ __forceinline__ void issue_entry(uint32_t ae, uint64_t bw, uint64_t a
     }
 }
 
-// One chunk's MMAs from a table held in registers: `ra` the A words and `rb` the
-// low words of chunk 0's B descriptors.  Chunk ch's weights start ch*CK/4 rows of
-// 16-byte K groups further on, so its low words are chunk 0's plus `bdel`; the
-// high words (SBO and version) are the same for every entry: `bhi`.
+// A tile's MMAs (one chunk) from a table held in registers: `ra` the A words and
+// `rb` the low words of the B descriptors, whose high words (SBO and version) are
+// the same for every entry: `bhi`.
 template <int NE, int MODE>
 __device__ __forceinline__ void issue_chunk_reg(const uint32_t (&ra)[NE], const uint32_t (&rb)[NE],
-                                                uint32_t bdel, bool first_chunk, uint32_t bhi,
-                                                uint64_t abase, uint32_t dbase, uint32_t acc_cols,
-                                                uint32_t idesc, uint32_t idesc_pair,
-                                                uint32_t a_lo, uint32_t b_lo) {
+                                                uint32_t bhi, uint64_t abase, uint32_t dbase,
+                                                uint32_t acc_cols, uint32_t idesc,
+                                                uint32_t idesc_pair, uint32_t a_lo, uint32_t b_lo) {
 #pragma unroll
     for (int e = 0; e < NE; ++e)
-        issue_entry<MODE>(ra[e], ((uint64_t)bhi << 32) | (rb[e] + bdel), abase, dbase, acc_cols,
-                          idesc, idesc_pair, first_chunk, a_lo, b_lo);
+        issue_entry<MODE>(ra[e], ((uint64_t)bhi << 32) | rb[e], abase, dbase, acc_cols, idesc,
+                          idesc_pair, true, a_lo, b_lo);
 }
 
 template <int NE, int UNROLL, int MODE>
@@ -368,33 +363,35 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
             // lo halves: the same descriptors with the start address moved
             const uint32_t a_lo = XT_LO >> 4, b_lo = W_LO >> 4;
             bool issued = false;
-            // Every shared-memory access of this thread waits behind the tensor core's
-            // operand reads (about 150 cycles each, even a wait on a phase that has
-            // completed), so the loop makes as few as it can: for the unrolled
-            // geometries the chunk's table sits in registers (it is the same for every
-            // tile), and the waits for the next stage and the next tile's accumulator are
-            // asked early, without blocking, and answered while this chunk's MMAs issue.
-            // (Measured per stride-1 K5 tile: 40 MMAs in 2740-2970 cycles plus 800 of
-            // table loads, waits and loop with the table and waits in line.)
-            auto mma_loop = [&](auto ne_c, auto nch_c) {
-                constexpr int NE = decltype(ne_c)::value, NCH = decltype(nch_c)::value;
-                uint32_t ra[NE > 0 ? NE : 1], rb[NE > 0 ? NE : 1], bhi = 0, bstep = 0;
-                if constexpr (NE > 0) {
+            if (n_ent == 20 && nchunks == 1) {
+                // The stride-1 K5 geometry at 32-channel chunks: one chunk of 20 entries
+                // per tile.  Every shared-memory access of this thread waits behind the
+                // tensor core's operand reads (about 150 cycles, even a wait on a phase
+                // that has long completed), so this loop makes few: the table (the same
+                // for every tile) sits in registers, the loop condition reads no shared
+                // flag, and for tf32 the waits for the next stage and accumulator are
+                // asked early with a non-blocking test, answered while this tile's MMAs
+                // issue.  Measured per tile (3xTF32, per-role clock stamps on the box):
+                // 3948 -> 3608 cycles; 452 -> 398 us (3xTF32) and 318 -> 283 us (tf32)
+                // against the table loop below, which the other geometries keep (the
+                // strided K4 one ran 3 % slower in this form).  The early test costs the
+                // 3xTF32 form more than it saves (406 against 398 us).
+                constexpr bool EARLY = MODE == tc1::MODE_TF32;
+                uint32_t ra[20], rb[20];
 #pragma unroll
-                    for (int e = 0; e < NE; ++e) {
-                        ra[e] = tab_a[e];
-                        rb[e] = (uint32_t)tab_b[e];
-                    }
-                    bhi = (uint32_t)(tab_b[0] >> 32);
-                    // the same step for every entry (the table is built that way)
-                    if (NCH > 1) bstep = (uint32_t)tab_b[NE] - rb[0];
+                for (int e = 0; e < 20; ++e) {
+                    ra[e] = tab_a[e];
+                    rb[e] = (uint32_t)tab_b[e];
                 }
+                const uint32_t bhi = (uint32_t)(tab_b[0] >> 32);
                 uint32_t tile = 0, b = 0;
-                uint32_t xs_i = 0, xs_ph = 0;        // converted stage and its phase parity
-                bool acc_ready = false, xt_ready = false;   // early answers for what comes next
+                uint32_t xs_i = 0, xs_ph = 0;   // converted stage and its phase parity
+                bool acc_ready = false, xt_ready = false;   // early answers (tf32)
                 for (long long u = blockIdx.x; u < n_units; u += gridDim.x, ++tile) {
-                    if (tile >= (uint32_t)nacc && !acc_ready &&
-                        !mbar_wait(&acc_empty[b], ((tile / nacc) & 1u) ^ 1u)) {
+                    const uint32_t s = xs_i;
+                    if ((tile >= (uint32_t)nacc && !acc_ready &&
+                         !mbar_wait(&acc_empty[b], ((tile / nacc) & 1u) ^ 1u)) ||
+                        (!xt_ready && !mbar_wait(&xt_full[s], xs_ph))) {
                         record_error(status, APS_DEVERR_TIMEOUT);
                         abort_flag = 1;
                         break;
@@ -402,61 +399,65 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
                     tc1::tc_fence_after();
                     const uint32_t dbase = tmem_base + b * taps.nclass * acc_cols;
                     const uint32_t bn = b + 1 == (uint32_t)nacc ? 0u : b + 1;
-                    bool fail = false;
-                    // one chunk's MMAs; false if its stage never came
-                    auto chunk = [&](int ch) {
-                        const uint32_t s = xs_i;
-                        if (!xt_ready && !mbar_wait(&xt_full[s], xs_ph)) {
-                            record_error(status, APS_DEVERR_TIMEOUT);
-                            abort_flag = 1;
-                            return false;
-                        }
-                        tc1::tc_fence_after();
-                        const uint32_t ns = s + 1 == (uint32_t)XTS ? 0u : s + 1;
-                        const uint32_t nph = s + 1 == (uint32_t)XTS ? xs_ph ^ 1u : xs_ph;
+                    const uint32_t ns = s + 1 == (uint32_t)XTS ? 0u : s + 1;
+                    const uint32_t nph = s + 1 == (uint32_t)XTS ? xs_ph ^ 1u : xs_ph;
+                    if (EARLY) {
                         xt_ready = mbar_test(&xt_full[ns], nph);
-                        if (ch == nchunks - 1)
-                            acc_ready = tile + 1 < (uint32_t)nacc ||
-                                        mbar_test(&acc_empty[bn], (((tile + 1) / nacc) & 1u) ^ 1u);
-                        const uint64_t abase = s == 0 ? a_stage[0] : (s == 1 ? a_stage[1] : a_stage[2]);
-                        if constexpr (NE > 0) {
-                            tc1::issue_chunk_reg<NE, MODE>(ra, rb, (uint32_t)ch * bstep, ch == 0,
-                                                           bhi, abase, dbase, acc_cols, idesc,
-                                                           idesc_pair, a_lo, b_lo);
-                        } else {
-                            const uint64_t *bt = tab_b + ch * n_ent;
-                            // 20 entries: the stride-1 K5 geometry at 32-channel chunks
-                            if (n_ent == 20)
-                                tc1::issue_chunk<20, 20, MODE>(tab_a, bt, n_ent, abase, dbase,
-                                                               acc_cols, idesc, idesc_pair, ch == 0,
-                                                               a_lo, b_lo);
-                            else
-                                tc1::issue_chunk<0, 1, MODE>(tab_a, bt, n_ent, abase, dbase,
-                                                             acc_cols, idesc, idesc_pair, ch == 0,
-                                                             a_lo, b_lo);
-                        }
-                        issued = true;
-                        tc1::umma_commit(&xt_empty[s]);
-                        xs_i = ns;
-                        xs_ph = nph;
-                        return true;
-                    };
-#pragma unroll 1
-                    for (int ch = 0; ch < nchunks && !fail; ++ch)
-                        if (!chunk(ch)) fail = true;
-                    if (fail) break;
+                        acc_ready = tile + 1 < (uint32_t)nacc ||
+                                    mbar_test(&acc_empty[bn], (((tile + 1) / nacc) & 1u) ^ 1u);
+                    }
+                    const uint64_t abase = s == 0 ? a_stage[0] : (s == 1 ? a_stage[1] : a_stage[2]);
+                    tc1::issue_chunk_reg<20, MODE>(ra, rb, bhi, abase, dbase, acc_cols, idesc,
+                                                   idesc_pair, a_lo, b_lo);
+                    issued = true;
+                    tc1::umma_commit(&xt_empty[s]);
                     tc1::umma_commit(&acc_full[b]);
+                    xs_i = ns;
+                    xs_ph = nph;
                     b = bn;
                 }
-            };
-            // the stride-1 K5 workload (20 entries, one chunk) and the strided K4 one
-            // (16 entries, two chunks); other geometries read the table per MMA
-            if (n_ent == 20 && nchunks == 1)
-                mma_loop(std::integral_constant<int, 20>{}, std::integral_constant<int, 1>{});
-            else if (n_ent == 16 && nchunks == 2)
-                mma_loop(std::integral_constant<int, 16>{}, std::integral_constant<int, 2>{});
-            else
-                mma_loop(std::integral_constant<int, 0>{}, std::integral_constant<int, 1>{});
+            } else {
+                uint32_t tile = 0;
+                uint32_t xs_i = 0, xs_ph = 0;   // converted stage and its phase parity
+                for (long long u = blockIdx.x; u < n_units && !abort_flag; u += gridDim.x, ++tile) {
+                    const uint32_t b = tile % (uint32_t)nacc;
+                    if (tile >= (uint32_t)nacc &&
+                        !mbar_wait(&acc_empty[b], ((tile / nacc) & 1u) ^ 1u)) {
+                        record_error(status, APS_DEVERR_TIMEOUT);
+                        abort_flag = 1;
+                        break;
+                    }
+                    tc1::tc_fence_after();
+                    const uint32_t dbase = tmem_base + b * taps.nclass * acc_cols;
+                    bool fail = false;
+                    for (int ch = 0; ch < nchunks; ++ch) {
+                        const uint32_t s = xs_i;
+                        if (!mbar_wait(&xt_full[s], xs_ph)) {
+                            record_error(status, APS_DEVERR_TIMEOUT);
+                            abort_flag = 1;
+                            fail = true;
+                            break;
+                        }
+                        tc1::tc_fence_after();
+                        const uint64_t abase = s == 0 ? a_stage[0] : (s == 1 ? a_stage[1] : a_stage[2]);
+                        const uint64_t *bt = tab_b + ch * n_ent;
+                        if (n_ent == 20)
+                            tc1::issue_chunk<20, 20, MODE>(tab_a, bt, n_ent, abase, dbase, acc_cols,
+                                                           idesc, idesc_pair, ch == 0, a_lo, b_lo);
+                        else
+                            tc1::issue_chunk<0, 1, MODE>(tab_a, bt, n_ent, abase, dbase, acc_cols,
+                                                         idesc, idesc_pair, ch == 0, a_lo, b_lo);
+                        issued = true;
+                        tc1::umma_commit(&xt_empty[s]);
+                        if (++xs_i == (uint32_t)XTS) {
+                            xs_i = 0;
+                            xs_ph ^= 1u;
+                        }
+                    }
+                    if (fail) break;
+                    tc1::umma_commit(&acc_full[b]);
+                }
+            }
             if (issued) {
                 // everything issued has completed before tensor memory is freed
                 tc1::umma_commit(drain);
@@ -637,10 +638,10 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
     } else {
         // ------------------------------------------------------ converters
         // converter warp cb owns channels 4cbx..4cbx+3 of every chunk, cbx = cb,
-        // cb + ACTIVE, ...; the launcher sets ACTIVE (`nconv`).  The split form writes
-        // twice the bytes per channel, and its shared-memory stores then slow the
-        // tensor core's operand reads: with long chunks two busy converters (the rest
-        // only arrive) leave the MMA more of the port.
+        // cb + ACTIVE, ... (ACTIVE = `nconv`, from the launcher).  The split form
+        // writes twice the bytes per channel, and its shared-memory stores then slow
+        // the tensor core's operand reads: two busy converters (the rest only arrive)
+        // leave the MMA more of the port.
         const int cb = converter_id(warp);
         const int ACTIVE = nconv;
         uint32_t it = 0;
@@ -857,13 +858,6 @@ aps_status launch_convt1d_tf32(const float *x, const int64_t in[3], const float 
     } else {
         ymap = map;   // unused
     }
-    // converting warps: all eight for tf32; for the split form two where a chunk
-    // has 16 MMA entries or more (their hi + lo stores then cost the MMAs' operand
-    // reads less: stride-1 K5 workload 407.6 us against 419.3 with 4 or 8), else all
-    // eight (strided K4 workload, 8-entry chunks: 267 against 274 us with 2)
-    int n_ent_chunk = 0;
-    for (int c = 0; c < taps.nclass; ++c) n_ent_chunk += taps.ntaps[c] * (CKr / 8);
-    const int nconv = (split && n_ent_chunk >= 16) ? 2 : CONVERTERS;
     const auto kern = paired  ? convt1d_tf32_kernel<MODE_X3_PAIRED>
                       : split ? convt1d_tf32_kernel<MODE_X3>
                               : convt1d_tf32_kernel<MODE_TF32>;
@@ -876,7 +870,7 @@ aps_status launch_convt1d_tf32(const float *x, const int64_t in[3], const float 
     const int vec = (l_out % 4 == 0) && (reinterpret_cast<uintptr_t>(y) % 16 == 0);
     const cudaError_t e = launch_pdl(kern, dim3((unsigned)grid), dim3(THREADS), smem, st, map, ymap, w, bias, y, (int)Cin,
                (int)c_out, k, s, (int)l_out, n_mtiles, n_units, win0, BW, cols, nacc, RS, nbuf,
-               dgroups, vec, tma_store, CKr, XTS, nconv, taps, status_word());
+               dgroups, vec, tma_store, CKr, XTS, split ? 2 : CONVERTERS, taps, status_word());
     return launch_status(e);
 }
 
