@@ -248,8 +248,8 @@ __global__ void __launch_bounds__(ctc::THREADS, 1)
     };
     // wait for buffer j's MMAs of the unit taken k-th; then its accumulator
     // row + bias -> 16 whole-warp row stores
-    auto epilogue = [&](int j, uint32_t kk, float *yb, int rows) {
-        if (!mbar_wait(&dfb[j], kk & 1u)) {
+    auto epilogue = [&](int j, uint32_t kk, float *yb, int rows, bool ready) {
+        if (!ready && !mbar_wait(&dfb[j], kk & 1u)) {
             record_error(status, APS_DEVERR_TIMEOUT);
             *abort_flag = 1;
             fail = true;
@@ -269,10 +269,17 @@ __global__ void __launch_bounds__(ctc::THREADS, 1)
     float *prev_y = nullptr;   // the previous unit's output corner (this lane's column)
     int prev_rows = 0;
     uint32_t c0 = 0, c1 = 0;         // commits to each buffer's barrier
+    // Each shared-memory access here waits behind the gathers' and the tensor
+    // core's traffic, so whether the next unit's box has landed, the previous
+    // unit's tile-1 MMAs are done and another thread has aborted are asked early
+    // (a non-blocking barrier test, a plain load) and answered while this unit's
+    // work runs.
+    bool full_ready = false;         // early answers for the next unit
+    int abort_seen = 0;
     for (long long u = blockIdx.x; u < n_units; u += gridDim.x, ++k) {
         const int b = (int)(k % STAGES);
         const long long ahead = u + (long long)(STAGES - 1) * gridDim.x;
-        if (tid == 0 && !*abort_flag && ahead < n_units) {
+        if (tid == 0 && !abort_seen && ahead < n_units) {
             const int nb = (int)((k + STAGES - 1) % STAGES);
             if (k >= 1 && !mbar_wait(&empty[nb], ((k - 1) / STAGES) & 1u)) {
                 record_error(status, APS_DEVERR_TIMEOUT);
@@ -282,13 +289,15 @@ __global__ void __launch_bounds__(ctc::THREADS, 1)
                 ++issued;
             }
         }
-        bool ok = !fail && !*abort_flag;
-        if (ok && !mbar_wait(&full[b], (k / STAGES) & 1u)) {
+        bool ok = !fail && !abort_seen;
+        if (ok && !full_ready && !mbar_wait(&full[b], (k / STAGES) & 1u)) {
             record_error(status, APS_DEVERR_TIMEOUT);
             *abort_flag = 1;
             ok = false;
         }
         ok = __all_sync(0xffffffffu, ok);
+        // the previous unit's tile-1 MMAs: asked now, needed after this unit's tile 0
+        const bool d1_ready = k > 0 && mbar_test(&dfb[1], (k - 1) & 1u);
         const int grows = ok ? slot[b].rows : 0;
         const float *xb = xs + b * stage_stride;
         if (ok && TILE_ROWS * grp < grows) gather(xb, 0);
@@ -297,7 +306,7 @@ __global__ void __launch_bounds__(ctc::THREADS, 1)
         if (tc::named_bar_or(gbar, 128, !ok)) break;
         issue(0, grows);
         ++c0;
-        if (k > 0) epilogue(1, k - 1, prev_y, prev_rows);
+        if (k > 0) epilogue(1, k - 1, prev_y, prev_rows, d1_ready);
         if (!fail && TILE_ROWS * (grp + GROUPS) < grows) gather(xb, 1);
         const long long gn = slot[b].n;
         const int god = slot[b].od, goh0 = slot[b].oh0, gow0 = slot[b].ow0, gcols = slot[b].cols;
@@ -308,15 +317,18 @@ __global__ void __launch_bounds__(ctc::THREADS, 1)
         if (tc::named_bar_or(gbar, 128, fail)) break;
         issue(1, grows);
         ++c1;
+        // the next unit's box and the abort flag, answered during the epilogue below
+        full_ready = mbar_test(&full[(k + 1) % STAGES], ((k + 1) / STAGES) & 1u);
+        abort_seen = *abort_flag;
         float *ycur = lane < gcols
             ? y + ((gn * COUT) * Do + god) * plane + (long long)goh0 * Wo + gow0 + lane : nullptr;
-        epilogue(0, k, ycur, grows);
+        epilogue(0, k, ycur, grows, false);
         prev_y = ycur;
         prev_rows = grows;
     }
     // the last unit's buffer-1 tiles
     if (__all_sync(0xffffffffu, c1 > 0 && c1 == k && !fail && !*abort_flag))
-        epilogue(1, c1 - 1, prev_y, prev_rows);
+        epilogue(1, c1 - 1, prev_y, prev_rows, false);
 
     // ---- leave nothing in flight: each buffer's last MMAs (their wait may
     // have run out), the fills no warp consumed; then free the tensor memory
