@@ -58,6 +58,7 @@
 // 4-channel block (hi + lo stores from eight warps at once slowed the MMAs by 3-4 %;
 // the strided K4 workload's short chunks run the same with 2, 4 or 8).
 #include <algorithm>
+#include <type_traits>
 
 #include "aps_dev.cuh"
 #include "aps_internal.h"
@@ -416,6 +417,66 @@ __global__ void __launch_bounds__(tc1::THREADS, 1)
                     xs_ph = nph;
                     b = bn;
                 }
+            } else if (n_ent == 8 && nchunks == 4) {
+                // Four chunks per tile (the strided K4 workload in 3xTF32: 16-channel
+                // chunks of 8 entries): chunk 0's table in registers, chunk ch's B words
+                // chunk 0's plus ch times a fixed step (the weights of the next channels
+                // start one step further on): 249 -> 230 us.  The same for the tf32 form's
+                // two 16-entry chunks ran slower (167 against 154 us), so that keeps the
+                // table loop.
+                auto reg_loop = [&](auto ne_c) {
+                    constexpr int NE = decltype(ne_c)::value;
+                    uint32_t ra[NE], rb[NE];
+#pragma unroll
+                    for (int e = 0; e < NE; ++e) {
+                        ra[e] = tab_a[e];
+                        rb[e] = (uint32_t)tab_b[e];
+                    }
+                    const uint32_t bhi = (uint32_t)(tab_b[0] >> 32);
+                    const uint32_t bstep = (uint32_t)tab_b[NE] - rb[0];
+                    uint32_t tile = 0;
+                    uint32_t xs_i = 0, xs_ph = 0;
+                    for (long long u = blockIdx.x; u < n_units; u += gridDim.x, ++tile) {
+                        const uint32_t b = tile % (uint32_t)nacc;
+                        if (tile >= (uint32_t)nacc &&
+                            !mbar_wait(&acc_empty[b], ((tile / nacc) & 1u) ^ 1u)) {
+                            record_error(status, APS_DEVERR_TIMEOUT);
+                            abort_flag = 1;
+                            break;
+                        }
+                        tc1::tc_fence_after();
+                        const uint32_t dbase = tmem_base + b * taps.nclass * acc_cols;
+                        bool fail = false;
+#pragma unroll 1
+                        for (int ch = 0; ch < nchunks; ++ch) {
+                            const uint32_t s = xs_i;
+                            if (!mbar_wait(&xt_full[s], xs_ph)) {
+                                record_error(status, APS_DEVERR_TIMEOUT);
+                                abort_flag = 1;
+                                fail = true;
+                                break;
+                            }
+                            tc1::tc_fence_after();
+                            const uint64_t abase =
+                                s == 0 ? a_stage[0] : (s == 1 ? a_stage[1] : a_stage[2]);
+                            const uint32_t bdel = (uint32_t)ch * bstep;
+#pragma unroll
+                            for (int e = 0; e < NE; ++e)
+                                tc1::issue_entry<MODE>(ra[e], ((uint64_t)bhi << 32) | (rb[e] + bdel),
+                                                       abase, dbase, acc_cols, idesc, idesc_pair,
+                                                       ch == 0, a_lo, b_lo);
+                            issued = true;
+                            tc1::umma_commit(&xt_empty[s]);
+                            if (++xs_i == (uint32_t)XTS) {
+                                xs_i = 0;
+                                xs_ph ^= 1u;
+                            }
+                        }
+                        if (fail) break;
+                        tc1::umma_commit(&acc_full[b]);
+                    }
+                };
+                reg_loop(std::integral_constant<int, 8>{});
             } else {
                 uint32_t tile = 0;
                 uint32_t xs_i = 0, xs_ph = 0;   // converted stage and its phase parity
