@@ -373,10 +373,8 @@ aps_status aps_convtranspose3d(const float *x, const int64_t in[5], const float 
     for (int i = 0; i < 3; ++i)
         fast = fast && k[i] == 3 && s[i] == 2 && p[i] == 1 && d[i] == 1 && op[i] <= 1;
     if (fast) {
-        // tensor cores (W <= 32, 16-byte input rows), else the FP32 pipe
+        // tensor cores (16-byte input rows)
         st = launch_convt3d_tc(x, in, w, bias, y, out, cs);
-        if (st != APS_ERR_UNSUPPORTED) return st;
-        st = launch_convt3d_k3s2p1(x, in, w, bias, y, out, cs);
         if (st != APS_ERR_UNSUPPORTED) return st;
     }
     return launch_convt3d_direct(x, in, w, bias, c_out, k, s, p, d, y, out, cs);

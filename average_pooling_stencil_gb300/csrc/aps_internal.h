@@ -116,17 +116,14 @@ aps_status launch_ct3d_pool_direct(const float *x, const int64_t in[5], const fl
                                    const int d[3], int pool_k, float scale1, float scale2,
                                    float *y, const int64_t out[5], cudaStream_t st);
 
-// ConvTranspose3d, fp32: the k3 s2 p1 d1 kernel (C_out 16, C_in <= 8, TMA
-// staging) and the direct per-output kernel for any geometry.
 // Standalone ConvTranspose3d k3 s2 p1 on the tensor cores (3xTF32: fp32
-// accuracy) for C_in <= 8, W <= 32 and 16-byte input rows; APS_ERR_UNSUPPORTED
-// otherwise (the caller then uses launch_convt3d_k3s2p1).
+// accuracy) for C_in <= 8 and 16-byte input rows (W % 4 == 0; rows wider than 32
+// in 32-column blocks); APS_ERR_UNSUPPORTED otherwise (the caller then uses
+// launch_convt3d_direct).
 aps_status launch_convt3d_tc(const float *x, const int64_t in[5], const float *w,
                              const float *bias, float *y, const int64_t out[5], cudaStream_t st);
 
-aps_status launch_convt3d_k3s2p1(const float *x, const int64_t in[5], const float *w,
-                                 const float *bias, float *y, const int64_t out[5],
-                                 cudaStream_t st);
+// ConvTranspose3d, fp32, any geometry: one thread per output.
 aps_status launch_convt3d_direct(const float *x, const int64_t in[5], const float *w,
                                  const float *bias, int64_t c_out, const int k[3],
                                  const int s[3], const int p[3], const int d[3], float *y,

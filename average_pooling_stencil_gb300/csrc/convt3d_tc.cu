@@ -17,7 +17,9 @@
 //
 // Design (GB300): one persistent CTA per SM, two groups of four warps and a
 // TMA warp.  A unit is 4 input rows x (W <= 32) input columns of one (n, md)
-// input plane -- outputs: planes 2md, 2md+1, rows 8*blk .. +7, all columns.
+// input plane -- outputs: planes 2md, 2md+1, rows 8*blk .. +7, all columns --
+// or, for W > 32, a 32-column block of them (box origin 32*mwb, 128-byte
+// aligned), whose outputs leave straight from registers.
 // CTA-local unit k goes to group k % 2 and stage k % 8 of a ring the TMA
 // warp fills (one 4-D box per unit: C_in x 2 planes x 5 rows x 36 columns,
 // zero-filled outside the tensor).  Warp q of a group owns input row q of
@@ -85,7 +87,7 @@ static_assert(STAGES % GROUPS == 0, "a group's units always use the same stages"
 
 struct Slot {
     long long n;
-    int md, mh0, pad[4];
+    int md, mh0, mw0, pad[3];
 };
 static_assert(sizeof(Slot) * STAGES <= OFF_BIAS - OFF_SLOT, "slots fit");
 
@@ -120,13 +122,15 @@ template <int CIN>
 __global__ void __launch_bounds__(c3t::THREADS, 1)
     convt3d_tc_kernel(const __grid_constant__ CUtensorMap xmap, const float *__restrict__ w,
                       const float *__restrict__ bias, float *__restrict__ y, int D, int H, int W,
-                      int BW, int Do, int Ho, int Wo, int n_mhb, long long n_units,
-                      unsigned int *status) {
+                      int BW, int Do, int Ho, int Wo, int n_mhb, int n_mwb, int direct_rt,
+                      long long n_units, unsigned int *status) {
     pdl_trigger();
     pdl_wait();
     using namespace c3t;
     constexpr int D_COL = d_col_of(CIN), HEAD_BYTES = head_bytes_of(CIN);
-    constexpr bool DIRECT = direct_of(CIN);
+    // outputs from registers: C_in > 3 always, and rows wider than 32 (units of
+    // 32-column blocks, whose runs are not whole rows)
+    const bool DIRECT = direct_of(CIN) || direct_rt;
     extern __shared__ __align__(128) unsigned char smraw[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smraw + OFF_FULL);
     uint64_t *empty = reinterpret_cast<uint64_t *>(smraw + OFF_EMPTY);
@@ -200,16 +204,19 @@ __global__ void __launch_bounds__(c3t::THREADS, 1)
                     *abort_flag = 1;
                     break;
                 }
-                const int mhb = (int)(u % n_mhb);
-                const long long t = u / n_mhb;
+                const int mwb = (int)(u % n_mwb);
+                long long t = u / n_mwb;
+                const int mhb = (int)(t % n_mhb);
+                t /= n_mhb;
                 const int md = (int)(t % D);
                 const long long n = t / D;
                 slot[s].n = n;
                 slot[s].md = md;
                 slot[s].mh0 = MROWS * mhb;
+                slot[s].mw0 = 32 * mwb;
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 mbar_arrive_expect_tx(&full[s], (uint32_t)stage_floats * 4u);
-                tma_load_4d(xs + s * stage_stride, &xmap, &full[s], 0, MROWS * mhb, md,
+                tma_load_4d(xs + s * stage_stride, &xmap, &full[s], 32 * mwb, MROWS * mhb, md,
                             (int)(n * CIN));
             }
             // the loads in flight land before the CTA exits (the latest of each stage)
@@ -229,7 +236,6 @@ __global__ void __launch_bounds__(c3t::THREADS, 1)
         float bias_r[COUT];
 #pragma unroll
         for (int co = 0; co < COUT; ++co) bias_r[co] = bsm[co];
-        const bool in_w = lane < W;
         uint32_t j = 0, ncommit = 0;   // units this group has taken; MMA commits (MMA thread)
         bool fail = false;
         // C_in <= 3: whether the group's next box has landed and whether another
@@ -314,7 +320,8 @@ __global__ void __launch_bounds__(c3t::THREADS, 1)
 
             // where the outputs go, read before the stage and its slot are released
             const long long gn = slot[s].n;
-            const int gmd = slot[s].md, gmh0 = slot[s].mh0;
+            const int gmd = slot[s].md, gmh0 = slot[s].mh0, gmw0 = slot[s].mw0;
+            const bool in_w = gmw0 + lane < W;   // this lane's input column exists
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
             if (EARLY) {
@@ -331,13 +338,13 @@ __global__ void __launch_bounds__(c3t::THREADS, 1)
                 *abort_flag = 1;
             }
             okd = __all_sync(0xffffffffu, okd);
-            if constexpr (DIRECT) {
+            if (DIRECT) {
                 if (tc::named_bar_or(gbar, 128, !okd)) break;
-                // outputs straight from registers: lane l holds output columns 2l
-                // and 2l + 1 of every channel of its (r_d, r_h) row
+                // outputs straight from registers: lane l holds output columns
+                // 2(mw0 + l) and 2(mw0 + l) + 1 of every channel of its (r_d, r_h) row
                 const int oh0 = 2 * gmh0;
                 const int nrows = Ho - oh0 < OROWS ? Ho - oh0 : OROWS;
-                float *y0 = y + ((gn * COUT) * Do + 2 * gmd) * plane + (long long)oh0 * Wo;
+                float *y0 = y + ((gn * COUT) * Do + 2 * gmd) * plane + (long long)oh0 * Wo + 2 * gmw0;
                 tc::tc_fence_after();
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
@@ -347,7 +354,7 @@ __global__ void __launch_bounds__(c3t::THREADS, 1)
                     const int row = 2 * q + rh;
                     if (2 * gmd + rd < Do && row < nrows && in_w) {
                         float *yp = y0 + rd * plane + (long long)row * Wo + 2 * lane;
-                        const bool w1 = 2 * lane + 1 < Wo;
+                        const bool w1 = 2 * (gmw0 + lane) + 1 < Wo;
 #pragma unroll
                         for (int co = 0; co < COUT; ++co) {
                             yp[0] = __uint_as_float(v[co]) + bias_r[co];
@@ -448,15 +455,18 @@ aps_status launch_convt3d_tc(const float *x, const int64_t in[5], const float *w
     using namespace c3t;
     const int64_t N = in[0], Cin = in[1], D = in[2], H = in[3], W = in[4];
     const int64_t Do = out[2], Ho = out[3], Wo = out[4];
-    // one unit spans the input's width (W <= 32, so each output run is whole
-    // rows); the TMA box needs 16-byte rows
-    if (Cin < 1 || Cin > CIN_MAX || W > 32 || W % 4 != 0 ||
+    // a unit spans the input's width when W <= 32 (each output run is then whole
+    // rows, and C_in <= 3 stages them for bulk copies), else a 32-column block
+    // (outputs from registers); the TMA box needs 16-byte rows
+    if (Cin < 1 || Cin > CIN_MAX || W % 4 != 0 ||
         reinterpret_cast<uintptr_t>(x) % 16 != 0 || D >= (1 << 30) || H >= (1 << 30) ||
         N * Cin >= (1ll << 31) || N * D >= (1ll << 40))
         return APS_ERR_UNSUPPORTED;
-    const int BW = (int)((W + 1 + 3) & ~3);   // staged columns 0..W (column W reads as zero)
-    const int64_t n_mhb = ceil_div(H, MROWS);
-    const long long n_units = N * D * n_mhb;
+    // staged columns: the block's 32 (or W) and one more (past W it reads as zero)
+    const int BW = W > 32 ? BWMAX : (int)((W + 1 + 3) & ~3);
+    const int64_t n_mhb = ceil_div(H, MROWS), n_mwb = ceil_div(W, (int64_t)32);
+    const long long n_units = N * D * n_mhb * n_mwb;
+    const int direct = direct_of((int)Cin) || W > 32;
     CUtensorMap map;
     const cuuint64_t dims[4] = {(cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)D, (cuuint64_t)(N * Cin)};
     const cuuint64_t strides[3] = {(cuuint64_t)(W * 4), (cuuint64_t)(H * W * 4),
@@ -470,9 +480,10 @@ aps_status launch_convt3d_tc(const float *x, const int64_t in[5], const float *w
     const size_t smem =
         (size_t)head_bytes_of((int)Cin) +
         ((size_t)STAGES * stage_stride_of((int)Cin) +
-         (direct_of((int)Cin) ? 0 : (size_t)GROUPS * staging_floats_of((int)Wo, ac, ap))) * 4;
+         (direct ? 0 : (size_t)GROUPS * staging_floats_of((int)Wo, ac, ap))) * 4;
     void (*const kerns[CIN_MAX])(const CUtensorMap, const float *, const float *, float *, int,
-                                 int, int, int, int, int, int, int, long long, unsigned int *) = {
+                                 int, int, int, int, int, int, int, int, int, long long,
+                                 unsigned int *) = {
         convt3d_tc_kernel<1>, convt3d_tc_kernel<2>, convt3d_tc_kernel<3>, convt3d_tc_kernel<4>,
         convt3d_tc_kernel<5>, convt3d_tc_kernel<6>, convt3d_tc_kernel<7>, convt3d_tc_kernel<8>};
     const auto kern = kerns[Cin - 1];
@@ -480,7 +491,8 @@ aps_status launch_convt3d_tc(const float *x, const int64_t in[5], const float *w
     if (resident_ctas((const void *)kern, THREADS, (int)smem) < 1) return APS_ERR_UNSUPPORTED;
     const long long grid = std::min<long long>(sm_count(), n_units);
     const cudaError_t e = launch_pdl(kern, dim3((unsigned)grid), dim3(THREADS), smem, st, map, w, bias, y, (int)D, (int)H,
-               (int)W, BW, (int)Do, (int)Ho, (int)Wo, (int)n_mhb, n_units, status_word());
+               (int)W, BW, (int)Do, (int)Ho, (int)Wo, (int)n_mhb, (int)n_mwb, direct, n_units,
+               status_word());
     return launch_status(e);
 }
 

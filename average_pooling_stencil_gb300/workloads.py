@@ -137,6 +137,7 @@ WORKLOADS = {
     9: _avgpool("avgpool_k2", (2, 2, 2), (2, 2, 2), (0, 0, 0), 1),
     10: _convt3d("convt3d_cin8", (128, 8, 16, 32, 32), 10),
     11: _fused("fused_k4", (128, 3, 16, 32, 32), 11, k=(4, 4, 4)),
+    12: _convt3d("convt3d_w64", (64, 3, 16, 32, 64), 12),
 }
 
 

@@ -207,6 +207,7 @@ PROFILE_OF = {
     "convt1d_strided_tf32x3": ("convt1d_tc.cu", "convt1d_tf32x3.md"),
     "convt3d": ("convt3d_tc.cu", "convt3d_tc_k3s2p1.md"),
     "convt3d_cin8": ("convt3d_tc.cu", "convt3d_tc_k3s2p1_cin8.md"),
+    "convt3d_w64": ("convt3d_tc.cu", "convt3d_tc_k3s2p1_w64.md"),
 }
 
 # per-config workloads: key, workload id, ConvTranspose1d precision (the C ABI's value:
@@ -227,6 +228,7 @@ PER_CONFIG = [
     ("convt1d_strided_tf32x3", 4, 2, "plain"),
     ("convt3d", 5, 0, "plain"),
     ("convt3d_cin8", 10, 0, "plain"),
+    ("convt3d_w64", 12, 0, "plain"),
 ]
 
 
@@ -382,7 +384,7 @@ class GpuCase:
                 pairs *= convt_pairs(x.shape[2 + i], oshape[2 + i], p["k"][i], p["stride"][i],
                                      p["pad"][i], p["dil"][i])
             self.flops = 2 * x.shape[0] * x.shape[1] * p["c_out"] * pairs
-            self.tc = x.shape[1] <= 8 and x.shape[4] % 4 == 0 and x.shape[4] <= 32
+            self.tc = x.shape[1] <= 8 and x.shape[4] % 4 == 0
             self.tensor_passes = 3 if self.tc else 0
             self.bound = "hbm" if self.tc else "hbm+alu"
         else:
@@ -865,7 +867,7 @@ def run_native(args):
     kernel_of = {"avgpool3d": "avgpool3d_k3s2p1_tma_kernel",
                  "ct3d_scale_pool_bias": ("ct3d_pool2_tc_kernel" if case.tc
                                           else "ct3d_pool2_fast_kernel"),
-                 "convtranspose3d": "convt3d_tc_kernel" if case.tc else "convt3d_k3s2p1_kernel",
+                 "convtranspose3d": "convt3d_tc_kernel" if case.tc else "convt3d_direct_kernel",
                  "convtranspose1d": ("convt1d_tiled_kernel" if case.kind == 3
                                      else "convt1d_tf32_kernel")}
     roof["kernel"] = kernel_of[case.wl.op]

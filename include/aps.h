@@ -177,10 +177,11 @@ aps_status aps_ct3d_scale_pool_bias(const float *x, const int64_t in_ncdhw[5],
  * p >= 0, 0 <= out_pad < max(s, d).
  * Fast path: k = 3, s = 2, p = 1, d = 1 in all dims (out_pad 0 or 1),
  * C_out = 16, 1 <= C_in <= 8, W % 4 == 0 and x 16-byte aligned (per-parity
- * tap sets, TMA-staged input).  With W <= 32 it runs on the tensor cores as
- * 3xTF32 (each operand split v = hi + lo, each product summed as lo*hi +
- * hi*lo + hi*hi in fp32), otherwise on the FP32 pipe; both meet
- * max |y - exact| <= 1e-5 * (1 + |exact|).  Every other valid request runs a
+ * tap sets, TMA-staged input): on the tensor cores as 3xTF32 (each operand
+ * split v = hi + lo, each product summed as lo*hi + hi*lo + hi*hi in fp32),
+ * meeting max |y - exact| <= 1e-5 * (1 + |exact|); where the tensor-core
+ * kernel cannot run (its shared memory or tensor memory unavailable), on the
+ * FP32 pipe at the same bound.  Every other valid request runs a
  * direct per-output kernel.
  */
 aps_status aps_convtranspose3d_out_shape(const int64_t in_ncdhw[5], int64_t c_out,

@@ -273,8 +273,8 @@ def test_fused_general_geometry_tables(xs, cout, k, s, p, op, d, q):
 
 # ------------------------------------------------------------ convtranspose3d
 CONVT3D_CASES = [  # (x shape, C_out, k, s, p, d, op, bias)
-    # W > 32: the FP32-pipe k3 s2 p1 d1 kernel (one and two column blocks, C_in 1..8,
-    # output padding)
+    # W > 32: the tensor-core kernel in 32-column blocks, outputs from registers (two and
+    # three blocks, the last one partial; C_in 1..8, output padding)
     ((1, 3, 4, 19, 36), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (0, 0, 0), True),
     ((1, 8, 3, 9, 40), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (1, 1, 1), False),
     ((1, 5, 2, 7, 36), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (0, 1, 0), True),
@@ -336,7 +336,7 @@ def test_convt3d_unaligned_input_takes_the_direct_kernel():
                  what="convt3d unaligned x")
 
 
-@pytest.mark.parametrize("cfg", [5, 10])
+@pytest.mark.parametrize("cfg", [5, 10, 12])
 def test_convt3d_full_workload_sampled_planes(cfg):
     wl = workloads.get(cfg)
     p = wl.params
