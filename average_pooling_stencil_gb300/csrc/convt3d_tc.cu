@@ -16,21 +16,22 @@
 // hi(x)lo(w) + hi(x)hi(w) in fp32.
 //
 // Design (GB300): one persistent CTA per SM, two groups of four warps and a
-// TMA warp.  A unit is 4 input rows x (W <= 32) input columns of one (n, md)
-// input plane -- outputs: planes 2md, 2md+1, rows 8*blk .. +7, all columns --
-// or, for W > 32, a 32-column block of them (box origin 32*mwb, 128-byte
-// aligned), whose outputs leave straight from registers.
+// TMA warp.  A unit is 128 input positions of one (n, md) input plane: 4 rows of
+// up to 32 columns, 2 rows of up to 64 or 1 row of up to 128 (each row spread over
+// 1, 2 or 4 warps of a group) -- outputs: planes 2md, 2md+1, twice the unit's rows,
+// all columns -- or, for rows wider than 128, a 128-column block of one row (box
+// origin 128*mwb, 128-byte aligned), whose outputs leave straight from registers.
 // CTA-local unit k goes to group k % 2 and stage k % 8 of a ring the TMA
-// warp fills (one 4-D box per unit: C_in x 2 planes x 5 rows x 36 columns,
-// zero-filled outside the tensor).  Warp q of a group owns input row q of
-// the unit and tensor-memory lanes 32q..32q+31, lane l input column l.  Per
+// warp fills (one 4-D box per unit: C_in x 2 planes x (rows + 1) x (columns + 1,
+// rounded up to 4), zero-filled outside the tensor).  Warp q of a group owns
+// tensor-memory lanes 32q..32q+31, one position of the unit per lane.  Per
 // unit a thread reads its 8*C_in inputs, writes its hi and lo A row into its
 // lane (tcgen05.st); after a group barrier the group's MMA thread issues 9
 // MMAs (M 128, N 128, K 8; A in tensor memory, B = the parity-tap matrix in
 // shared memory) and commits.  The epilogue loads the 128 accumulator columns
 // in four tcgen05.ld of 32 (one (r_d, r_h) pair and both r_w each), adds the
 // bias and writes the group's staging block, where output plane r_d, channel
-// co is one run of up to 8 x Wo floats at an offset congruent to its
+// co is one run of up to 2 x rows x Wo floats at an offset congruent to its
 // destination mod 16 bytes.  Each run then leaves by one cp.async.bulk issued by
 // its own lane (head and tail by plain stores); a group restages only after
 // its previous copies have read the block, while the other group computes.
@@ -58,10 +59,9 @@ constexpr int GROUPS = 2;
 constexpr int WORKERS = 4 * GROUPS;        // warps 0..7
 constexpr int W_FILL = WORKERS;            // warp 8: the TMA loads of the input ring
 constexpr int THREADS = 32 * (WORKERS + 1);   // 288
-constexpr int MROWS = 4;                   // input rows per unit (one per warp of a group)
-constexpr int XR = MROWS + 1;              // staged input rows
-constexpr int BWMAX = 36;                  // staged input columns (W + 1, rounded up to 4)
-constexpr int OROWS = 2 * MROWS;           // output rows per unit
+// A unit is 128 input positions: 4 rows of up to 32 columns, 2 of up to 64 or 1 of
+// up to 128 (lgw = 0, 1, 2: each input row spread over 1 << lgw warps of a group),
+// or a 128-column block of a wider row.
 constexpr int STAGES = 4 * GROUPS;         // input ring: four units in flight per group
 constexpr int TMEM_COLS = 512;
 constexpr int GROUP_COLS = TMEM_COLS / GROUPS;   // 256
@@ -91,21 +91,23 @@ struct Slot {
 };
 static_assert(sizeof(Slot) * STAGES <= OFF_BIAS - OFF_SLOT, "slots fit");
 
-__host__ __device__ inline int stage_stride_of(int Cin) {
-    return (Cin * 2 * XR * BWMAX + 31) & ~31;
+// Floats of one stage: the box (C_in x 2 planes x XRu rows x BW columns), plus the
+// columns a lane past the last input column may read on (at most UW).
+__host__ __device__ inline int stage_stride_of(int Cin, int XRu, int BW, int UW) {
+    return (Cin * 2 * XRu * BW + UW + 32 + 31) & ~31;
 }
 // Output staging of one group: run (r_d, co) at r_d*RDS + co*CH + a0, where
 // CH = the channel step of y mod 4 and RDS = the plane step of y mod 4 (both
 // mod 4), so that one shift a0 per unit gives every run the alignment of its
-// destination; each run holds up to OROWS x Wo floats after a shift of <= 3.
-__host__ __device__ inline int chan_stride_of(int Wo, int ac) {
-    return ((OROWS * Wo + 6) & ~3) + ac;
+// destination; each run holds up to orows x Wo floats after a shift of <= 3.
+__host__ __device__ inline int chan_stride_of(int Wo, int ac, int orows) {
+    return ((orows * Wo + 6) & ~3) + ac;
 }
-__host__ __device__ inline int plane_stride_of(int Wo, int ac, int ap) {
-    return ((COUT * chan_stride_of(Wo, ac) + 3) & ~3) + ap;
+__host__ __device__ inline int plane_stride_of(int Wo, int ac, int ap, int orows) {
+    return ((COUT * chan_stride_of(Wo, ac, orows) + 3) & ~3) + ap;
 }
-__host__ __device__ inline int staging_floats_of(int Wo, int ac, int ap) {
-    return (2 * plane_stride_of(Wo, ac, ap) + 31) & ~31;
+__host__ __device__ inline int staging_floats_of(int Wo, int ac, int ap, int orows) {
+    return (2 * plane_stride_of(Wo, ac, ap, orows) + 31) & ~31;
 }
 }  // namespace c3t
 
@@ -122,8 +124,8 @@ template <int CIN>
 __global__ void __launch_bounds__(c3t::THREADS, 1)
     convt3d_tc_kernel(const __grid_constant__ CUtensorMap xmap, const float *__restrict__ w,
                       const float *__restrict__ bias, float *__restrict__ y, int D, int H, int W,
-                      int BW, int Do, int Ho, int Wo, int n_mhb, int n_mwb, int direct_rt,
-                      long long n_units, unsigned int *status) {
+                      int BW, int Do, int Ho, int Wo, int n_mhb, int n_mwb, int lgw,
+                      int direct_rt, long long n_units, unsigned int *status) {
     pdl_trigger();
     pdl_wait();
     using namespace c3t;
@@ -140,14 +142,16 @@ __global__ void __launch_bounds__(c3t::THREADS, 1)
     Slot *slot = reinterpret_cast<Slot *>(smraw + OFF_SLOT);
     float *bsm = reinterpret_cast<float *>(smraw + OFF_BIAS);
     uint32_t *bop = reinterpret_cast<uint32_t *>(smraw + OFF_B);
-    const int stage_stride = stage_stride_of(CIN);
-    float *xs = reinterpret_cast<float *>(smraw + HEAD_BYTES);   // [STAGES][C_in][2][XR][BW]
+    const int MR = 4 >> lgw, XRu = MR + 1, UW = 32 << lgw;   // unit rows, staged rows, width
+    const int orows = 2 * MR;                                   // output rows per unit
+    const int stage_stride = stage_stride_of(CIN, XRu, BW, UW);
+    float *xs = reinterpret_cast<float *>(smraw + HEAD_BYTES);   // [STAGES][C_in][2][XRu][BW]
     const long long plane = (long long)Ho * Wo;
     const long long cstride = (long long)Do * plane;              // between output channels
     const int ac = (int)(cstride & 3), ap = (int)(plane & 3);
-    const int CH = chan_stride_of(Wo, ac), RDS = plane_stride_of(Wo, ac, ap);
+    const int CH = chan_stride_of(Wo, ac, orows), RDS = plane_stride_of(Wo, ac, ap, orows);
     float *ost = xs + STAGES * stage_stride;                       // [GROUPS][2][16][CH]
-    const int stage_floats = CIN * 2 * XR * BW;
+    const int stage_floats = CIN * 2 * XRu * BW;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     if (tid == 0) {
@@ -212,11 +216,11 @@ __global__ void __launch_bounds__(c3t::THREADS, 1)
                 const long long n = t / D;
                 slot[s].n = n;
                 slot[s].md = md;
-                slot[s].mh0 = MROWS * mhb;
-                slot[s].mw0 = 32 * mwb;
+                slot[s].mh0 = MR * mhb;
+                slot[s].mw0 = UW * mwb;
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 mbar_arrive_expect_tx(&full[s], (uint32_t)stage_floats * 4u);
-                tma_load_4d(xs + s * stage_stride, &xmap, &full[s], 32 * mwb, MROWS * mhb, md,
+                tma_load_4d(xs + s * stage_stride, &xmap, &full[s], UW * mwb, MR * mhb, md,
                             (int)(n * CIN));
             }
             // the loads in flight land before the CTA exits (the latest of each stage)
@@ -227,12 +231,15 @@ __global__ void __launch_bounds__(c3t::THREADS, 1)
     } else {
         // ------------------------------------------------------------ workers
         const int grp = warp >> 2, q = warp & 3;
+        // this thread's input position in the unit: row mr, column mc (tensor-memory
+        // lane 32q + lane = mr * UW + mc)
+        const int mr = q >> lgw, mc = ((q & ((1 << lgw) - 1)) << 5) + lane;
         const uint32_t lane_q = (uint32_t)(32 * q) << 16;   // this warp's tensor-memory lanes
         const uint32_t gcol = (uint32_t)(grp * GROUP_COLS); // the group's tile buffer
         const int gbar = 1 + grp;                            // the group's barrier (0 is __syncthreads)
         constexpr uint32_t IDESC = tc::idesc_tf32(128, NCOL);
         const uint32_t b_hi = smem_u32(bop), b_lo = b_hi + CIN * B_CI_BYTES;
-        float *og = ost + grp * staging_floats_of(Wo, ac, ap);   // the group's staging block
+        float *og = ost + grp * staging_floats_of(Wo, ac, ap, orows);   // the group's staging block
         float bias_r[COUT];
 #pragma unroll
         for (int co = 0; co < COUT; ++co) bias_r[co] = bsm[co];
@@ -258,19 +265,19 @@ __global__ void __launch_bounds__(c3t::THREADS, 1)
             }
             ok = __all_sync(0xffffffffu, ok);
 
-            // ---- the A row of input position (mh0 + q, lane): hi and lo of
+            // ---- the A row of input position (mh0 + mr, mw0 + mc): hi and lo of
             // its 8*C_in neighbourhood values
             if constexpr (CIN > 3) {
               if (ok) {
                 // one input channel at a time: its 8 hi and 8 lo columns
-                const float *xp = xs + s * stage_stride + q * BW + lane;
+                const float *xp = xs + s * stage_stride + mr * BW + mc;
 #pragma unroll
                 for (int ci = 0; ci < CIN; ++ci) {
                     uint32_t hv[8], lv[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const int a = e >> 2, b = (e >> 1) & 1, c = e & 1;
-                        const float v = xp[((ci * 2 + a) * XR + b) * BW + c];
+                        const float v = xp[((ci * 2 + a) * XRu + b) * BW + c];
                         hv[e] = __float_as_uint(v) & 0xFFFFE000u;
                         lv[e] = __float_as_uint(v - __uint_as_float(hv[e]));
                     }
@@ -280,14 +287,14 @@ __global__ void __launch_bounds__(c3t::THREADS, 1)
                 tc::tmem_st_wait();
               }
             } else if (ok) {
-                const float *xp = xs + s * stage_stride + q * BW + lane;
+                const float *xp = xs + s * stage_stride + mr * BW + mc;
                 uint32_t av[16 * CIN];   // hi[0 .. 8*CIN), then lo
 #pragma unroll
                 for (int ci = 0; ci < CIN; ++ci)
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const int a = e >> 2, b = (e >> 1) & 1, c = e & 1;
-                        const float v = xp[((ci * 2 + a) * XR + b) * BW + c];
+                        const float v = xp[((ci * 2 + a) * XRu + b) * BW + c];
                         const uint32_t hi = __float_as_uint(v) & 0xFFFFE000u;
                         av[ci * 8 + e] = hi;
                         av[8 * CIN + ci * 8 + e] = __float_as_uint(v - __uint_as_float(hi));
@@ -321,7 +328,7 @@ __global__ void __launch_bounds__(c3t::THREADS, 1)
             // where the outputs go, read before the stage and its slot are released
             const long long gn = slot[s].n;
             const int gmd = slot[s].md, gmh0 = slot[s].mh0, gmw0 = slot[s].mw0;
-            const bool in_w = gmw0 + lane < W;   // this lane's input column exists
+            const bool in_w = gmw0 + mc < W;   // this thread's input column exists
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
             if (EARLY) {
@@ -340,10 +347,10 @@ __global__ void __launch_bounds__(c3t::THREADS, 1)
             okd = __all_sync(0xffffffffu, okd);
             if (DIRECT) {
                 if (tc::named_bar_or(gbar, 128, !okd)) break;
-                // outputs straight from registers: lane l holds output columns
-                // 2(mw0 + l) and 2(mw0 + l) + 1 of every channel of its (r_d, r_h) row
+                // outputs straight from registers: the thread holds output columns
+                // 2(mw0 + mc) and 2(mw0 + mc) + 1 of every channel of its (r_d, r_h) row
                 const int oh0 = 2 * gmh0;
-                const int nrows = Ho - oh0 < OROWS ? Ho - oh0 : OROWS;
+                const int nrows = Ho - oh0 < orows ? Ho - oh0 : orows;
                 float *y0 = y + ((gn * COUT) * Do + 2 * gmd) * plane + (long long)oh0 * Wo + 2 * gmw0;
                 tc::tc_fence_after();
 #pragma unroll 1
@@ -351,10 +358,10 @@ __global__ void __launch_bounds__(c3t::THREADS, 1)
                     const int rd = c >> 1, rh = c & 1;
                     uint32_t v[32];   // v[rw*16 + co]
                     tc::tmem_ld32(tmem + lane_q + gcol + D_COL + 32 * c, v);
-                    const int row = 2 * q + rh;
+                    const int row = 2 * mr + rh;
                     if (2 * gmd + rd < Do && row < nrows && in_w) {
-                        float *yp = y0 + rd * plane + (long long)row * Wo + 2 * lane;
-                        const bool w1 = 2 * (gmw0 + lane) + 1 < Wo;
+                        float *yp = y0 + rd * plane + (long long)row * Wo + 2 * mc;
+                        const bool w1 = 2 * (gmw0 + mc) + 1 < Wo;
 #pragma unroll
                         for (int co = 0; co < COUT; ++co) {
                             yp[0] = __uint_as_float(v[co]) + bias_r[co];
@@ -374,7 +381,7 @@ __global__ void __launch_bounds__(c3t::THREADS, 1)
                 __syncwarp();
                 if (tc::named_bar_or(gbar, 128, !okd)) break;
                 const int oh0 = 2 * gmh0;
-                const int nrows = Ho - oh0 < OROWS ? Ho - oh0 : OROWS;
+                const int nrows = Ho - oh0 < orows ? Ho - oh0 : orows;
                 float *y0 = y + ((gn * COUT) * Do + 2 * gmd) * plane + (long long)oh0 * Wo;
                 const int a0 = (int)((reinterpret_cast<uintptr_t>(y0) >> 2) & 3u);
                 {
@@ -384,10 +391,10 @@ __global__ void __launch_bounds__(c3t::THREADS, 1)
                         const int rd = c >> 1, rh = c & 1;
                         uint32_t v[32];   // v[rw*16 + co]
                         tc::tmem_ld32(tmem + lane_q + gcol + D_COL + 32 * c, v);
-                        const int row = 2 * q + rh;
+                        const int row = 2 * mr + rh;
                         if (2 * gmd + rd < Do && row < nrows && in_w) {
-                            float *sp = og + rd * RDS + a0 + row * Wo + 2 * lane;
-                            const bool w1 = 2 * lane + 1 < Wo;
+                            float *sp = og + rd * RDS + a0 + row * Wo + 2 * mc;
+                            const bool w1 = 2 * mc + 1 < Wo;
     #pragma unroll
                             for (int co = 0; co < COUT; ++co) {
                                 sp[0] = __uint_as_float(v[co]) + bias_r[co];
@@ -462,16 +469,22 @@ aps_status launch_convt3d_tc(const float *x, const int64_t in[5], const float *w
         reinterpret_cast<uintptr_t>(x) % 16 != 0 || D >= (1 << 30) || H >= (1 << 30) ||
         N * Cin >= (1ll << 31) || N * D >= (1ll << 40))
         return APS_ERR_UNSUPPORTED;
-    // staged columns: the block's 32 (or W) and one more (past W it reads as zero)
-    const int BW = W > 32 ? BWMAX : (int)((W + 1 + 3) & ~3);
-    const int64_t n_mhb = ceil_div(H, MROWS), n_mwb = ceil_div(W, (int64_t)32);
+    // unit: 128 positions -- 4 rows of <= 32 columns, 2 of <= 64, 1 of <= 128, or a
+    // 128-column block of a wider row; staged columns: the unit's and one more (past
+    // W it reads as zero), a multiple of 4
+    const int lgw = W <= 32 ? 0 : W <= 64 ? 1 : 2;
+    const int MR = 4 >> lgw, UW = 32 << lgw;
+    const int BW = (int)((std::min<int64_t>(W, UW) + 1 + 3) & ~3);
+    const int64_t n_mhb = ceil_div(H, (int64_t)MR), n_mwb = ceil_div(W, (int64_t)UW);
     const long long n_units = N * D * n_mhb * n_mwb;
-    const int direct = direct_of((int)Cin) || W > 32;
+    // outputs from registers for C_in > 3 and for blocks of wider rows (whose
+    // runs are not whole rows); else staged runs leaving by bulk copies
+    const int direct = direct_of((int)Cin) || n_mwb > 1;
     CUtensorMap map;
     const cuuint64_t dims[4] = {(cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)D, (cuuint64_t)(N * Cin)};
     const cuuint64_t strides[3] = {(cuuint64_t)(W * 4), (cuuint64_t)(H * W * 4),
                                    (cuuint64_t)(D * H * W * 4)};
-    const cuuint32_t box[4] = {(cuuint32_t)BW, (cuuint32_t)XR, 2, (cuuint32_t)Cin};
+    const cuuint32_t box[4] = {(cuuint32_t)BW, (cuuint32_t)(MR + 1), 2, (cuuint32_t)Cin};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     if (!encode_tiled(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(x), dims,
                       strides, box, estr))
@@ -479,10 +492,10 @@ aps_status launch_convt3d_tc(const float *x, const int64_t in[5], const float *w
     const int ac = (int)((Do * Ho * Wo) & 3), ap = (int)((Ho * Wo) & 3);
     const size_t smem =
         (size_t)head_bytes_of((int)Cin) +
-        ((size_t)STAGES * stage_stride_of((int)Cin) +
-         (direct ? 0 : (size_t)GROUPS * staging_floats_of((int)Wo, ac, ap))) * 4;
+        ((size_t)STAGES * stage_stride_of((int)Cin, MR + 1, BW, UW) +
+         (direct ? 0 : (size_t)GROUPS * staging_floats_of((int)Wo, ac, ap, 2 * MR))) * 4;
     void (*const kerns[CIN_MAX])(const CUtensorMap, const float *, const float *, float *, int,
-                                 int, int, int, int, int, int, int, int, int, long long,
+                                 int, int, int, int, int, int, int, int, int, int, long long,
                                  unsigned int *) = {
         convt3d_tc_kernel<1>, convt3d_tc_kernel<2>, convt3d_tc_kernel<3>, convt3d_tc_kernel<4>,
         convt3d_tc_kernel<5>, convt3d_tc_kernel<6>, convt3d_tc_kernel<7>, convt3d_tc_kernel<8>};
@@ -491,8 +504,8 @@ aps_status launch_convt3d_tc(const float *x, const int64_t in[5], const float *w
     if (resident_ctas((const void *)kern, THREADS, (int)smem) < 1) return APS_ERR_UNSUPPORTED;
     const long long grid = std::min<long long>(sm_count(), n_units);
     const cudaError_t e = launch_pdl(kern, dim3((unsigned)grid), dim3(THREADS), smem, st, map, w, bias, y, (int)D, (int)H,
-               (int)W, BW, (int)Do, (int)Ho, (int)Wo, (int)n_mhb, (int)n_mwb, direct, n_units,
-               status_word());
+               (int)W, BW, (int)Do, (int)Ho, (int)Wo, (int)n_mhb, (int)n_mwb, lgw, direct,
+               n_units, status_word());
     return launch_status(e);
 }
 

@@ -273,12 +273,18 @@ def test_fused_general_geometry_tables(xs, cout, k, s, p, op, d, q):
 
 # ------------------------------------------------------------ convtranspose3d
 CONVT3D_CASES = [  # (x shape, C_out, k, s, p, d, op, bias)
-    # W > 32: the tensor-core kernel in 32-column blocks, outputs from registers (two and
-    # three blocks, the last one partial; C_in 1..8, output padding)
+    # W > 32: units of 2 rows of up to 64 columns or 1 row of up to 128 (C_in <= 3: staged
+    # runs; C_in 4..8: outputs from registers), and 128-column blocks of wider rows
+    # (outputs from registers; the last block partial); output padding
     ((1, 3, 4, 19, 36), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (0, 0, 0), True),
     ((1, 8, 3, 9, 40), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (1, 1, 1), False),
     ((1, 5, 2, 7, 36), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (0, 1, 0), True),
     ((1, 3, 2, 2, 68), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (1, 0, 1), True),
+    ((2, 2, 3, 5, 64), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (0, 0, 0), True),
+    ((1, 1, 2, 3, 128), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (1, 1, 1), True),
+    ((1, 3, 2, 4, 100), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (0, 1, 1), False),
+    ((1, 3, 2, 3, 260), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (0, 0, 1), True),
+    ((1, 8, 2, 2, 136), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), (1, 0, 0), True),
     # W <= 32: the tensor-core kernel, C_in 1..3 with staged output runs and C_in 4..8
     # with outputs from registers (output padding in every dim, H not a multiple of 4, a
     # single input plane, no bias)
