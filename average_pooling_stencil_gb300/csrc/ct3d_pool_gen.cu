@@ -18,6 +18,10 @@
 // bias)*scale2.  Input cells outside the tensor contribute nothing (they are
 // the transposed convolution's missing terms, not zero padding of x).
 //
+// Tiled kernel: geometries with one phase per dim, the window moving one input
+// per pooled output and at most 3 offsets per dim (some dim with 3) -- e.g. 4-tap
+// kernels at stride 2 with pool 2 -- run as a tiled 3x3x3 correlation (below).
+//
 // Kernel: each CTA builds Weff for all phase combinations in shared memory
 // (host-built per-dim tables come in the launch parameters), then each thread
 // takes one pooled position and accumulates 16 output channels at a time in
@@ -237,6 +241,181 @@ __global__ void __launch_bounds__(gen::THREADS)
     }
 }
 
+// ---------------------------------------------------------------- tiled form
+// Geometries with one phase per dim and the window moving one input per pooled
+// output (pool size = stride), at most 3 input offsets per dim: the pooled
+// output is a plain 3x3x3 correlation of the input (zero outside it) from its
+// origin P + i0, so it is tiled like the pages' k3 s2 p1 geometry.  A CTA of 8
+// warps takes units of 16 pooled rows x 32 pooled columns of one (n, pd) plane
+// and one 16-channel output block; the unit's input -- C_in channels x 3 planes
+// x 18 rows x 40 columns from the origin, its x coordinate rounded down to a
+// multiple of 4 (a TMA box must start 16-byte aligned) -- is one 4-D TMA box,
+// double-buffered behind mbarriers with bounded waits.  Warp w owns pooled rows
+// 2w, 2w+1 and lane l pooled column l, all 16 channels of the block: per input
+// channel a thread reads its 3 x 4 x 3 window once and applies the 27 taps with
+// broadcast float4 weight reads and packed fp32x2 FMAs.  Outputs leave by
+// whole-warp stores of 32 consecutive columns per channel row.
+namespace gent {
+constexpr int WARPS = 8, THREADS = 32 * WARPS;
+constexpr int RB = 2 * WARPS;       // pooled rows per unit
+constexpr int WB = 32;              // pooled columns per unit
+constexpr int XR = RB + 2;          // staged rows
+constexpr int BW = 40;              // staged columns: 32 + 2, shifted by up to 3
+constexpr int NT = 27;              // taps (3 x 3 x 3)
+constexpr int CO_T = 16;
+__host__ __device__ inline int stage_stride_of(int Cin) { return (Cin * 3 * XR * BW + 31) & ~31; }
+}  // namespace gent
+
+__global__ void __launch_bounds__(gent::THREADS, 2)
+    ct3d_pool_gen_tiled_kernel(const __grid_constant__ CUtensorMap xmap,
+                               const float *__restrict__ w, const float *__restrict__ conv_bias,
+                               const float *__restrict__ bias, float wscale, float scale1,
+                               float scale2, float *__restrict__ y, int Cin, int Cout, int COP,
+                               int Do, int Ho, int Wo, int kD, int kH, int kW, int i0d, int i0h,
+                               int i0w, int n_cob, int n_hb, int n_wb, long long n_units,
+                               const __grid_constant__ gen::Geom g, unsigned int *status) {
+    using namespace gent;
+    pdl_trigger();
+    pdl_wait();
+    extern __shared__ __align__(128) float smt[];
+    const int stage_stride = stage_stride_of(Cin);
+    float *xs = smt;                                  // [2][Cin][3][XR][BW]
+    float *wsm = xs + 2 * stage_stride;               // [Cin][27][COP]
+    float *bsm = wsm + (size_t)Cin * NT * COP;        // [COP]
+    uint64_t *bar = reinterpret_cast<uint64_t *>(bsm + COP);   // [2]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t stage_bytes = (uint32_t)(Cin * 3 * XR * BW) * 4u;
+
+    struct Unit {
+        long long n;
+        int cob, pd, ph0, pw0;
+    };
+    auto unit = [&](long long u) {
+        Unit t;
+        t.cob = (int)(u % n_cob);
+        long long r = u / n_cob;
+        t.pw0 = (int)(r % n_wb) * WB;
+        r /= n_wb;
+        t.ph0 = (int)(r % n_hb) * RB;
+        r /= n_hb;
+        t.pd = (int)(r % Do);
+        t.n = r / Do;
+        return t;
+    };
+    // the box origin's x rounded down to a multiple of 4; the thread then reads
+    // from column (origin - rounded) + lane
+    auto stage = [&](const Unit &t, int b) {
+        if (tid == 0) {
+            const int x0 = (t.pw0 + i0w) & ~3;
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive_expect_tx(&bar[b], stage_bytes);
+            tma_load_4d(xs + b * stage_stride, &xmap, &bar[b], x0, t.ph0 + i0h, t.pd + i0d,
+                        (int)(t.n * Cin));
+        }
+    };
+    if (tid == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    Unit cur{};
+    if ((long long)blockIdx.x < n_units) {
+        cur = unit(blockIdx.x);
+        stage(cur, 0);
+    }
+    // ---- collapsed weights [ci][tap][co] (scaled) and the folded bias, once per CTA
+    const gen::Dim &GD = g.d[0], &GH = g.d[1], &GW = g.d[2];
+    for (int e = tid; e < Cin * NT * COP; e += THREADS) {
+        const int co = e % COP, tap = (e / COP) % NT, ci = e / (COP * NT);
+        const int a = tap / 9, b = (tap / 3) % 3, c = tap % 3;
+        float v = 0.f;
+        if (co < Cout && a < GD.nd[0] && b < GH.nd[0] && c < GW.nd[0])
+            v = gen::tap_set_sum(w + ((long long)ci * Cout + co) * kD * kH * kW, kH, kW,
+                                 GD.kmask[0][a], GH.kmask[0][b], GW.kmask[0][c]) * wscale;
+        wsm[e] = v;
+    }
+    for (int co = tid; co < COP; co += THREADS) {
+        const float cb = co < Cout && conv_bias ? __ldg(conv_bias + co) : 0.f;
+        bsm[co] = co < Cout ? (cb * scale1 + __ldg(bias + co)) * scale2 : 0.f;
+    }
+    __syncthreads();
+
+    const long long plane = (long long)Ho * Wo;
+    long long k = 0;
+    for (long long u = blockIdx.x; u < n_units; u += gridDim.x, ++k) {
+        const int b = (int)(k & 1);
+        const bool more = u + gridDim.x < n_units;
+        if (more) stage(unit(u + gridDim.x), b ^ 1);
+        const bool ok = mbar_wait(&bar[b], (uint32_t)(k >> 1) & 1u);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                record_error(status, APS_DEVERR_TIMEOUT);
+                if (more) mbar_wait(&bar[b ^ 1], (uint32_t)((k + 1) >> 1) & 1u);
+            }
+            return;
+        }
+        const int co0 = cur.cob * CO_T;
+        float2 acc[CO_T / 2][2];
+#pragma unroll
+        for (int c2 = 0; c2 < CO_T / 2; ++c2) {
+            const float2 bv = make_float2(bsm[co0 + 2 * c2], bsm[co0 + 2 * c2 + 1]);
+            acc[c2][0] = bv;
+            acc[c2][1] = bv;
+        }
+        const int shift = (cur.pw0 + i0w) - ((cur.pw0 + i0w) & ~3);
+        const float *xb = xs + b * stage_stride + (2 * warp) * BW + shift + lane;
+#pragma unroll 1
+        for (int ci = 0; ci < Cin; ++ci) {
+            float xv[3][4][3];
+#pragma unroll
+            for (int a = 0; a < 3; ++a)
+#pragma unroll
+                for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+                    for (int c = 0; c < 3; ++c)
+                        xv[a][rr][c] = xb[((ci * 3 + a) * XR + rr) * BW + c];
+            const float4 *wq = reinterpret_cast<const float4 *>(wsm + (size_t)ci * NT * COP + co0);
+#pragma unroll
+            for (int tap = 0; tap < NT; ++tap) {
+                const int a = tap / 9, bb = (tap / 3) % 3, c = tap % 3;
+                const float4 *wt = wq + tap * (COP / 4);
+                const float4 w0 = wt[0], w1 = wt[1], w2 = wt[2], w3 = wt[3];
+                const float2 wp[CO_T / 2] = {make_float2(w0.x, w0.y), make_float2(w0.z, w0.w),
+                                             make_float2(w1.x, w1.y), make_float2(w1.z, w1.w),
+                                             make_float2(w2.x, w2.y), make_float2(w2.z, w2.w),
+                                             make_float2(w3.x, w3.y), make_float2(w3.z, w3.w)};
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const float xg = xv[a][i + bb][c];
+#pragma unroll
+                    for (int c2 = 0; c2 < CO_T / 2; ++c2)
+                        acc[c2][i] = __ffma2_rn(make_float2(xg, xg), wp[c2], acc[c2][i]);
+                }
+            }
+        }
+        // ---- outputs: per channel and row, one whole-warp store of 32 columns
+        const int pw = cur.pw0 + lane;
+        float *yb = y + ((cur.n * Cout) * Do + cur.pd) * plane;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int ph = cur.ph0 + 2 * warp + i;
+            if (ph < Ho && pw < Wo) {
+                float *yr = yb + (long long)ph * Wo + pw;
+#pragma unroll
+                for (int c2 = 0; c2 < CO_T / 2; ++c2) {
+                    const int co = co0 + 2 * c2;
+                    if (co < Cout) yr[(long long)co * Do * plane] = acc[c2][i].x;
+                    if (co + 1 < Cout) yr[(long long)(co + 1) * Do * plane] = acc[c2][i].y;
+                }
+            }
+        }
+        // every thread is done with stage b before the next iteration refills it
+        __syncthreads();
+        if (more) cur = unit(u + gridDim.x);
+    }
+}
+
 namespace {
 int gcd_i(int a, int b) {
     while (b) {
@@ -302,6 +481,45 @@ aps_status launch_ct3d_pool_gen(const float *x, const int64_t in[5], const float
     for (int i = 0; i < 3; ++i)
         if (!build_dim(k[i], s[i], p[i], d[i], pool_k, g.d[i])) return APS_ERR_UNSUPPORTED;
     const int COP = (int)((c_out + CO_T - 1) / CO_T) * CO_T;
+    // one phase per dim, the window moving one input per pooled output, at most 3
+    // input offsets per dim: the tiled 3x3x3 form (TMA-staged, 16-byte input rows)
+    bool tiled = in[1] <= 8 && in[4] % 4 == 0 && reinterpret_cast<uintptr_t>(x) % 16 == 0 &&
+                 in[0] * in[1] < ((int64_t)1 << 31) && (int64_t)COP * in[1] * gent::NT * 4 <= 32768;
+    for (int i = 0; i < 3; ++i)
+        tiled = tiled && g.d[i].T == 1 && g.d[i].step == 1 && g.d[i].md <= 3 && g.d[i].nd[0] > 0;
+    // (at most 2 offsets in every dim: the unrolled 2 x 2 x 2 kernel below does a third
+    // of the multiply-adds)
+    tiled = tiled && (g.d[0].md == 3 || g.d[1].md == 3 || g.d[2].md == 3);
+    if (tiled) {
+        const int Cin = (int)in[1];
+        const size_t smem_t = ((size_t)2 * gent::stage_stride_of(Cin) +
+                               (size_t)Cin * gent::NT * COP + COP) * 4 + 16;
+        const int per_sm_t = resident_ctas((const void *)ct3d_pool_gen_tiled_kernel, gent::THREADS,
+                                           (int)smem_t);
+        CUtensorMap map;
+        const cuuint64_t dims[4] = {(cuuint64_t)in[4], (cuuint64_t)in[3], (cuuint64_t)in[2],
+                                    (cuuint64_t)(in[0] * in[1])};
+        const cuuint64_t strides[3] = {(cuuint64_t)(in[4] * 4), (cuuint64_t)(in[3] * in[4] * 4),
+                                       (cuuint64_t)(in[2] * in[3] * in[4] * 4)};
+        const cuuint32_t box[4] = {(cuuint32_t)gent::BW, (cuuint32_t)gent::XR, 3, (cuuint32_t)Cin};
+        const cuuint32_t estr[4] = {1, 1, 1, 1};
+        if (per_sm_t >= 1 && encode_tiled(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
+                                          const_cast<float *>(x), dims, strides, box, estr)) {
+            const int n_cob = COP / gent::CO_T;
+            const int64_t n_hb = ceil_div(out[3], (int64_t)gent::RB);
+            const int64_t n_wb = ceil_div(out[4], (int64_t)gent::WB);
+            const long long n_units = out[0] * out[2] * n_hb * n_wb * n_cob;
+            const long long grid = std::min<long long>((long long)per_sm_t * sm_count(), n_units);
+            const float q3 = (float)pool_k * pool_k * pool_k;
+            const cudaError_t e = launch_pdl(
+                ct3d_pool_gen_tiled_kernel, dim3((unsigned)grid), dim3(gent::THREADS), smem_t, st,
+                map, w, conv_bias, bias, scale1 * scale2 / q3, scale1, scale2, y, Cin, (int)c_out,
+                COP, (int)out[2], (int)out[3], (int)out[4], k[0], k[1], k[2], g.d[0].i0[0],
+                g.d[1].i0[0], g.d[2].i0[0], n_cob, (int)n_hb, (int)n_wb, n_units, g,
+                status_word());
+            return launch_status(e);
+        }
+    }
     // offsets per phase at most 2 in every dim (the pages' geometry and its
     // pool variants), or at most 3 (4-tap kernels at stride 2, pool 2): unrolled
     // cells, Weff laid out ND x ND x ND per (ci, phase); the rest run-time loops

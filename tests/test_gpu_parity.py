@@ -261,7 +261,16 @@ def test_fused_general_geometry(cout, k, s, p, op, d, q):
     ((1, 2, 4, 5, 9), 20, (3, 4, 3), (2, 2, 2), (1, 1, 1), (1, 0, 1), (1, 1, 1), 2),
     ((1, 3, 3, 7, 10), 7, (5, 5, 3), (2, 2, 2), (2, 2, 1), (0, 0, 0), (1, 1, 1), 2),
     ((2, 2, 4, 6, 8), 16, (3, 3, 3), (2, 2, 2), (1, 1, 1), (0, 0, 0), (2, 1, 1), 2),
-    ((1, 2, 4, 5, 6), 9, (4, 4, 2), (2, 2, 1), (1, 2, 0), (0, 1, 0), (1, 1, 1), 3)])
+    ((1, 2, 4, 5, 6), 9, (4, 4, 2), (2, 2, 1), (1, 2, 0), (0, 1, 0), (1, 1, 1), 3),
+    # one phase per dim, pool = stride, 3 offsets in some dim, 16-byte rows: the tiled
+    # 3 x 3 x 3 kernel (a TMA box whose x origin is rounded down to 4; two and a ragged
+    # output-channel block; several row and column blocks; 8 input channels; a plain
+    # stride-1 3 x 3 x 3 convolution with pool 1)
+    ((2, 3, 5, 6, 8), 16, (4, 4, 4), (2, 2, 2), (1, 1, 1), (0, 0, 0), (1, 1, 1), 2),
+    ((1, 2, 4, 5, 36), 20, (3, 4, 3), (2, 2, 2), (1, 1, 1), (1, 0, 1), (1, 1, 1), 2),
+    ((1, 3, 3, 7, 40), 7, (5, 5, 3), (2, 2, 2), (2, 2, 1), (0, 0, 0), (1, 1, 1), 2),
+    ((2, 4, 3, 18, 68), 16, (3, 3, 3), (1, 1, 1), (1, 1, 1), (0, 0, 0), (1, 1, 1), 1),
+    ((1, 8, 2, 3, 4), 16, (4, 4, 4), (2, 2, 2), (1, 1, 1), (1, 1, 1), (1, 1, 1), 2)])
 def test_fused_general_geometry_tables(xs, cout, k, s, p, op, d, q):
     x, = rng_inputs(9, xs)
     w, cb, b = rng_inputs(10, (xs[1], cout) + k, (cout,), (cout,), lo=-0.2, hi=0.2)
