@@ -754,22 +754,21 @@ def run_reference(args):
     return 0
 
 
+# per_config columns: the driver keeps only the last 1500 characters of the
+# output, so each workload is one array in this order
+PER_CONFIG_COLS = ["us", "out_s", "frac", "bound", "dram_B", "cpu_out_s"]
+
+
 def per_config_entry(key, c, t, peaks, peak_src, cpu_out_s):
-    """One compact per_config entry: time, outputs/s, roofline, DRAM traffic per
-    launch (or "stale" / None) and the oracle's outputs/s on the host cores."""
+    """One per_config entry, in PER_CONFIG_COLS order: time per launch (us),
+    outputs/s, fraction of the binding roofline, its kind ("hbm": measured copy
+    peak; "alu": FP32 unit peak), DRAM bytes per launch from the kernel's profile
+    (or "stale" / None) and the oracle's outputs/s on the host cores."""
     r = roofline_for(c, t, peaks, peak_src, None)
     src = PROFILE_OF.get(key)
-    e = {"us": sig(1e6 * t), "out_s": sig(c.outputs / t), "bound": r["bound"],
-         "achieved": sig(r["achieved"]), "unit": r["unit"], "frac": sig(r["frac"], 3),
-         "traffic": sig(traffic_from_profile(src[0], src[1], key), 3) if src else None,
-         "cpu_out_s": sig(cpu_out_s, 3)}
-    if c.bound == "hbm+alu":
-        e["tflops"] = sig(r["achieved_tflops"])
-    if "frac_of_measured_ceiling" in r:
-        e["frac_meas"] = sig(r["frac_of_measured_ceiling"], 3)
-    if "tensor_frac_of_ceiling" in r:
-        e["tc_frac"] = sig(r["tensor_frac_of_ceiling"], 3)
-    return e
+    return [sig(1e6 * t), sig(c.outputs / t, 3), sig(r["frac"], 3), r["bound"],
+            sig(traffic_from_profile(src[0], src[1], key), 3) if src else None,
+            sig(cpu_out_s, 3)]
 
 
 def run_native(args):
@@ -911,7 +910,8 @@ def run_native(args):
         import oracle
         only = set(args.only.split(",")) if args.only else None
         want_cpu = ws == 1 and not args.no_cpu_baseline
-        per = {"_peaks": {"hbm_GB_s": peaks["hbm_gbs"],
+        per = {"_cols": PER_CONFIG_COLS,
+               "_peaks": {"hbm_GB_s": peaks["hbm_gbs"],
                           "fp32_TF_s": sig(fp32_peak_tflops(float(peaks.get("sm_max_mhz",
                                                                              2070.0)))),
                           "fp32_meas_TF_s": sig(peaks["fma_measured"]["packed"]),
@@ -950,9 +950,9 @@ def run_native(args):
                                                   whole=(mode == "graph"))[0]
             e = per_config_entry(key, c, t, peaks, peak_src, cpu_of.get(c.wl.name))
             if mode == "graph":
-                e.update(bound="launch", achieved=None, unit=None, frac=None)
+                e[2], e[3] = None, "launch"
             if t_flushed is not None:
-                e["us_flush"] = sig(1e6 * t_flushed)
+                per["_fused_us_after_flush"] = sig(1e6 * t_flushed)
             per[key] = e
             if want_cpu and mode == "graph":
                 # the tiny workload on one host thread as well

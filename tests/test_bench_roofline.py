@@ -111,8 +111,16 @@ def test_compact_json_round_trips_and_keeps_the_per_config_block_short():
                             bound="alu" if prec == 3 else "hbm",
                             tensor_passes={0: 3, 1: 1, 2: 3, 3: 0}[prec])
         per[key] = bench.per_config_entry(key, c, 303.3e-6, PEAKS, "measured", 2.1e7)
-    # the driver keeps a few KB of the line's tail; the whole block must fit in it
-    assert len(bench.compact_json({"per_config": per})) < 2800
+    per["_cols"] = bench.PER_CONFIG_COLS
+    per["_peaks"] = {"hbm_GB_s": 6780.7, "fp32_TF_s": 80.55, "fp32_meas_TF_s": 75.9,
+                     "tf32_gemm_TF_s": 1066.0}
+    per["_cpu"] = {"model": "Neoverse-V2", "threads": 16, "fused_tiny_1thread_s": 0.006503,
+                   "fused_tiny_1thread_out_s": 7750000.0}
+    per["_fused_us_after_flush"] = 42.63
+    # the driver keeps the last 1500 characters of the output; the whole block, and the
+    # line's closing braces, must fit in it
+    assert len(bench.compact_json({"per_config": per})) < 1450
+    assert all(len(v) == len(bench.PER_CONFIG_COLS) for k, v in per.items() if k[0] != "_")
 
 
 def test_both_arms_print_the_same_config():
