@@ -315,6 +315,38 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// k2 s2 p0 with whole windows (floor mode) and 16-byte rows: a thread takes two
+// adjacent outputs, i.e. one 16-byte run of each of the window's four input rows
+// (4 x LDG.128; a warp reads 512 contiguous bytes of each row), sums each window
+// in the (d, h, w) order of the kernel above and stores the pair with one 8-byte
+// store.  64-bit plane offsets; the pair index fits 32 bits.
+__global__ void __launch_bounds__(256)
+    avgpool3d_k2s2_vec_kernel(const float *__restrict__ x, float *__restrict__ y,
+                              unsigned pairs, int D, int H, int W, int Do, int Ho, int Wo) {
+    const unsigned half = (unsigned)Wo >> 1;   // output pairs per row
+    const size_t hw = (size_t)H * W;
+    for (unsigned idx = blockIdx.x * blockDim.x + threadIdx.x; idx < pairs;
+         idx += gridDim.x * blockDim.x) {
+        const unsigned pw = idx % half;
+        unsigned t = idx / half;
+        const unsigned oh = t % (unsigned)Ho;
+        t /= (unsigned)Ho;
+        const unsigned od = t % (unsigned)Do;
+        const unsigned nc = t / (unsigned)Do;
+        const float *p0 = x + ((size_t)nc * D + 2 * od) * hw + (size_t)(2 * oh) * W + 4 * pw;
+        const float4 a = __ldg(reinterpret_cast<const float4 *>(p0));
+        const float4 b = __ldg(reinterpret_cast<const float4 *>(p0 + W));
+        const float4 c = __ldg(reinterpret_cast<const float4 *>(p0 + hw));
+        const float4 e = __ldg(reinterpret_cast<const float4 *>(p0 + hw + W));
+        float s0 = 0.f, s1 = 0.f;
+        s0 += a.x; s0 += a.y; s0 += b.x; s0 += b.y; s0 += c.x; s0 += c.y; s0 += e.x; s0 += e.y;
+        s1 += a.z; s1 += a.w; s1 += b.z; s1 += b.w; s1 += c.z; s1 += c.w; s1 += e.z; s1 += e.w;
+        float2 *yp = reinterpret_cast<float2 *>(
+            y + (((size_t)nc * Do + od) * Ho + oh) * (size_t)Wo + 2 * pw);
+        *yp = make_float2(s0 / 8.f, s1 / 8.f);
+    }
+}
+
 aps_status launch_avgpool3d_direct(const float *x, const int64_t in[5], const int k[3],
                                    const int s[3], const int p[3], int count_include_pad,
                                    float *y, const int64_t out[5], cudaStream_t st) {
@@ -326,6 +358,21 @@ aps_status launch_avgpool3d_direct(const float *x, const int64_t in[5], const in
     const long long blocks =
         std::min<long long>(ceil_div(total, threads), (long long)sm_count() * 16);
     const bool cube = k[0] == k[1] && k[1] == k[2] && (k[0] == 2 || k[0] == 3);
+    // k2 s2 p0, every window whole, 16-byte input rows and 8-byte output pairs
+    if (cube && k[0] == 2 && s[0] == 2 && s[1] == 2 && s[2] == 2 && p[0] == 0 && p[1] == 0 &&
+        p[2] == 0 && out[2] == in[2] / 2 && out[3] == in[3] / 2 && out[4] == in[4] / 2 &&
+        in[4] % 4 == 0 && reinterpret_cast<uintptr_t>(x) % 16 == 0 &&
+        reinterpret_cast<uintptr_t>(y) % 8 == 0 && total / 2 < ((int64_t)1 << 31)) {
+        const long long pairs = total / 2;
+        const int sms = sm_count();
+        const long long blocks2 =
+            std::max<long long>(1, std::min<long long>(ceil_div(pairs, threads), (long long)sms * 8));
+        const cudaError_t e = launch_plain(
+            avgpool3d_k2s2_vec_kernel, dim3((unsigned)blocks2), dim3(threads), 0, st, x, y,
+            (unsigned)pairs, (int)in[2], (int)in[3], (int)in[4], (int)out[2], (int)out[3],
+            (int)out[4]);
+        return launch_status(e);
+    }
     // 32-bit output index (with headroom for the grid stride) and plane offsets
     if (cube && total <= ((int64_t)1 << 31) && in[2] * in[3] * in[4] < ((int64_t)1 << 31)) {
         const auto kern = k[0] == 2 ? avgpool3d_win_kernel<2> : avgpool3d_win_kernel<3>;

@@ -194,7 +194,7 @@ def traffic_from_profile(kernel_file, profile_name, key):
 PROFILE_OF = {
     "avgpool": ("avgpool3d.cu", "avgpool3d_k3s2p1_tma.md"),
     "avgpool_nopad": ("avgpool3d.cu", "avgpool3d_k3s2p1_tma.md"),
-    "avgpool_k2": ("avgpool3d.cu", "avgpool3d_win_k2s2.md"),
+    "avgpool_k2": ("avgpool3d.cu", "avgpool3d_k2s2_vec.md"),
     "fused": ("ct3d_pool_tc.cu", "ct3d_pool2_tc_fused.md"),
     "fused_cin8": ("ct3d_pool.cu", "ct3d_pool2_fast_fused_cin8.md"),
     "fused_op1": ("ct3d_pool_tc.cu", "ct3d_pool2_tc_fused.md"),

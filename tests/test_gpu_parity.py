@@ -99,6 +99,18 @@ def test_avgpool_general_windows(k, s, p, cip, ceil):
                  what=f"avgpool {k} {s} {p} {cip} {ceil}")
 
 
+# k2 s2 p0 with whole windows and 16-byte rows: the vectorised pair kernel (odd D and H
+# leave their last plane and row unused; rows of 4 give one pair per row); and the same
+# with rows of 10 (not 16-byte), which takes the unrolled-window kernel
+@pytest.mark.parametrize("shape", [(2, 3, 6, 8, 16), (1, 2, 7, 9, 20), (3, 1, 2, 2, 4),
+                                   (1, 2, 5, 6, 10)])
+def test_avgpool_k2s2_pairs(shape):
+    x, = rng_inputs(4, shape)
+    for cip in (1, 0):
+        y = B.avgpool3d(dev(x), 2, 2, 0, bool(cip))
+        assert_close(y.cpu().numpy(), ora.avgpool3d(x, 2, 2, 0, cip, 0), what=f"avgpool k2 {shape}")
+
+
 def test_avgpool_repeatable_bitwise():
     x = dev(workloads.get(1).with_input_shape((2, 4, 10, 34, 132)).generate("x"))
     a = B.avgpool3d(x, 3, 2, 1)
