@@ -462,9 +462,7 @@ aps_status launch_convt3d_tc(const float *x, const int64_t in[5], const float *w
     using namespace c3t;
     const int64_t N = in[0], Cin = in[1], D = in[2], H = in[3], W = in[4];
     const int64_t Do = out[2], Ho = out[3], Wo = out[4];
-    // a unit spans the input's width when W <= 32 (each output run is then whole
-    // rows, and C_in <= 3 stages them for bulk copies), else a 32-column block
-    // (outputs from registers); the TMA box needs 16-byte rows
+    // the TMA box needs 16-byte rows
     if (Cin < 1 || Cin > CIN_MAX || W % 4 != 0 ||
         reinterpret_cast<uintptr_t>(x) % 16 != 0 || D >= (1 << 30) || H >= (1 << 30) ||
         N * Cin >= (1ll << 31) || N * D >= (1ll << 40))

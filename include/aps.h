@@ -1,8 +1,10 @@
 /*
  * aps.h -- C ABI of the average_pooling_stencil GB300 library (libaps.so).
  *
- * Three fp32 stencil ops on contiguous NC(D)HW / NCL tensors, each computed by
- * hand-written CUDA kernels for sm_103a:
+ * Three fp32 stencil ops on contiguous NC(D)HW / NCL tensors, and the
+ * standalone transposed convolution of the first (aps_convtranspose3d, the
+ * pre-pool tensor of the page's unfused chain), each computed by hand-written
+ * CUDA kernels for sm_103a:
  *
  *   aps_ct3d_scale_pool_bias  ConvTranspose3d -> x scale1 -> AvgPool3d(pool_k)
  *                             -> + bias[c] -> x scale2, fused so that the
@@ -88,7 +90,8 @@ typedef enum {
 /* Precision choices of aps_convtranspose1d. */
 #define APS_PREC_FP32 0   /* fp32 accuracy: max |y - exact| <= 1e-5 * (1 + |exact|);
                              runs as APS_PREC_TF32X3 where that form accepts the shape
-                             (3x the speed at the same bound), else as APS_PREC_FP32_FMA */
+                             (3-4x the speed at the same bound), else as
+                             APS_PREC_FP32_FMA */
 #define APS_PREC_TF32 1   /* tcgen05 tensor cores, tf32 operands, fp32 accumulate;
                              ||y - exact||_F <= 5e-3 * ||exact||_F */
 #define APS_PREC_TF32X3 2 /* tensor cores, each operand split v = hi + lo (tf32) and
@@ -114,8 +117,11 @@ const char *aps_status_string(int status);
  * x: [N, C, D, H, W] device fp32.  y: [N, C, Do, Ho, Wo] device fp32 (shape
  * from aps_avgpool3d_out_shape).  Requires k >= 1, s >= 1, 0 <= 2p <= k.
  * Fast path: k = 3, s = 2, p = 1 in all dims, floor mode, count_include_pad
- * on or off, W % 4 == 0, x 16-byte and y 8-byte aligned (TMA-tiled kernel);
- * every other valid request runs a direct-window kernel.
+ * on or off, W % 4 == 0, x 16-byte and y 8-byte aligned (TMA-tiled kernel).
+ * k = 2, s = 2, p = 0 with whole windows, W % 4 == 0, x 16-byte and y 8-byte
+ * aligned: a vectorised kernel (two outputs per thread).  Other cubic windows
+ * of 2 or 3: an unrolled window kernel; every other valid request: a
+ * direct-window kernel.
  */
 aps_status aps_avgpool3d_out_shape(const int64_t in_ncdhw[5], const int k[3],
                                    const int stride[3], const int pad[3],
@@ -179,10 +185,10 @@ aps_status aps_ct3d_scale_pool_bias(const float *x, const int64_t in_ncdhw[5],
  * C_out = 16, 1 <= C_in <= 8, W % 4 == 0 and x 16-byte aligned (per-parity
  * tap sets, TMA-staged input): on the tensor cores as 3xTF32 (each operand
  * split v = hi + lo, each product summed as lo*hi + hi*lo + hi*hi in fp32),
- * meeting max |y - exact| <= 1e-5 * (1 + |exact|); where the tensor-core
- * kernel cannot run (its shared memory or tensor memory unavailable), on the
- * FP32 pipe at the same bound.  Every other valid request runs a
- * direct per-output kernel.
+ * meeting max |y - exact| <= 1e-5 * (1 + |exact|).  Every other valid
+ * request, and a fast-path one whose tensor-core kernel cannot be made
+ * resident (shared memory or tensor memory unavailable), runs a direct
+ * per-output kernel on the FP32 pipe at the same bound.
  */
 aps_status aps_convtranspose3d_out_shape(const int64_t in_ncdhw[5], int64_t c_out,
                                          const int k[3], const int stride[3],
