@@ -41,6 +41,7 @@ EXPORTS = [
     "aps_convtranspose3d_out_shape", "aps_convtranspose3d",
     "aps_convtranspose1d_out_shape", "aps_convtranspose1d", "aps_device_status",
     "aps_fp32_fma_probe", "aps_debug_fail_launches", "aps_debug_stall_next_pool",
+    "aps_debug_skip_tensor_cores",
 ]
 
 _lib = None
@@ -88,9 +89,11 @@ def lib():
         L.aps_debug_fail_launches.restype = None
         L.aps_debug_stall_next_pool.argtypes = [ctypes.c_ulonglong]
         L.aps_debug_stall_next_pool.restype = None
+        L.aps_debug_skip_tensor_cores.argtypes = [ctypes.c_int]
+        L.aps_debug_skip_tensor_cores.restype = None
         for name in EXPORTS:
             if name not in ("aps_status_string", "aps_abi_version", "aps_debug_fail_launches",
-                            "aps_debug_stall_next_pool"):
+                            "aps_debug_stall_next_pool", "aps_debug_skip_tensor_cores"):
                 getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -191,6 +194,12 @@ def aps_debug_stall_next_pool(wait_limit_ns: int) -> None:
     """Test hook: the next TMA-path avgpool launch withholds one input box and its
     waits give up after wait_limit_ns (0 clears)."""
     lib().aps_debug_stall_next_pool(int(wait_limit_ns))
+
+
+def aps_debug_skip_tensor_cores(on: bool) -> None:
+    """Test hook: while on, every op passes over its tensor-core kernels (its FP32-pipe
+    fallbacks run; explicit tf32 / 3xTF32 ConvTranspose1d requests are refused)."""
+    lib().aps_debug_skip_tensor_cores(int(bool(on)))
 
 
 def aps_fp32_fma_probe(packed, blocks, iters, sink_ptr, stream=0) -> int:

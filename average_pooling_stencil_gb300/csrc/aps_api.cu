@@ -137,6 +137,9 @@ bool encode_tiled(CUtensorMap *map, CUtensorMapDataType type, uint32_t rank, voi
 
 // Launches still to report as rejected (aps_debug_fail_launches).
 static std::atomic<int> g_fail_launches{0};
+// Set: dispatch passes over the tensor-core kernels (aps_debug_skip_tensor_cores).
+static std::atomic<int> g_skip_tc{0};
+static bool tensor_cores_on() { return g_skip_tc.load(std::memory_order_relaxed) == 0; }
 
 aps_status launch_status(cudaError_t launch_result) {
     if (launch_result != cudaSuccess) {
@@ -322,8 +325,10 @@ aps_status aps_ct3d_scale_pool_bias(const float *x, const int64_t in[5], const f
     for (int i = 0; i < 3; ++i)
         fast = fast && k[i] == 3 && s[i] == 2 && p[i] == 1 && op[i] <= 1 && d[i] == 1;
     if (fast) {
-        // tensor cores (C_in <= 3, 16-byte input rows), else the FP32-pipe kernel
-        st = launch_ct3d_pool2_tc(x, in, w, conv_bias, bias, scale1, scale2, y, out, cs);
+        // tensor cores (16-byte input rows), else the FP32-pipe kernel
+        st = tensor_cores_on()
+            ? launch_ct3d_pool2_tc(x, in, w, conv_bias, bias, scale1, scale2, y, out, cs)
+            : APS_ERR_UNSUPPORTED;
         if (st != APS_ERR_UNSUPPORTED) return st;
         st = launch_ct3d_pool2_fast(x, in, w, conv_bias, bias, scale1, scale2, y, out, cs);
         if (st != APS_ERR_UNSUPPORTED) return st;
@@ -372,7 +377,7 @@ aps_status aps_convtranspose3d(const float *x, const int64_t in[5], const float 
     bool fast = c_out == 16 && in[1] >= 1 && in[1] <= 8;
     for (int i = 0; i < 3; ++i)
         fast = fast && k[i] == 3 && s[i] == 2 && p[i] == 1 && d[i] == 1 && op[i] <= 1;
-    if (fast) {
+    if (fast && tensor_cores_on()) {
         // tensor cores (16-byte input rows)
         st = launch_convt3d_tc(x, in, w, bias, y, out, cs);
         if (st != APS_ERR_UNSUPPORTED) return st;
@@ -416,9 +421,9 @@ aps_status aps_convtranspose1d(const float *x, const int64_t in[3], const float 
     // no input channels: every output is its bias (exact at any precision)
     if (in[1] == 0) return launch_convt1d_direct(x, in, w, bias, c_out, k, s, p, d, y, out[2], cs);
     if (precision == APS_PREC_TF32 || precision == APS_PREC_TF32X3)
-        return launch_convt1d_tf32(x, in, w, bias, c_out, k, s, p, d, y, out[2],
+        return !tensor_cores_on() ? APS_ERR_UNSUPPORTED : launch_convt1d_tf32(x, in, w, bias, c_out, k, s, p, d, y, out[2],
                                    precision == APS_PREC_TF32X3, cs);
-    if (precision == APS_PREC_FP32) {
+    if (precision == APS_PREC_FP32 && tensor_cores_on()) {
         // fp32 accuracy: 3xTF32 on the tensor cores where the shape allows
         st = launch_convt1d_tf32(x, in, w, bias, c_out, k, s, p, d, y, out[2], true, cs);
         if (st != APS_ERR_UNSUPPORTED) return st;
@@ -452,4 +457,8 @@ aps_status aps_device_status(unsigned int *bits, int clear) {
 
 extern "C" void aps_debug_fail_launches(int n) {
     aps::g_fail_launches.store(n > 0 ? n : 0, std::memory_order_relaxed);
+}
+
+extern "C" void aps_debug_skip_tensor_cores(int on) {
+    aps::g_skip_tc.store(on ? 1 : 0, std::memory_order_relaxed);
 }

@@ -259,6 +259,16 @@ aps_status aps_fp32_fma_probe(int packed, int blocks, int iters, float *sink,
  * callers see it.  Host-only, thread-safe. */
 void aps_debug_fail_launches(int n);
 
+/* Test hook for the fallback kernels (not part of any op): while on != 0,
+ * every entry point passes over its tensor-core kernels, as if they could not
+ * be made resident on this device -- the fused op and aps_convtranspose3d then
+ * run their FP32-pipe kernels, aps_convtranspose1d with APS_PREC_FP32 runs as
+ * APS_PREC_FP32_FMA, and APS_PREC_TF32 / APS_PREC_TF32X3 return
+ * APS_ERR_UNSUPPORTED.  Results stay within each op's stated bound.  Lets a
+ * test reach the fallbacks on shapes the tensor cores take.  Host-only,
+ * process-wide, thread-safe; on = 0 restores the normal dispatch. */
+void aps_debug_skip_tensor_cores(int on);
+
 /* Test hook for a wait that runs out (not part of any op): the next
  * aps_avgpool3d launch that takes the TMA-tiled kernel withholds the first
  * input box of its first CTA -- the box's barrier still expects its bytes --

@@ -219,18 +219,62 @@ def test_fused_unaligned_input_takes_the_fp32_kernel():
     assert_close(y.cpu().numpy(), fused_ref(base, x, w, cb, b), what="fused unaligned x")
 
 
+class skip_tensor_cores:
+    """Within the block every op passes over its tensor-core kernels (the library's test
+    hook), so that its FP32-pipe fallbacks run on shapes the tensor cores take."""
+
+    def __enter__(self):
+        B.aps_debug_skip_tensor_cores(True)
+
+    def __exit__(self, *exc):
+        B.aps_debug_skip_tensor_cores(False)
+
+
+FUSED_FAST = dict(stride=(2, 2, 2), pad=(1, 1, 1), out_pad=(0, 0, 0), dil=(1, 1, 1), pool_k=2,
+                  scale1=0.5, scale2=1.0)
+
+
+def fused_fast_ref(x, w, cb, b, op=(0, 0, 0)):
+    return ora.ct3d_scale_pool_bias(x, w, cb, b, (2, 2, 2), (1, 1, 1), op, (1, 1, 1), 2, 0.5, 1.0)
+
+
 # many small units: every CTA of the FP32-pipe kernel's persistent grid takes several, so
 # its double-buffered input ring goes round (and its barrier phases flip) many times; W = 4
-# stages the input by TMA, W = 5 by element copies
+# stages the input by TMA (the tensor cores passed over), W = 5 by element copies
 @pytest.mark.parametrize("shape", [(80, 5, 33, 3, 4), (80, 4, 33, 3, 5)])
 def test_fused_fp32_kernel_many_units_per_cta(shape):
     x, = rng_inputs(45, shape)
     w, cb, b = rng_inputs(46, (shape[1], 16, 3, 3, 3), (16,), (16,), lo=-0.2, hi=0.2)
-    prm = dict(stride=(2, 2, 2), pad=(1, 1, 1), out_pad=(0, 0, 0), dil=(1, 1, 1), pool_k=2,
-               scale1=0.5, scale2=1.0)
-    ref = ora.ct3d_scale_pool_bias(x, w, cb, b, (2, 2, 2), (1, 1, 1), (0, 0, 0), (1, 1, 1), 2,
-                                   0.5, 1.0)
-    assert_close(fused_gpu(x, w, cb, b, prm), ref, what=f"fused fp32 many units {shape}")
+    with skip_tensor_cores():
+        got = fused_gpu(x, w, cb, b, FUSED_FAST)
+    assert_close(got, fused_fast_ref(x, w, cb, b), what=f"fused fp32 many units {shape}")
+
+
+# the FP32-pipe kernel on shapes the tensor cores take (16-byte rows): C_in 1..8, whole
+# rows of 32 and a 36-column window, ragged row blocks, output padding
+@pytest.mark.parametrize("shape,op", [((2, 3, 4, 8, 32), (0, 0, 0)), ((1, 8, 3, 33, 36), (1, 1, 0)),
+                                      ((2, 1, 3, 9, 12), (0, 1, 1)), ((1, 6, 5, 6, 20), (1, 0, 1))])
+def test_fused_fp32_fallback_on_tensor_core_shapes(shape, op):
+    x, = rng_inputs(49, shape)
+    w, cb, b = rng_inputs(50, (shape[1], 16, 3, 3, 3), (16,), (16,), lo=-0.2, hi=0.2)
+    with skip_tensor_cores():
+        got = fused_gpu(x, w, cb, b, dict(FUSED_FAST, out_pad=op))
+    assert_close(got, fused_fast_ref(x, w, cb, b, op), what=f"fused fp32 fallback {shape} op {op}")
+
+
+# C_in 4..8 on the tensor cores: each tile's product in chunks of <= 3 channels through two
+# alternating A slots (2 chunks for C_in 4..6, 3 for 7..8).  Whole rows of 32 (3 stages at
+# C_in 8), a 36-column window in two column blocks, ragged row blocks, output padding, and
+# many units per CTA (the stage ring and the slot barriers go round many times)
+@pytest.mark.parametrize("shape,op", [
+    ((3, 4, 5, 9, 12), (0, 0, 0)), ((2, 5, 4, 40, 36), (0, 0, 0)), ((1, 7, 3, 33, 64), (1, 1, 1)),
+    ((2, 8, 6, 32, 32), (0, 0, 0)), ((2, 8, 3, 9, 32), (1, 1, 1)), ((1, 6, 2, 17, 8), (0, 1, 0)),
+    ((160, 8, 9, 3, 4), (0, 0, 0)), ((96, 5, 9, 3, 8), (1, 0, 1))])
+def test_fused_tensor_core_chunked_channels(shape, op):
+    x, = rng_inputs(51, shape)
+    w, cb, b = rng_inputs(52, (shape[1], 16, 3, 3, 3), (16,), (16,), lo=-0.2, hi=0.2)
+    got = fused_gpu(x, w, cb, b, dict(FUSED_FAST, out_pad=op))
+    assert_close(got, fused_fast_ref(x, w, cb, b, op), what=f"fused chunked {shape} op {op}")
 
 
 def test_fused_without_conv_bias_and_other_scales():
@@ -336,16 +380,27 @@ def test_convt3d_cases(xs, cout, k, s, p, d, op, has_bias):
                  what=f"convt3d {xs} k{k} s{s} p{p} d{d} op{op}")
 
 
-# ~1500 units, several per CTA of the persistent grids, so the input rings wrap many
-# times: C_in 8 at W 4 (tensor cores, outputs from registers), C_in 3 and 8 at W 36 (the
-# FP32-pipe kernel)
+# ~1500 units, several per CTA of the persistent grid, so the input ring wraps many
+# times: C_in 8 at W 4 (outputs from registers), C_in 3 and 8 at W 36 (units of 2 rows of
+# up to 64 columns; staged runs for C_in 3)
 @pytest.mark.parametrize("xs", [(48, 8, 16, 3, 4), (24, 3, 16, 3, 36), (12, 8, 16, 3, 36)])
-def test_convt3d_fp32_kernel_many_units_per_cta(xs):
+def test_convt3d_many_units_per_cta(xs):
     x, = rng_inputs(47, xs)
     w, b = rng_inputs(48, (xs[1], 16, 3, 3, 3), (16,), lo=-0.3, hi=0.3)
     args = ((2, 2, 2), (1, 1, 1), (1, 1, 1), (0, 0, 0))
     y = B.convtranspose3d(dev(x), dev(w), dev(b), *args)
     assert_close(y.cpu().numpy(), ora.convt(x, w, b, *args), what=f"convt3d many units {xs}")
+
+
+# the direct kernel on shapes the tensor cores take (the tensor cores passed over)
+@pytest.mark.parametrize("xs,op", [((2, 3, 3, 8, 16), (0, 0, 0)), ((1, 8, 2, 5, 36), (1, 1, 1))])
+def test_convt3d_direct_fallback_on_tensor_core_shapes(xs, op):
+    x, = rng_inputs(53, xs)
+    w, b = rng_inputs(54, (xs[1], 16, 3, 3, 3), (16,), lo=-0.3, hi=0.3)
+    args = ((2, 2, 2), (1, 1, 1), (1, 1, 1), op)
+    with skip_tensor_cores():
+        y = B.convtranspose3d(dev(x), dev(w), dev(b), *args)
+    assert_close(y.cpu().numpy(), ora.convt(x, w, b, *args), what=f"convt3d direct fallback {xs}")
 
 
 def test_convt3d_unaligned_input_takes_the_direct_kernel():
@@ -563,6 +618,25 @@ def test_convt1d_tf32_cases(s, K, d, p, op, cin, cout, L, has_bias):
                           precision=B.APS_PREC_TF32)
     assert_frobenius(y.cpu().numpy(), ora.convt(x, w, b, s, p, d, op),
                      what=f"tf32 s{s} K{K} d{d} p{p} op{op} {cin}->{cout} L{L}")
+
+
+def test_convt1d_with_tensor_cores_passed_over():
+    """With the tensor cores passed over, APS_PREC_FP32 on a shape 3xTF32 takes runs the
+    FP32-pipe kernel (the same bits as APS_PREC_FP32_FMA), and the explicit tensor-core
+    precisions are refused without a launch."""
+    x, = rng_inputs(55, (2, 32, 400))
+    w, b = rng_inputs(56, (32, 64, 5), (64,), lo=-0.3, hi=0.3)
+    args = (dev(x), dev(w), dev(b), 1, 0, 3, 0)
+    with skip_tensor_cores():
+        y = B.convtranspose1d(*args, precision=B.APS_PREC_FP32)
+        for prec in (B.APS_PREC_TF32, B.APS_PREC_TF32X3):
+            with pytest.raises(B.ApsError) as e:
+                B.convtranspose1d(*args, precision=prec)
+            assert e.value.status == B.APS_ERR_UNSUPPORTED
+    fma = B.convtranspose1d(*args, precision=B.APS_PREC_FP32_FMA)
+    assert torch.equal(y, fma)
+    assert_close(y.cpu().numpy(), ora.convt(x, w, b, 1, 0, 3, 0), what="convt1d fp32 fallback")
+    assert not torch.equal(B.convtranspose1d(*args, precision=B.APS_PREC_FP32), fma)
 
 
 # 3xTF32 (APS_PREC_TF32X3): the fp32 elementwise bound, on the tensor cores
