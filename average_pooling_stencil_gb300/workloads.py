@@ -17,15 +17,21 @@ Each workload mirrors one task traced on the Kimi-K2.6 pages:
 Initialiser bounds are the usual 1/sqrt(fan) uniform ones: fan = C_out*prod(k)
 for the transposed-conv weights (432 = 16*27, 320 = 64*5, 256 = 64*4).
 
-Variants that send the same ops down their other kernels (measured beside
-the workloads above):
+Variants that send the same ops down their other kernels or code paths
+(measured beside the workloads above):
   * ``fused_cin8`` / ``convt3d_cin8`` -- the fused op and the standalone
-    ConvTranspose3d with 8 input channels (the FP32-pipe kernels).
+    ConvTranspose3d with 8 input channels (the fused op's product in channel
+    chunks; the ConvTranspose3d outputs stored from registers).
   * ``fused_op1``  -- the fused op with output_padding 1 (pre-pool
-    [32,64,64], pooled [16,32,32]): a geometry only the general kernel serves.
+    [32,64,64], pooled [16,32,32]; the last pooled position of each dim
+    reads one input past the end as zero).
+  * ``fused_k4``   -- the fused op with 4-tap kernels (a general geometry:
+    the tiled 3x3x3 form of the general kernel).
+  * ``convt3d_w64`` -- the standalone ConvTranspose3d on rows of 64 (units of
+    two input rows).
   * ``avgpool_nopad`` -- the avgpool workload with count_include_pad off.
   * ``avgpool_k2``    -- AvgPool3d(k2, s2, p0), the pool of l2_p50's chain,
-    alone on the avgpool workload's input (the general pool kernel).
+    alone on the avgpool workload's input (the vectorised k2 s2 kernel).
 """
 from __future__ import annotations
 

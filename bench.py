@@ -196,7 +196,7 @@ PROFILE_OF = {
     "avgpool_nopad": ("avgpool3d.cu", "avgpool3d_k3s2p1_tma.md"),
     "avgpool_k2": ("avgpool3d.cu", "avgpool3d_k2s2_vec.md"),
     "fused": ("ct3d_pool_tc.cu", "ct3d_pool2_tc_fused.md"),
-    "fused_cin8": ("ct3d_pool.cu", "ct3d_pool2_fast_fused_cin8.md"),
+    "fused_cin8": ("ct3d_pool_tc.cu", "ct3d_pool2_tc_chunked_cin8.md"),
     "fused_op1": ("ct3d_pool_tc.cu", "ct3d_pool2_tc_fused.md"),
     "fused_k4": ("ct3d_pool_gen.cu", "ct3d_pool_gen_k4.md"),
     "convt1d": ("convt1d.cu", "convt1d_tiled_fp32.md"),
@@ -345,6 +345,7 @@ class GpuCase:
             self.d[n] = h.to(dev, non_blocking=False)
         x = self.d["x"]
         self.tc = False
+        self.chunked = False
         self.tensor_passes = 0
         if wl.op == "avgpool3d":
             st, oshape = aps.binding.aps_avgpool3d_out_shape(x.shape, p["k"], p["stride"],
@@ -371,9 +372,11 @@ class GpuCase:
                                           p["stride"][i], p["pad"][i], p["dil"][i],
                                           p["pool_k"])
                 self.flops = 2 * x.shape[0] * cin * p["c_out"] * cells
-            # C_in <= 3 with 16-byte input rows runs on the tensor cores (3xTF32,
-            # three MMA passes), bound by HBM; otherwise on the FP32 pipe
-            self.tc = fast and cin <= 3 and x.shape[4] % 4 == 0
+            # 16-byte input rows run on the tensor cores (3xTF32, three MMA passes;
+            # C_in 4..8 in chunks of <= 3 channels), bound by HBM; otherwise on the
+            # FP32 pipe
+            self.tc = fast and x.shape[4] % 4 == 0
+            self.chunked = self.tc and cin > 3
             self.tensor_passes = 3 if self.tc else 0
             self.bound = "hbm" if self.tc else "hbm+alu"
         elif wl.op == "convtranspose3d":
@@ -864,7 +867,8 @@ def run_native(args):
     clocks = sampler.summary(t_wall0, t_wall1)
     roof = roofline_for(case, per_launch, peaks, peak_src, clocks.get("sm_mhz"))
     kernel_of = {"avgpool3d": "avgpool3d_k3s2p1_tma_kernel",
-                 "ct3d_scale_pool_bias": ("ct3d_pool2_tc_kernel" if case.tc
+                 "ct3d_scale_pool_bias": ("ct3d_pool2_tc_chunked_kernel" if case.chunked
+                                          else "ct3d_pool2_tc_kernel" if case.tc
                                           else "ct3d_pool2_fast_kernel"),
                  "convtranspose3d": "convt3d_tc_kernel" if case.tc else "convt3d_direct_kernel",
                  "convtranspose1d": ("convt1d_tiled_kernel" if case.kind == 3

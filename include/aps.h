@@ -147,10 +147,12 @@ aps_status aps_avgpool3d(const float *x, const int64_t in_ncdhw[5], const int k[
  * (zero past the input's end, which only the last pooled position of a dim with
  * out_pad 1 reaches) with 8 collapsed weights per (ci, co) plus a folded bias (the page's
  * grouping of the 27 taps by input neighbour), computed in one kernel whose
- * CTAs collapse the weights themselves.  With C_in <= 3, W % 4 == 0 and x
- * 16-byte aligned that kernel runs the correlation on the tensor cores as
- * 3xTF32 (each operand split v = hi + lo, each product summed as lo*hi + hi*lo
- * + hi*hi in fp32); otherwise on the FP32 pipe.  Both meet
+ * CTAs collapse the weights themselves.  With W % 4 == 0 and x 16-byte
+ * aligned that kernel runs the correlation on the tensor cores as 3xTF32
+ * (each operand split v = hi + lo, each product summed as lo*hi + hi*lo +
+ * hi*hi in fp32; C_in 4..8 in chunks of up to 3 input channels); otherwise,
+ * or where the tensor-core kernel cannot be made resident, on the FP32 pipe.
+ * Both meet
  * max |y - exact| <= 1e-5 * (1 + |exact|).  Every other valid geometry runs on
  * per-phase collapsed weights while its per-dim phase tables fit (at most 8
  * phases and 8 input offsets per phase per dim, at most 32 taps per dim, at
