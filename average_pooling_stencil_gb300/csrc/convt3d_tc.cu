@@ -21,7 +21,7 @@
 // 1, 2 or 4 warps of a group) -- outputs: planes 2md, 2md+1, twice the unit's rows,
 // all columns -- or, for rows wider than 128, a 128-column block of one row (box
 // origin 128*mwb, 128-byte aligned), whose outputs leave straight from registers.
-// CTA-local unit k goes to group k % 2 and stage k % 8 of a ring the TMA
+// CTA-local unit k goes to group k % 2 and stage k % nst of a ring the TMA
 // warp fills (one 4-D box per unit: C_in x 2 planes x (rows + 1) x (columns + 1,
 // rounded up to 4), zero-filled outside the tensor).  Warp q of a group owns
 // tensor-memory lanes 32q..32q+31, one position of the unit per lane.  Per
@@ -40,9 +40,11 @@
 // issued and frees the tensor memory.
 // C_in 4..8: the A row grows to 16*C_in columns (the accumulator then starts
 // at column 128 of the group's 256) and B to 8 KB per input channel, so the
-// staging blocks no longer fit beside the ring: the epilogue writes each
-// thread's outputs straight from registers instead (for each channel, its two
-// r_w outputs; a warp's 32 lanes cover 64 consecutive outputs of one row).
+// staging blocks fit only beside a shorter input ring (the launcher takes the
+// most stages that fit, down to one per group).  Where they do not fit at all,
+// and for blocks of wider rows, the epilogue writes each thread's outputs
+// straight from registers (for each channel, its two r_w outputs; a warp's 32
+// lanes cover 64 consecutive outputs of one row).
 #include <algorithm>
 #include <cstring>
 
@@ -62,7 +64,7 @@ constexpr int THREADS = 32 * (WORKERS + 1);   // 288
 // A unit is 128 input positions: 4 rows of up to 32 columns, 2 of up to 64 or 1 of
 // up to 128 (lgw = 0, 1, 2: each input row spread over 1 << lgw warps of a group),
 // or a 128-column block of a wider row.
-constexpr int STAGES = 4 * GROUPS;         // input ring: four units in flight per group
+constexpr int STAGES = 4 * GROUPS;         // input ring: up to four units in flight per group
 constexpr int TMEM_COLS = 512;
 constexpr int GROUP_COLS = TMEM_COLS / GROUPS;   // 256
 // accumulator: 128 columns after A hi + lo (16 * C_in columns)
@@ -78,12 +80,12 @@ constexpr int OFF_BIAS = 448;              // float [16]
 constexpr int OFF_B = 512;                 // B, hi then lo: [C_in][2][128][4] words each
 constexpr int B_CI_BYTES = 2 * NCOL * 16;  // one input channel's K-step of 8: 4096 bytes
 __host__ __device__ constexpr int head_bytes_of(int cin) { return OFF_B + 2 * cin * B_CI_BYTES; }
-// outputs straight from registers (no staging blocks) above 3 input channels
-__host__ __device__ constexpr bool direct_of(int cin) { return cin > 3; }
+constexpr size_t kMaxSmemPerCta = 227 * 1024;   // opt-in dynamic shared memory of one CTA
 static_assert(head_bytes_of(1) % 128 == 0, "stages start 128-byte aligned");
 static_assert(d_col_of(CIN_MAX) >= 16 * CIN_MAX && d_col_of(CIN_MAX) + NCOL <= GROUP_COLS,
               "tile buffer layout");
 static_assert(STAGES % GROUPS == 0, "a group's units always use the same stages");
+// stages of a launch: nst, a multiple of GROUPS in [GROUPS, STAGES]
 
 struct Slot {
     long long n;
@@ -119,20 +121,21 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t *v) {
         : "memory");
 }
 
-// CIN: input channels (1..8).
-template <int CIN>
+// CIN: input channels (1..8); NST: stages of the input ring at compile time (0: the
+// run-time nst)
+template <int CIN, int NST>
 __global__ void __launch_bounds__(c3t::THREADS, 1)
     convt3d_tc_kernel(const __grid_constant__ CUtensorMap xmap, const float *__restrict__ w,
                       const float *__restrict__ bias, float *__restrict__ y, int D, int H, int W,
                       int BW, int Do, int Ho, int Wo, int n_mhb, int n_mwb, int lgw,
-                      int direct_rt, long long n_units, unsigned int *status) {
+                      int direct_rt, int nst, long long n_units, unsigned int *status) {
     pdl_trigger();
     pdl_wait();
     using namespace c3t;
     constexpr int D_COL = d_col_of(CIN), HEAD_BYTES = head_bytes_of(CIN);
-    // outputs from registers: C_in > 3 always, and rows wider than 32 (units of
-    // 32-column blocks, whose runs are not whole rows)
-    const bool DIRECT = direct_of(CIN) || direct_rt;
+    // outputs from registers (the launcher's choice): 128-column blocks of wider
+    // rows, whose runs are not whole rows, and where the staging blocks do not fit
+    const bool DIRECT = direct_rt != 0;
     extern __shared__ __align__(128) unsigned char smraw[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smraw + OFF_FULL);
     uint64_t *empty = reinterpret_cast<uint64_t *>(smraw + OFF_EMPTY);
@@ -145,17 +148,18 @@ __global__ void __launch_bounds__(c3t::THREADS, 1)
     const int MR = 4 >> lgw, XRu = MR + 1, UW = 32 << lgw;   // unit rows, staged rows, width
     const int orows = 2 * MR;                                   // output rows per unit
     const int stage_stride = stage_stride_of(CIN, XRu, BW, UW);
-    float *xs = reinterpret_cast<float *>(smraw + HEAD_BYTES);   // [STAGES][C_in][2][XRu][BW]
+    float *xs = reinterpret_cast<float *>(smraw + HEAD_BYTES);   // [nst][C_in][2][XRu][BW]
     const long long plane = (long long)Ho * Wo;
     const long long cstride = (long long)Do * plane;              // between output channels
     const int ac = (int)(cstride & 3), ap = (int)(plane & 3);
     const int CH = chan_stride_of(Wo, ac, orows), RDS = plane_stride_of(Wo, ac, ap, orows);
-    float *ost = xs + STAGES * stage_stride;                       // [GROUPS][2][16][CH]
+    float *ost = xs + (NST ? NST : nst) * stage_stride;            // [GROUPS][2][16][CH]
+    const uint32_t ust = NST ? (uint32_t)NST : (uint32_t)nst;
     const int stage_floats = CIN * 2 * XRu * BW;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     if (tid == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < (int)ust; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 4);   // the four warps of the unit's group
         }
@@ -194,16 +198,16 @@ __global__ void __launch_bounds__(c3t::THREADS, 1)
 
     if (warp == W_FILL) {
         // -------------------------------------------------- input ring (lane 0)
-        // CTA-local unit k goes to stage k % STAGES, which held unit k - STAGES
-        // of the same group (units alternate between the groups), once that
-        // group is done with it.
+        // CTA-local unit k goes to stage k % nst, which held unit k - nst of
+        // the same group (units alternate between the groups, nst is even),
+        // once that group is done with it.
         if (lane == 0) {
             tma_prefetch_desc(&xmap);
             uint32_t k = 0;
             for (long long u = blockIdx.x; u < n_units; u += gridDim.x, ++k) {
-                const int s = (int)(k % STAGES);
+                const int s = (int)(k % ust);
                 if (*abort_flag) break;
-                if (k >= STAGES && !mbar_wait(&empty[s], ((k - STAGES) / STAGES) & 1u)) {
+                if (k >= ust && !mbar_wait(&empty[s], ((k - ust) / ust) & 1u)) {
                     record_error(status, APS_DEVERR_TIMEOUT);
                     *abort_flag = 1;
                     break;
@@ -224,8 +228,8 @@ __global__ void __launch_bounds__(c3t::THREADS, 1)
                             (int)(n * CIN));
             }
             // the loads in flight land before the CTA exits (the latest of each stage)
-            for (uint32_t j = k > STAGES ? k - STAGES : 0; j < k; ++j)
-                mbar_wait(&full[j % STAGES], (j / STAGES) & 1u);
+            for (uint32_t j = k > ust ? k - ust : 0; j < k; ++j)
+                mbar_wait(&full[j % ust], (j / ust) & 1u);
         }
         __syncwarp();
     } else {
@@ -256,9 +260,10 @@ __global__ void __launch_bounds__(c3t::THREADS, 1)
         for (long long kk = grp;; kk += GROUPS, ++j) {
             const long long u = blockIdx.x + kk * gridDim.x;
             if (u >= n_units) break;
-            const int s = (int)(kk % STAGES);
+            const uint32_t kq = (uint32_t)kk;   // CTA-local unit (< 2^32: the launcher checks)
+            const int s = (int)(kq % ust);
             bool ok = !fail && !(EARLY ? abort_seen : *abort_flag);
-            if (ok && !full_ready && !mbar_wait(&full[s], (uint32_t)(kk / STAGES) & 1u)) {
+            if (ok && !full_ready && !mbar_wait(&full[s], (kq / ust) & 1u)) {
                 record_error(status, APS_DEVERR_TIMEOUT);
                 *abort_flag = 1;
                 ok = false;
@@ -332,8 +337,8 @@ __global__ void __launch_bounds__(c3t::THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
             if (EARLY) {
-                const long long kn = kk + GROUPS;
-                full_ready = mbar_test(&full[kn % STAGES], (uint32_t)(kn / STAGES) & 1u);
+                const uint32_t kn = kq + GROUPS;
+                full_ready = mbar_test(&full[kn % ust], (kn / ust) & 1u);
                 abort_seen = *abort_flag;
             }
 
@@ -475,9 +480,27 @@ aps_status launch_convt3d_tc(const float *x, const int64_t in[5], const float *w
     const int BW = (int)((std::min<int64_t>(W, UW) + 1 + 3) & ~3);
     const int64_t n_mhb = ceil_div(H, (int64_t)MR), n_mwb = ceil_div(W, (int64_t)UW);
     const long long n_units = N * D * n_mhb * n_mwb;
-    // outputs from registers for C_in > 3 and for blocks of wider rows (whose
-    // runs are not whole rows); else staged runs leaving by bulk copies
-    const int direct = direct_of((int)Cin) || n_mwb > 1;
+    const long long grid = std::min<long long>(sm_count(), n_units);
+    if (n_units / grid >= (1ll << 31)) return APS_ERR_UNSUPPORTED;   // CTA-local unit counters
+    // staged runs leaving by bulk copies where the staging blocks fit beside B and
+    // the input ring; outputs from registers for blocks of wider rows (whose runs
+    // are not whole rows) and where the staging does not fit.  The ring has four
+    // stages per group; for C_in > 3 (B of 8 KB per channel) as many as fit beside
+    // the staging, down to one per group (C_in <= 3 keeps its ring at compile time)
+    const int ac = (int)((Do * Ho * Wo) & 3), ap = (int)((Ho * Wo) & 3);
+    const size_t stage_bytes = (size_t)stage_stride_of((int)Cin, MR + 1, BW, UW) * 4;
+    const size_t staging_bytes = (size_t)GROUPS * staging_floats_of((int)Wo, ac, ap, 2 * MR) * 4;
+    auto fits = [&](int ns) {
+        return head_bytes_of((int)Cin) + ns * stage_bytes + staging_bytes <= kMaxSmemPerCta;
+    };
+    int direct = n_mwb > 1, nst = STAGES;
+    if (!direct) {
+        while (Cin > 3 && nst > GROUPS && !fits(nst)) nst -= GROUPS;
+        if (!fits(nst)) {
+            direct = 1;
+            nst = STAGES;
+        }
+    }
     CUtensorMap map;
     const cuuint64_t dims[4] = {(cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)D, (cuuint64_t)(N * Cin)};
     const cuuint64_t strides[3] = {(cuuint64_t)(W * 4), (cuuint64_t)(H * W * 4),
@@ -487,23 +510,19 @@ aps_status launch_convt3d_tc(const float *x, const int64_t in[5], const float *w
     if (!encode_tiled(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(x), dims,
                       strides, box, estr))
         return APS_ERR_UNSUPPORTED;
-    const int ac = (int)((Do * Ho * Wo) & 3), ap = (int)((Ho * Wo) & 3);
-    const size_t smem =
-        (size_t)head_bytes_of((int)Cin) +
-        ((size_t)STAGES * stage_stride_of((int)Cin, MR + 1, BW, UW) +
-         (direct ? 0 : (size_t)GROUPS * staging_floats_of((int)Wo, ac, ap, 2 * MR))) * 4;
+    const size_t smem = head_bytes_of((int)Cin) + nst * stage_bytes + (direct ? 0 : staging_bytes);
     void (*const kerns[CIN_MAX])(const CUtensorMap, const float *, const float *, float *, int,
-                                 int, int, int, int, int, int, int, int, int, int, long long,
+                                 int, int, int, int, int, int, int, int, int, int, int, long long,
                                  unsigned int *) = {
-        convt3d_tc_kernel<1>, convt3d_tc_kernel<2>, convt3d_tc_kernel<3>, convt3d_tc_kernel<4>,
-        convt3d_tc_kernel<5>, convt3d_tc_kernel<6>, convt3d_tc_kernel<7>, convt3d_tc_kernel<8>};
+        convt3d_tc_kernel<1, STAGES>, convt3d_tc_kernel<2, STAGES>, convt3d_tc_kernel<3, STAGES>,
+        convt3d_tc_kernel<4, 0>,      convt3d_tc_kernel<5, 0>,      convt3d_tc_kernel<6, 0>,
+        convt3d_tc_kernel<7, 0>,      convt3d_tc_kernel<8, 0>};
     const auto kern = kerns[Cin - 1];
     // one CTA per SM: each holds all 512 tensor-memory columns
     if (resident_ctas((const void *)kern, THREADS, (int)smem) < 1) return APS_ERR_UNSUPPORTED;
-    const long long grid = std::min<long long>(sm_count(), n_units);
     const cudaError_t e = launch_pdl(kern, dim3((unsigned)grid), dim3(THREADS), smem, st, map, w, bias, y, (int)D, (int)H,
                (int)W, BW, (int)Do, (int)Ho, (int)Wo, (int)n_mhb, (int)n_mwb, lgw, direct,
-               n_units, status_word());
+               nst, n_units, status_word());
     return launch_status(e);
 }
 
