@@ -269,7 +269,9 @@ def test_fused_fp32_fallback_on_tensor_core_shapes(shape, op):
 @pytest.mark.parametrize("shape,op", [
     ((3, 4, 5, 9, 12), (0, 0, 0)), ((2, 5, 4, 40, 36), (0, 0, 0)), ((1, 7, 3, 33, 64), (1, 1, 1)),
     ((2, 8, 6, 32, 32), (0, 0, 0)), ((2, 8, 3, 9, 32), (1, 1, 1)), ((1, 6, 2, 17, 8), (0, 1, 0)),
-    ((160, 8, 9, 3, 4), (0, 0, 0)), ((96, 5, 9, 3, 8), (1, 0, 1))])
+    ((160, 8, 9, 3, 4), (0, 0, 0)), ((96, 5, 9, 3, 8), (1, 0, 1)),
+    # 33 staged rows of 36 columns at C_in 8: a 76 KB stage, so the ring holds two
+    ((1, 8, 2, 33, 36), (0, 0, 0)), ((2, 8, 3, 34, 36), (1, 0, 1))])
 def test_fused_tensor_core_chunked_channels(shape, op):
     x, = rng_inputs(51, shape)
     w, cb, b = rng_inputs(52, (shape[1], 16, 3, 3, 3), (16,), (16,), lo=-0.2, hi=0.2)
@@ -390,6 +392,48 @@ def test_convt3d_many_units_per_cta(xs):
     args = ((2, 2, 2), (1, 1, 1), (1, 1, 1), (0, 0, 0))
     y = B.convtranspose3d(dev(x), dev(w), dev(b), *args)
     assert_close(y.cpu().numpy(), ora.convt(x, w, b, *args), what=f"convt3d many units {xs}")
+
+
+# a seeded sweep over the fast path's shapes: C_in 1..8, ragged sizes, 16-byte rows or not,
+# output padding per dim (every kernel of the fast path, with its ring and block counts)
+def _fused_sweep(n, seed=20261202):
+    r = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        cin = int(r.integers(1, 9))
+        w = int(r.choice([4, 8, 12, 20, 28, 32, 36, 44, 64, 13, 30]))
+        out.append(((int(r.integers(1, 4)), cin, int(r.integers(2, 7)), int(r.integers(2, 40)), w),
+                    tuple(int(v) for v in r.integers(0, 2, 3))))
+    return out
+
+
+@pytest.mark.parametrize("shape,op", _fused_sweep(16))
+def test_fused_fast_path_seeded_sweep(shape, op):
+    x, = rng_inputs(57, shape)
+    w, cb, b = rng_inputs(58, (shape[1], 16, 3, 3, 3), (16,), (16,), lo=-0.2, hi=0.2)
+    got = fused_gpu(x, w, cb, b, dict(FUSED_FAST, out_pad=op))
+    assert_close(got, fused_fast_ref(x, w, cb, b, op), what=f"fused sweep {shape} op {op}")
+
+
+# a seeded sweep over the ConvTranspose3d fast path: C_in 1..8 (the ring depth the staging
+# leaves), widths for units of 4 / 2 / 1 rows and 128-column blocks, 16-byte rows or not
+def _convt3d_sweep(n, seed=20261203):
+    r = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        w = int(r.choice([4, 12, 28, 32, 36, 60, 64, 100, 128, 132, 30, 66]))
+        out.append(((int(r.integers(1, 3)), int(r.integers(1, 9)), int(r.integers(1, 5)),
+                     int(r.integers(1, 12)), w), tuple(int(v) for v in r.integers(0, 2, 3))))
+    return out
+
+
+@pytest.mark.parametrize("xs,op", _convt3d_sweep(12))
+def test_convt3d_fast_path_seeded_sweep(xs, op):
+    x, = rng_inputs(59, xs)
+    w, b = rng_inputs(60, (xs[1], 16, 3, 3, 3), (16,), lo=-0.3, hi=0.3)
+    args = ((2, 2, 2), (1, 1, 1), (1, 1, 1), op)
+    y = B.convtranspose3d(dev(x), dev(w), dev(b), *args)
+    assert_close(y.cpu().numpy(), ora.convt(x, w, b, *args), what=f"convt3d sweep {xs} op {op}")
 
 
 # the direct kernel on shapes the tensor cores take (the tensor cores passed over)
