@@ -43,6 +43,9 @@
 // together, drains what it issued and frees the tensor memory.  The kernel is
 // launched as a programmatic dependent of the one before it on the stream:
 // barrier set-up and the tensor-memory allocation overlap that kernel's tail.
+// That is the kernel for C_in <= 3; C_in 4..8, whose A rows do not fit a tile
+// buffer, runs ct3d_pool2_tc_chunked_kernel below (the same units and groups,
+// each tile's product in chunks of up to 3 input channels).
 #include <algorithm>
 #include <cstring>
 #include <type_traits>
@@ -124,6 +127,32 @@ __device__ __forceinline__ void build_collapsed_b(uint32_t *bop, float *bsm,
     }
 }
 
+// Decodes unit u (a block of up to RB output rows x WB output columns of one
+// (n, od) plane) into slot g and loads its input window -- C_in channels x 2
+// planes from (od, oh0, ow0), zero-filled outside the tensor -- into dst by one
+// 4-D TMA box behind barrier bar.  Issued by one thread.
+__device__ __forceinline__ void fill_unit(UnitSlot &g, uint64_t *bar, float *dst,
+                                          const CUtensorMap *xmap, long long u, int n_owb,
+                                          int n_ohb, int Do, int Ho, int Wo, int RB, int WB,
+                                          int cin, uint32_t bytes) {
+    const int owb = (int)(u % n_owb);
+    long long t = u / n_owb;
+    const int ohb = (int)(t % n_ohb);
+    t /= n_ohb;
+    const int od = (int)(t % Do);
+    const long long n = t / Do;
+    const int oh0 = ohb * RB, ow0 = owb * WB;
+    g.n = n;
+    g.od = od;
+    g.oh0 = oh0;
+    g.ow0 = ow0;
+    g.rows = Ho - oh0 < RB ? Ho - oh0 : RB;
+    g.cols = Wo - ow0 < WB ? Wo - ow0 : WB;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_arrive_expect_tx(bar, bytes);
+    tma_load_4d(dst, xmap, bar, ow0, oh0, od, (int)(n * cin));
+}
+
 // Calls f(std::integral_constant<int, I>) for I = 0 .. N-1, unrolled.
 template <int N, int I = 0, class F>
 __device__ __forceinline__ void static_for(F &&f) {
@@ -168,23 +197,8 @@ __global__ void __launch_bounds__(ctc::THREADS, 1)
 
     // decode unit u into the slot of stage b and load its input window
     auto fill = [&](long long u, int b) {
-        const int owb = (int)(u % n_owb);
-        long long t = u / n_owb;
-        const int ohb = (int)(t % n_ohb);
-        t /= n_ohb;
-        const int od = (int)(t % Do);
-        const long long n = t / Do;
-        const int oh0 = ohb * RB, ow0 = owb * WB;
-        UnitSlot &g = slot[b];
-        g.n = n;
-        g.od = od;
-        g.oh0 = oh0;
-        g.ow0 = ow0;
-        g.rows = Ho - oh0 < RB ? Ho - oh0 : RB;
-        g.cols = Wo - ow0 < WB ? Wo - ow0 : WB;
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive_expect_tx(&full[b], (uint32_t)stage_floats * 4u);
-        tma_load_4d(xs + b * stage_stride, &xmap, &full[b], ow0, oh0, od, (int)(n * CIN));
+        fill_unit(slot[b], &full[b], xs + b * stage_stride, &xmap, u, n_owb, n_ohb, Do, Ho, Wo, RB,
+                  WB, CIN, (uint32_t)stage_floats * 4u);
     };
 
     if (tid == 0) {
@@ -417,23 +431,8 @@ __global__ void __launch_bounds__(ctc::THREADS, 1)
     const uint32_t ust = (uint32_t)nst;
 
     auto fill = [&](long long u, int b) {
-        const int owb = (int)(u % n_owb);
-        long long t = u / n_owb;
-        const int ohb = (int)(t % n_ohb);
-        t /= n_ohb;
-        const int od = (int)(t % Do);
-        const long long n = t / Do;
-        const int oh0 = ohb * RB, ow0 = owb * WB;
-        UnitSlot &g = slot[b];
-        g.n = n;
-        g.od = od;
-        g.oh0 = oh0;
-        g.ow0 = ow0;
-        g.rows = Ho - oh0 < RB ? Ho - oh0 : RB;
-        g.cols = Wo - ow0 < WB ? Wo - ow0 : WB;
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive_expect_tx(&full[b], (uint32_t)stage_floats * 4u);
-        tma_load_4d(xs + b * stage_stride, &xmap, &full[b], ow0, oh0, od, (int)(n * CIN));
+        fill_unit(slot[b], &full[b], xs + b * stage_stride, &xmap, u, n_owb, n_ohb, Do, Ho, Wo, RB,
+                  WB, CIN, (uint32_t)stage_floats * 4u);
     };
 
     if (tid == 0) {
