@@ -122,7 +122,7 @@ def test_shape_queries_agree_with_oracle_sizes():
             assert st == 0 and out == (1, 2, want, want, want), (L, k, s, p, c)
 
 
-FAKE = 0x10000  # never dereferenced: every call below fails validation first
+FAKE = 0x10000  # never dereferenced: every call below returns before any CUDA call
 
 
 def test_null_pointers_rejected():
@@ -171,6 +171,22 @@ def test_empty_tensors_are_noops():
     assert B.aps_ct3d_scale_pool_bias(FAKE, (0, 3, 4, 4, 4), FAKE, 0, FAKE, 16, 3, 2, 1, 0, 1, 2,
                                       0.5, 1.0, FAKE) == B.APS_OK
     assert B.aps_convtranspose1d(FAKE, (0, 2, 8), FAKE, 0, 4, 3, 1, 0, 1, 0, 0, FAKE) == B.APS_OK
+
+
+def test_skip_tensor_cores_hook_refuses_the_explicit_tensor_core_precisions_before_cuda():
+    """With the hook on, APS_PREC_TF32 / APS_PREC_TF32X3 are refused by a host check (no CUDA
+    call: this runs without a GPU); validation still comes first; the hook turns off again."""
+    B.aps_debug_skip_tensor_cores(True)
+    try:
+        for prec in (B.APS_PREC_TF32, B.APS_PREC_TF32X3):
+            assert B.aps_convtranspose1d(FAKE, (1, 32, 64), FAKE, 0, 64, 5, 1, 0, 3, 0, prec,
+                                         FAKE) == B.APS_ERR_UNSUPPORTED
+            assert B.aps_convtranspose1d(0, (1, 32, 64), FAKE, 0, 64, 5, 1, 0, 3, 0, prec,
+                                         FAKE) == B.APS_ERR_NULL
+            assert B.aps_convtranspose1d(FAKE, (0, 32, 64), FAKE, 0, 64, 5, 1, 0, 3, 0, prec,
+                                         FAKE) == B.APS_OK
+    finally:
+        B.aps_debug_skip_tensor_cores(False)
 
 
 def test_tensor_api_requires_cuda_tensors():
