@@ -37,6 +37,9 @@ aps_status launch_status(cudaError_t launch_result);
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Opt-in dynamic shared memory of one CTA on sm_103a (bytes).
+constexpr size_t kMaxSmemPerCta = 227 * 1024;
+
 // Launches `kern` on `st` as a programmatic dependent of the kernel before it
 // on the stream (the kernel calls pdl_wait before touching global memory), so
 // that its launch and on-chip setup overlap the previous kernel's tail.

@@ -853,8 +853,8 @@ aps_status launch_convt1d_tf32(const float *x, const int64_t in[3], const float 
     // and y and its rows are 16-byte aligned; otherwise by the direct stores
     const int tma_store =
         (s <= 2 && l_out % 4 == 0 && reinterpret_cast<uintptr_t>(y) % 16 == 0) ? 1 : 0;
-    // 227 KB per CTA, less the 1 KB of static shared memory the kernel declares
-    const size_t budget = 227 * 1024 - 1024;
+    // the CTA's shared memory, less the 1 KB of static shared memory the kernel declares
+    const size_t budget = kMaxSmemPerCta - 1024;
     // Deepest pipeline that fits, trying in order: chunks of 32 channels then
     // (split only) 16; 3 converted stages then 2; then, as before, 4 staging
     // slabs if the raw ring can still hold 2 stages, otherwise 2 (for direct

@@ -80,7 +80,6 @@ constexpr int OFF_BIAS = 448;              // float [16]
 constexpr int OFF_B = 512;                 // B, hi then lo: [C_in][2][128][4] words each
 constexpr int B_CI_BYTES = 2 * NCOL * 16;  // one input channel's K-step of 8: 4096 bytes
 __host__ __device__ constexpr int head_bytes_of(int cin) { return OFF_B + 2 * cin * B_CI_BYTES; }
-constexpr size_t kMaxSmemPerCta = 227 * 1024;   // opt-in dynamic shared memory of one CTA
 static_assert(head_bytes_of(1) % 128 == 0, "stages start 128-byte aligned");
 static_assert(d_col_of(CIN_MAX) >= 16 * CIN_MAX && d_col_of(CIN_MAX) + NCOL <= GROUP_COLS,
               "tile buffer layout");

@@ -98,7 +98,6 @@ static_assert(sizeof(UnitSlot) * STAGES <= OFF_BIAS - OFF_SLOT, "slots fit");
 constexpr int CIN_CHUNKED_MAX = 8;
 constexpr int HEAD_BYTES_CHUNKED = OFF_B + 2 * CIN_CHUNKED_MAX * B_CI_BYTES;   // 8576
 static_assert(HEAD_BYTES_CHUNKED % 128 == 0, "stages start 128-byte aligned");
-constexpr size_t kMaxSmemPerCta = 227 * 1024;   // opt-in dynamic shared memory of one CTA
 
 // B = collapsed weights, split hi / lo, K-major: word (ci, kc, co, e) holds
 // Weff[ci][co][tap 4*kc+e] (tap = a*4 + b*2 + c), so that input channel ci is
