@@ -29,6 +29,9 @@ Variants that send the same ops down their other kernels or code paths
     the tiled 3x3x3 form of the general kernel).
   * ``convt3d_w64`` -- the standalone ConvTranspose3d on rows of 64 (units of
     two input rows).
+  * ``fused_w30``  -- the fused op on rows of 30 floats, which are not 16-byte
+    strided: no TMA box can read them, so it takes the FP32-pipe kernel with
+    element copies.
   * ``avgpool_nopad`` -- the avgpool workload with count_include_pad off.
   * ``avgpool_k2``    -- AvgPool3d(k2, s2, p0), the pool of l2_p50's chain,
     alone on the avgpool workload's input (the vectorised k2 s2 kernel).
@@ -144,6 +147,7 @@ WORKLOADS = {
     10: _convt3d("convt3d_cin8", (128, 8, 16, 32, 32), 10),
     11: _fused("fused_k4", (128, 3, 16, 32, 32), 11, k=(4, 4, 4)),
     12: _convt3d("convt3d_w64", (64, 3, 16, 32, 64), 12),
+    13: _fused("fused_w30", (128, 3, 16, 32, 30), 13),
 }
 
 

@@ -199,6 +199,7 @@ PROFILE_OF = {
     "fused_cin8": ("ct3d_pool_tc.cu", "ct3d_pool2_tc_chunked_cin8.md"),
     "fused_op1": ("ct3d_pool_tc.cu", "ct3d_pool2_tc_fused.md"),
     "fused_k4": ("ct3d_pool_gen.cu", "ct3d_pool_gen_k4.md"),
+    "fused_w30": ("ct3d_pool.cu", "ct3d_pool2_fast_fused_w30.md"),
     "convt1d": ("convt1d.cu", "convt1d_tiled_fp32.md"),
     "convt1d_strided": ("convt1d.cu", "convt1d_tiled_fp32.md"),
     "convt1d_tf32": ("convt1d_tc.cu", "convt1d_tf32.md"),
@@ -218,6 +219,7 @@ PER_CONFIG = [
     ("fused_cin8", 6, 0, "rotate"),
     ("fused_op1", 7, 0, "rotate"),
     ("fused_k4", 11, 0, "rotate"),
+    ("fused_w30", 13, 0, "rotate"),
     ("avgpool_nopad", 8, 0, "plain"),
     ("avgpool_k2", 9, 0, "plain"),
     ("convt1d", 3, 3, "plain"),

@@ -79,7 +79,7 @@ def test_workload_output_shapes():
             3: (32, 64, 131084), 4: (16, 64, 131076), 5: (128, 16, 31, 63, 63),
             6: (128, 16, 15, 31, 31), 7: (128, 16, 16, 32, 32), 8: (16, 32, 64, 64, 128),
             9: (16, 32, 64, 64, 128), 10: (128, 16, 31, 63, 63), 11: (128, 16, 16, 32, 32),
-            12: (64, 16, 31, 63, 127)}
+            12: (64, 16, 31, 63, 127), 13: (128, 16, 15, 31, 29)}
     for cfg, shape in want.items():
         wl = workloads.get(cfg)
         p = wl.params
