@@ -158,10 +158,10 @@ def fused_gpu(x, w, cb, b, p):
                                   p["scale1"], p["scale2"]).cpu().numpy()
 
 
-# the tiny and full workloads, and the full one with 8 input channels (the FP32-pipe
-# kernel, cfg 6), with output_padding 1 (cfg 7, the tensor-core kernel) and with 4-tap
-# kernels (cfg 11, the general kernel)
-@pytest.mark.parametrize("cfg", [0, 2, 6, 7, 11])
+# the tiny and full workloads, and the full one with 8 input channels (cfg 6, the
+# tensor-core kernel in channel chunks), with output_padding 1 (cfg 7), with 4-tap kernels
+# (cfg 11, the general kernel) and on rows of 30 floats (cfg 13, the FP32-pipe kernel)
+@pytest.mark.parametrize("cfg", [0, 2, 6, 7, 11, 13])
 def test_fused_workloads_all_outputs(cfg):
     wl = workloads.get(cfg)
     x, w, cb, b = (wl.generate(n) for n in ("x", "w", "conv_bias", "bias"))
